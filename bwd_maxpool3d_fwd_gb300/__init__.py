@@ -1,1 +1,166 @@
-"""3-D max pooling for GB300 (binding added with the CUDA library)."""
+"""3-D max pooling for GB300: Python binding of libmp3d.so.
+
+The functions here carry the names of the C entry points declared in
+``include/mp3d.h`` and only marshal arguments: they take CUDA tensors
+(PyTorch is used for device memory and streams), pass raw device pointers,
+sizes and the current stream to the library, and raise ``MP3DError`` on a
+nonzero status. Every step of the computation runs in the library's CUDA
+kernels; there is no CPU fallback. If the library has not been built, the
+first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmp3d.so")
+
+F32, F16, BF16 = 0, 1, 2
+BWD_AUTO, BWD_GATHER, BWD_ATOMIC = 0, 1, 2
+DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 10: "bwd_disjoint",
+         11: "bwd_overlap_mask", 12: "bwd_overlap_direct", 13: "bwd_atomic"}
+
+_lib = None
+
+
+class MP3DError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({mp3d_status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmp3d.so, with argument types set."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libmp3d.so not found at {LIB_PATH}; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    pi32 = ctypes.POINTER(ctypes.c_int)
+    L.maxpool3d_fwd.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 7 + [vp]
+    L.adaptive_maxpool3d_fwd.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 4 + [vp]
+    L.maxpool3d_bwd.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 11 + [vp, sz, vp]
+    L.maxpool3d_bwd_workspace_bytes.argtypes = [i64] * 5 + [i32, i32]
+    L.maxpool3d_bwd_workspace_bytes.restype = sz
+    L.maxpool3d_fwd_plan.argtypes = [i64] * 5 + [i32] * 7 + [pi32]
+    L.adaptive_maxpool3d_fwd_plan.argtypes = [i64] * 5 + [i32] * 4 + [pi32]
+    L.maxpool3d_bwd_plan.argtypes = [i64] * 5 + [i32] * 11 + [pi32]
+    L.mp3d_status_string.argtypes = [i32]
+    L.mp3d_status_string.restype = ctypes.c_char_p
+    for f in (L.maxpool3d_fwd, L.adaptive_maxpool3d_fwd, L.maxpool3d_bwd, L.maxpool3d_fwd_plan,
+              L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan):
+        f.restype = i32
+    _lib = L
+    return L
+
+
+def mp3d_status_string(status: int) -> str:
+    return lib().mp3d_status_string(status).decode()
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype not in DTYPE_CODE:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, float16, bfloat16 only)")
+    return DTYPE_CODE[t.dtype]
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError("tensors must be CUDA tensors (this library has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (NCDHW)")
+
+
+def _stream(t: torch.Tensor, stream):
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MP3DError(status, where)
+
+
+def pool_out_size(size, kernel, stride):
+    """Output extent per axis for fixed windows without padding: (I - K) // S + 1."""
+    return tuple((i - k) // s + 1 for i, k, s in zip(size, kernel, stride))
+
+
+def maxpool3d_fwd(x, y, idx, kernel, stride, stream=None):
+    """Fixed-window forward into caller-allocated y (x's dtype) and idx (int64)."""
+    _cuda(x, y, idx)
+    N, C, D, H, W = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().maxpool3d_fwd(x.data_ptr(), y.data_ptr(), idx.data_ptr(), N, C, D, H, W,
+                                 *kernel, *stride, _code(x), _stream(x, stream))
+    _check(st, "maxpool3d_fwd")
+
+
+def adaptive_maxpool3d_fwd(x, y, idx, out_size, stream=None):
+    """Adaptive-window forward into caller-allocated y and idx."""
+    _cuda(x, y, idx)
+    N, C, D, H, W = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().adaptive_maxpool3d_fwd(x.data_ptr(), y.data_ptr(), idx.data_ptr(), N, C, D, H,
+                                          W, *out_size, _code(x), _stream(x, stream))
+    _check(st, "adaptive_maxpool3d_fwd")
+
+
+def maxpool3d_bwd_workspace_bytes(in_shape, dtype, algo=BWD_AUTO) -> int:
+    N, C, D, H, W = in_shape
+    return lib().maxpool3d_bwd_workspace_bytes(N, C, D, H, W, DTYPE_CODE[dtype], algo)
+
+
+def maxpool3d_bwd(grad_out, idx, grad_in, kernel=None, stride=None, algo=BWD_AUTO,
+                  workspace=None, stream=None):
+    """Backward into caller-allocated grad_in. kernel/stride None = adaptive windows."""
+    _cuda(grad_out, idx, grad_in, workspace)
+    N, C, D, H, W = grad_in.shape
+    od, oh, ow = grad_out.shape[2:]
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(grad_in.device):
+        st = lib().maxpool3d_bwd(grad_out.data_ptr(), idx.data_ptr(), grad_in.data_ptr(),
+                                 N, C, D, H, W, od, oh, ow, *k, *s, _code(grad_out), algo,
+                                 ws_ptr, ws_bytes, _stream(grad_in, stream))
+    _check(st, "maxpool3d_bwd")
+
+
+def maxpool3d_fwd_plan(in_shape, kernel, stride, dtype) -> str:
+    p = ctypes.c_int(-1)
+    _check(lib().maxpool3d_fwd_plan(*in_shape, *kernel, *stride, DTYPE_CODE[dtype],
+                                    ctypes.byref(p)), "maxpool3d_fwd_plan")
+    return PATHS[p.value]
+
+
+def adaptive_maxpool3d_fwd_plan(in_shape, out_size, dtype) -> str:
+    p = ctypes.c_int(-1)
+    _check(lib().adaptive_maxpool3d_fwd_plan(*in_shape, *out_size, DTYPE_CODE[dtype],
+                                             ctypes.byref(p)), "adaptive_maxpool3d_fwd_plan")
+    return PATHS[p.value]
+
+
+def maxpool3d_bwd_plan(in_shape, out_size, kernel, stride, dtype, algo=BWD_AUTO) -> str:
+    p = ctypes.c_int(-1)
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    _check(lib().maxpool3d_bwd_plan(*in_shape, *out_size, *k, *s, DTYPE_CODE[dtype], algo,
+                                    ctypes.byref(p)), "maxpool3d_bwd_plan")
+    return PATHS[p.value]

@@ -1,0 +1,346 @@
+// C ABI of libmp3d.so: argument checks, shape math, path choice, launch.
+//
+// Every argument error is reported before the first CUDA call, so a bad
+// call touches neither the device nor the buffers. The library allocates
+// nothing and never synchronises; it enqueues on the caller's stream.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+#include "mp3d.h"
+
+using namespace mp3d;
+
+namespace {
+
+constexpr long long kMaxVol = (1LL << 31) - 1;   // per-plane volumes stay int32
+
+int elem_size(int dtype) {
+    switch (dtype) {
+    case MP3D_F32: return 4;
+    case MP3D_F16: return 2;
+    case MP3D_BF16: return 2;
+    default: return 0;
+    }
+}
+
+bool log_enabled() {
+    static int on = -1;
+    if (on < 0) {
+        const char* v = std::getenv("MP3D_LOG");
+        on = (v && *v && std::strcmp(v, "0") != 0) ? 1 : 0;
+    }
+    return on == 1;
+}
+
+const char* path_name(int path) {
+    switch (path) {
+    case MP3D_PATH_NOOP: return "noop";
+    case MP3D_PATH_FWD_GENERIC: return "fwd_generic";
+    case MP3D_PATH_FWD_S2: return "fwd_s2";
+    case MP3D_PATH_FWD_GLOBAL: return "fwd_global";
+    case MP3D_PATH_BWD_DISJOINT: return "bwd_disjoint";
+    case MP3D_PATH_BWD_OVERLAP_MASK: return "bwd_overlap_mask";
+    case MP3D_PATH_BWD_OVERLAP_DIRECT: return "bwd_overlap_direct";
+    case MP3D_PATH_BWD_ATOMIC: return "bwd_atomic";
+    default: return "?";
+    }
+}
+
+void log_path(const char* op, int path, const Geo& g, int dtype) {
+    if (!log_enabled()) return;
+    std::fprintf(stderr,
+                 "mp3d: %s path=%s dtype=%d P=%lld in=%dx%dx%d out=%dx%dx%d %s k=%d,%d,%d s=%d,%d,%d\n",
+                 op, path_name(path), dtype, g.P, g.D, g.H, g.W, g.OD, g.OH, g.OW,
+                 g.adaptive ? "adaptive" : "fixed", g.kd, g.kh, g.kw, g.sd, g.sh, g.sw);
+}
+
+// Number of SMs of the current device (cached per device).
+cudaError_t sm_count(int* out) {
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+int check_dims(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, Geo* g) {
+    if (N < 0 || C < 0 || D < 1 || H < 1 || W < 1) return MP3D_ERR_SHAPE;
+    if (D > kMaxVol || H > kMaxVol || W > kMaxVol) return MP3D_ERR_SHAPE;
+    if (D * H > kMaxVol || D * H * W > kMaxVol) return MP3D_ERR_SHAPE;
+    const long long vol = D * H * W;
+    if (C > 0 && N > (1LL << 62) / C) return MP3D_ERR_SHAPE;
+    const long long P = N * C;
+    if (P > 0 && P > (1LL << 62) / vol) return MP3D_ERR_SHAPE;
+    std::memset(g, 0, sizeof(*g));
+    g->P = P;
+    g->D = (int)D; g->H = (int)H; g->W = (int)W;
+    g->vol = (int)vol;
+    return MP3D_OK;
+}
+
+int set_out(Geo* g, long long od, long long oh, long long ow) {
+    if (od < 1 || oh < 1 || ow < 1) return MP3D_ERR_SHAPE;
+    if (od > kMaxVol || oh > kMaxVol || ow > kMaxVol) return MP3D_ERR_SHAPE;
+    if (od * oh > kMaxVol || od * oh * ow > kMaxVol) return MP3D_ERR_SHAPE;
+    if (g->P > 0 && g->P > (1LL << 62) / (od * oh * ow)) return MP3D_ERR_SHAPE;
+    g->OD = (int)od; g->OH = (int)oh; g->OW = (int)ow;
+    g->ovol = (int)(od * oh * ow);
+    return MP3D_OK;
+}
+
+int fixed_geo(Geo* g, int kd, int kh, int kw, int sd, int sh, int sw) {
+    if (kd < 1 || kh < 1 || kw < 1 || sd < 1 || sh < 1 || sw < 1) return MP3D_ERR_WINDOW;
+    if (kd > g->D || kh > g->H || kw > g->W) return MP3D_ERR_WINDOW;
+    g->adaptive = 0;
+    g->kd = kd; g->kh = kh; g->kw = kw;
+    g->sd = sd; g->sh = sh; g->sw = sw;
+    return set_out(g, (g->D - kd) / sd + 1, (g->H - kh) / sh + 1, (g->W - kw) / sw + 1);
+}
+
+int adaptive_geo(Geo* g, int od, int oh, int ow) {
+    g->adaptive = 1;
+    return set_out(g, od, oh, ow);
+}
+
+// [a, a+na) and [b, b+nb) (bytes) overlap?
+bool overlaps(const void* a, long long na, const void* b, long long nb) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return na > 0 && nb > 0 && pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+bool misaligned(const void* p, int bytes) { return ((uintptr_t)p % (uintptr_t)bytes) != 0; }
+
+// Every window covers the whole plane: a global reduction per plane.
+bool is_global(const Geo& g) {
+    if (g.ovol != 1) return false;
+    if (g.adaptive) return true;
+    return g.kd == g.D && g.kh == g.H && g.kw == g.W;
+}
+
+// Disjoint windows: each input lies in at most one window.
+bool is_disjoint(const Geo& g) {
+    if (g.adaptive) return g.D % g.OD == 0 && g.H % g.OH == 0 && g.W % g.OW == 0;
+    return g.kd <= g.sd && g.kh <= g.sh && g.kw <= g.sw;
+}
+
+// The disjoint gather works on fixed windows: divisible adaptive windows
+// are fixed windows with kernel = stride = input / output.
+Geo as_fixed(const Geo& g) {
+    Geo f = g;
+    if (g.adaptive) {
+        f.adaptive = 0;
+        f.kd = f.sd = g.D / g.OD;
+        f.kh = f.sh = g.H / g.OH;
+        f.kw = f.sw = g.W / g.OW;
+    }
+    return f;
+}
+
+int fwd_path(const Geo& g, int dtype) {
+    if (g.P == 0) return MP3D_PATH_NOOP;
+    if (is_global(g)) return MP3D_PATH_FWD_GLOBAL;
+    if (fwd_s2_supported(g, dtype)) return MP3D_PATH_FWD_S2;
+    return MP3D_PATH_FWD_GENERIC;
+}
+
+int bwd_path(const Geo& g, int algo) {
+    if (g.P == 0) return MP3D_PATH_NOOP;
+    if (algo == MP3D_BWD_ATOMIC) return MP3D_PATH_BWD_ATOMIC;
+    if (is_disjoint(g)) return MP3D_PATH_BWD_DISJOINT;
+    if (bwd_mask_supported(g)) return MP3D_PATH_BWD_OVERLAP_MASK;
+    return MP3D_PATH_BWD_OVERLAP_DIRECT;
+}
+
+int run_fwd(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, cudaStream_t s) {
+    const int path = fwd_path(g, dtype);
+    log_path("fwd", path, g, dtype);
+    if (path == MP3D_PATH_NOOP) return MP3D_OK;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    cudaError_t e;
+    switch (path) {
+    case MP3D_PATH_FWD_GLOBAL: e = launch_fwd_global(x, y, idx, g, dtype, sms, s); break;
+    case MP3D_PATH_FWD_S2: e = launch_fwd_s2(x, y, idx, g, dtype, sms, s); break;
+    default: e = launch_fwd_generic(x, y, idx, g, dtype, sms, s); break;
+    }
+    return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+// Checks shared by both forward entry points once the geometry is known.
+int check_fwd_buffers(const void* x, const void* y, const int64_t* idx, const Geo& g, int dtype) {
+    const int es = elem_size(dtype);
+    if (es == 0) return MP3D_ERR_DTYPE;
+    if (g.P == 0) return MP3D_OK;
+    if (!x || !y || !idx) return MP3D_ERR_NULLPTR;
+    if (misaligned(x, es) || misaligned(y, es) || misaligned(idx, 8)) return MP3D_ERR_ALIGN;
+    const long long nx = g.P * g.vol * es, ny = g.P * g.ovol * es, ni = g.P * g.ovol * 8;
+    if (overlaps(x, nx, y, ny) || overlaps(x, nx, idx, ni) || overlaps(y, ny, idx, ni))
+        return MP3D_ERR_ALIAS;
+    return MP3D_OK;
+}
+
+int bwd_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+            int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype, int algo) {
+    int st = check_dims(N, C, D, H, W, g);
+    if (st) return st;
+    const bool all_zero = !kd && !kh && !kw && !sd && !sh && !sw;
+    if (all_zero) {
+        st = adaptive_geo(g, od, oh, ow);
+    } else {
+        st = fixed_geo(g, kd, kh, kw, sd, sh, sw);
+        if (!st && (g->OD != od || g->OH != oh || g->OW != ow)) st = MP3D_ERR_WINDOW;
+    }
+    if (st) return st;
+    if (elem_size(dtype) == 0) return MP3D_ERR_DTYPE;
+    if (algo < MP3D_BWD_AUTO || algo > MP3D_BWD_ATOMIC) return MP3D_ERR_ALGO;
+    return MP3D_OK;
+}
+
+size_t workspace_needed(const Geo& g, int dtype, int algo) {
+    if (algo != MP3D_BWD_ATOMIC || dtype == MP3D_F32) return 0;
+    return (size_t)(g.P * (long long)g.vol) * sizeof(float);
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+int maxpool3d_fwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int kd, int kh,
+                       int kw, int sd, int sh, int sw, int dtype, int* path) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = fixed_geo(&g, kd, kh, kw, sd, sh, sw);
+    if (!st && elem_size(dtype) == 0) st = MP3D_ERR_DTYPE;
+    if (!st && path) *path = fwd_path(g, dtype);
+    return st;
+}
+
+int adaptive_maxpool3d_fwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od,
+                                int oh, int ow, int dtype, int* path) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = adaptive_geo(&g, od, oh, ow);
+    if (!st && elem_size(dtype) == 0) st = MP3D_ERR_DTYPE;
+    if (!st && path) *path = fwd_path(g, dtype);
+    return st;
+}
+
+int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+                       int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype,
+                       int algo, int* path) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, algo);
+    if (!st && path) *path = bwd_path(g, algo);
+    return st;
+}
+
+int maxpool3d_fwd(const void* x, void* y, int64_t* idx, int64_t N, int64_t C, int64_t D,
+                  int64_t H, int64_t W, int kd, int kh, int kw, int sd, int sh, int sw,
+                  int dtype, cudaStream_t stream) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = fixed_geo(&g, kd, kh, kw, sd, sh, sw);
+    if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
+    if (st) return st;
+    return run_fwd(x, y, idx, g, dtype, stream);
+}
+
+int adaptive_maxpool3d_fwd(const void* x, void* y, int64_t* idx, int64_t N, int64_t C,
+                           int64_t D, int64_t H, int64_t W, int od, int oh, int ow, int dtype,
+                           cudaStream_t stream) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = adaptive_geo(&g, od, oh, ow);
+    if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
+    if (st) return st;
+    return run_fwd(x, y, idx, g, dtype, stream);
+}
+
+size_t maxpool3d_bwd_workspace_bytes(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                                     int dtype, int algo) {
+    Geo g;
+    if (check_dims(N, C, D, H, W, &g)) return 0;
+    if (elem_size(dtype) == 0 || algo < MP3D_BWD_AUTO || algo > MP3D_BWD_ATOMIC) return 0;
+    return workspace_needed(g, dtype, algo);
+}
+
+int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64_t N, int64_t C,
+                  int64_t D, int64_t H, int64_t W, int od, int oh, int ow, int kd, int kh,
+                  int kw, int sd, int sh, int sw, int dtype, int algo, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, algo);
+    if (st) return st;
+    const int es = elem_size(dtype);
+    const size_t need = workspace_needed(g, dtype, algo);
+    if (g.P > 0) {
+        if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
+        if (misaligned(grad_out, es) || misaligned(idx, 8) || misaligned(grad_in, es))
+            return MP3D_ERR_ALIGN;
+        const long long ng = g.P * g.ovol * es, ni = g.P * g.ovol * 8, nin = g.P * g.vol * es;
+        if (overlaps(grad_in, nin, grad_out, ng) || overlaps(grad_in, nin, idx, ni))
+            return MP3D_ERR_ALIAS;
+        if (need > 0) {
+            if (!workspace || workspace_bytes < need || misaligned(workspace, 16))
+                return MP3D_ERR_WORKSPACE;
+            if (overlaps(workspace, (long long)need, grad_in, nin) ||
+                overlaps(workspace, (long long)need, grad_out, ng) ||
+                overlaps(workspace, (long long)need, idx, ni))
+                return MP3D_ERR_ALIAS;
+        }
+    }
+    const int path = bwd_path(g, algo);
+    const Geo gk = (path == MP3D_PATH_BWD_DISJOINT) ? as_fixed(g) : g;
+    log_path("bwd", path, gk, dtype);
+    if (path == MP3D_PATH_NOOP) return MP3D_OK;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    cudaError_t e;
+    switch (path) {
+    case MP3D_PATH_BWD_ATOMIC:
+        e = launch_bwd_atomic(grad_out, idx, grad_in, (float*)workspace, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_DISJOINT:
+        e = launch_bwd_disjoint(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_OVERLAP_MASK:
+        e = launch_bwd_overlap_mask(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    default:
+        e = launch_bwd_overlap_direct(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    }
+    return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+const char* mp3d_status_string(int status) {
+    switch (status) {
+    case MP3D_OK: return "ok";
+    case MP3D_ERR_NULLPTR: return "a required pointer is NULL";
+    case MP3D_ERR_SHAPE: return "invalid size (dimension < 1, N or C < 0, or a volume >= 2^31)";
+    case MP3D_ERR_WINDOW: return "invalid window (kernel or stride < 1, kernel larger than the "
+                                 "input, or output sizes that do not match the window)";
+    case MP3D_ERR_DTYPE: return "unsupported dtype (f32, f16, bf16 only)";
+    case MP3D_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+    case MP3D_ERR_CUDA: return "CUDA launch or device query failed";
+    case MP3D_ERR_ALGO: return "unknown backward algorithm";
+    case MP3D_ERR_ALIGN: return "pointer not aligned to its element size";
+    case MP3D_ERR_ALIAS: return "an output buffer overlaps another buffer";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

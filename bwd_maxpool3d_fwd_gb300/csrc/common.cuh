@@ -1,0 +1,81 @@
+// Device-side helpers shared by the pooling kernels: element types, the
+// max/argmax comparison rule, window geometry and launch bookkeeping.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+namespace mp3d {
+
+// ---------------------------------------------------------------- types
+
+enum Dtype { F32 = 0, F16 = 1, BF16 = 2 };
+
+// Exact widening to float and round-to-nearest-even narrowing.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// "v beats the running maximum m": larger, or a NaN against a number.
+// Equal values (including +0 against -0) do not beat, so the first
+// occurrence in scan order is kept.
+__device__ __forceinline__ bool beats(float v, float m) {
+    return (v != v) ? (m == m) : (v > m);
+}
+
+// ---------------------------------------------------------------- geometry
+
+// Problem geometry as the kernels see it. Per-plane volumes are < 2^31, so
+// in-plane offsets are 32-bit; plane counts and global offsets are 64-bit.
+struct Geo {
+    long long P;          // planes N*C
+    int D, H, W;          // input extent
+    int OD, OH, OW;       // output extent
+    int kd, kh, kw;       // fixed window (unused when adaptive)
+    int sd, sh, sw;
+    int adaptive;         // 1: adaptive windows
+    int vol;              // D*H*W
+    int ovol;             // OD*OH*OW
+};
+
+// Window i along one axis: [start, end).
+__device__ __forceinline__ int win_start(int i, int I, int O, int K, int S, bool adaptive) {
+    return adaptive ? (int)(((long long)i * I) / O) : i * S;
+}
+__device__ __forceinline__ int win_end(int i, int I, int O, int K, int S, bool adaptive) {
+    return adaptive ? (int)(((long long)(i + 1) * I + O - 1) / O) : i * S + K;
+}
+
+// Range [lo, hi] of windows along one axis that contain position x
+// (empty when lo > hi).
+__device__ __forceinline__ int cover_lo(int x, int I, int O, int K, int S, bool adaptive) {
+    if (adaptive) return (int)(((long long)x * O) / I);
+    return x < K ? 0 : (x - K) / S + 1;
+}
+__device__ __forceinline__ int cover_hi(int x, int I, int O, int K, int S, bool adaptive) {
+    if (adaptive) return (int)(((long long)(x + 1) * O - 1) / I);
+    int h = x / S;
+    return h < O - 1 ? h : O - 1;
+}
+
+// ---------------------------------------------------------------- vectors
+
+// Element-wise access to a 16-byte vector of T.
+template <typename T> struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    union { uint4 u; T e[N]; };
+};
+
+}  // namespace mp3d

@@ -1,0 +1,37 @@
+// Launchers shared between the C-ABI layer (api.cu) and the kernel files.
+// Every launcher enqueues on `stream`, returns the cudaError_t of the launch
+// and never synchronises.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mp3d {
+
+// Forward paths (fwd.cu).
+cudaError_t launch_fwd_generic(const void* x, void* y, int64_t* idx, const Geo& g,
+                               int dtype, int sms, cudaStream_t s);
+cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g,
+                              int dtype, int sms, cudaStream_t s);
+cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g,
+                          int dtype, int sms, cudaStream_t s);
+// Whether the stride-2 kernel handles this geometry and type.
+bool fwd_s2_supported(const Geo& g, int dtype);
+
+// Backward paths (bwd.cu). For the disjoint gather, g.kd..g.sw hold the
+// fixed window (adaptive divisible shapes are passed as kernel = stride =
+// input / output).
+cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi,
+                                const Geo& g, int dtype, int sms, cudaStream_t s);
+cudaError_t launch_bwd_overlap_direct(const void* go, const int64_t* idx, void* gi,
+                                      const Geo& g, int dtype, int sms, cudaStream_t s);
+cudaError_t launch_bwd_overlap_mask(const void* go, const int64_t* idx, void* gi,
+                                    const Geo& g, int dtype, int sms, cudaStream_t s);
+// Whether the shared-mask gather handles this geometry.
+bool bwd_mask_supported(const Geo& g);
+cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, float* ws,
+                              const Geo& g, int dtype, int sms, cudaStream_t s);
+
+}  // namespace mp3d

@@ -1,0 +1,165 @@
+/*
+ * mp3d.h: C ABI of libmp3d.so, 3-D max pooling over NCDHW tensors on
+ * NVIDIA GB300 (sm_103a): forward with argmax indices (fixed and adaptive
+ * windows) and the backward that routes each output gradient to its argmax
+ * input.
+ *
+ * Sources (web pages on the subject):
+ *  [MPF]  teenygrad API docs, "Struct Maxpool3dForward": a 3-D max-pooling
+ *         forward pass; Constraints: no padding, OD = (D - KD)/STRIDE_D + 1,
+ *         likewise OH, OW. Its launch-argument tuple (input pointer, output
+ *         pointer, eight i32) is the model for passing plain pointers and
+ *         integer sizes here.
+ *  [AMPB] FlagGems-Experimental PR #308, "Add adaptive_max_pool3d_backward
+ *         Moore Threads specialized operator", Summary: the backward
+ *         scatters each output window's gradient back to its argmax input;
+ *         when every axis divides evenly the windows tile the input and one
+ *         gather launch suffices (no zero pass, no atomics); otherwise
+ *         windows overlap and contributions to one input accumulate (the
+ *         page uses a zero fill and an atomic scatter, kept here as an
+ *         ablation).
+ *
+ * Conventions shared by every entry point
+ *  - Layout: every tensor is dense, contiguous NCDHW. A "plane" is one
+ *    (n, c) slice of D*H*W elements. Outputs are dense [N, C, OD, OH, OW].
+ *  - Indices: int64 flat offsets d*H*W + h*W + w inside the element's own
+ *    plane (not global offsets).
+ *  - Ties: the first occurrence in (d, h, w) row-major order wins; +0 and
+ *    -0 compare equal; a NaN beats every number and the first NaN wins.
+ *    The output value is a bit copy of the winning input element.
+ *  - Ownership: the caller allocates and owns every buffer, including the
+ *    workspace. The library allocates nothing on the device, frees
+ *    nothing, and never synchronises.
+ *  - Pointers: device pointers (or managed memory), aligned to their
+ *    element size. Inputs and outputs must not overlap.
+ *  - Asynchrony: work is enqueued on `stream` (0 = the legacy default
+ *    stream); the call returns after the launch.
+ *  - Errors: argument errors return a nonzero status before any CUDA call,
+ *    with nothing written. A launch failure returns MP3D_ERR_CUDA.
+ *  - Empty input: N*C == 0 is a no-op returning MP3D_OK (other arguments are
+ *    still checked).
+ *  - Limits: D*H*W and OD*OH*OW must each be below 2^31.
+ *  - Types: f32, f16, bf16 only; any other code returns MP3D_ERR_DTYPE
+ *    (there is no fallback).
+ */
+#ifndef MP3D_H
+#define MP3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MP3D_F32 = 0, MP3D_F16 = 1, MP3D_BF16 = 2 } mp3d_dtype;
+
+/* Backward algorithm. AUTO picks the gather (disjoint or overlapping) from
+ * the shape; GATHER forces the deterministic gather; ATOMIC runs the
+ * ablation of [AMPB]'s non-divisible path: zero fill, atomicAdd scatter in
+ * binary32 and, for f16/bf16, a final rounding pass. */
+typedef enum { MP3D_BWD_AUTO = 0, MP3D_BWD_GATHER = 1, MP3D_BWD_ATOMIC = 2 } mp3d_bwd_algo;
+
+typedef enum {
+    MP3D_OK = 0,
+    MP3D_ERR_NULLPTR = 1,    /* a required pointer is NULL                 */
+    MP3D_ERR_SHAPE = 2,      /* a size < 1 (or N, C < 0), or a volume >= 2^31 */
+    MP3D_ERR_WINDOW = 3,     /* kernel/stride < 1, kernel > input, or output
+                                sizes that do not match the window          */
+    MP3D_ERR_DTYPE = 4,      /* dtype not in mp3d_dtype                     */
+    MP3D_ERR_WORKSPACE = 5,  /* workspace missing or too small              */
+    MP3D_ERR_CUDA = 6,       /* a CUDA launch or query failed               */
+    MP3D_ERR_ALGO = 7,       /* algo not in mp3d_bwd_algo                   */
+    MP3D_ERR_ALIGN = 8,      /* a pointer not aligned to its element size   */
+    MP3D_ERR_ALIAS = 9       /* an output overlaps an input or another output */
+} mp3d_status;
+
+/* Kernel paths reported by the *_plan queries (for logging and tests). */
+typedef enum {
+    MP3D_PATH_NOOP = 0,              /* N*C == 0                              */
+    MP3D_PATH_FWD_GENERIC = 1,       /* one thread per output, any window     */
+    MP3D_PATH_FWD_S2 = 2,            /* stride-2 register-column kernel       */
+    MP3D_PATH_FWD_GLOBAL = 3,        /* one window per plane (global pool)    */
+    MP3D_PATH_BWD_DISJOINT = 10,     /* single-pass gather, disjoint windows  */
+    MP3D_PATH_BWD_OVERLAP_MASK = 11, /* overlapping gather via shared masks   */
+    MP3D_PATH_BWD_OVERLAP_DIRECT = 12, /* overlapping gather, direct reads    */
+    MP3D_PATH_BWD_ATOMIC = 13        /* zero fill + atomic scatter ablation   */
+} mp3d_path;
+
+/*
+ * Fixed-window forward [MPF]. x: [N, C, D, H, W]; y: [N, C, OD, OH, OW] of
+ * the same type; idx: int64 [N, C, OD, OH, OW], with
+ * OD = (D - kd)/sd + 1, OH = (H - kh)/sh + 1, OW = (W - kw)/sw + 1
+ * (no padding). y[n,c,od,oh,ow] is the maximum of x over
+ * d in [od*sd, od*sd + kd), h in [oh*sh, oh*sh + kh), w in [ow*sw, ow*sw + kw).
+ * Requires 1 <= k <= input size and s >= 1 on every axis.
+ * idx may be NULL only together with N*C == 0.
+ */
+int maxpool3d_fwd(const void* x, void* y, int64_t* idx,
+                  int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                  int kd, int kh, int kw, int sd, int sh, int sw,
+                  int dtype, cudaStream_t stream);
+
+/*
+ * Adaptive-window forward (the forward of [AMPB]'s operator). Output size
+ * (od, oh, ow) is given, each >= 1 (an output larger than the input is
+ * accepted). Window i along an axis of input size I and output size O is
+ * [floor(i*I/O), ceil((i+1)*I/O)). Buffers as for maxpool3d_fwd.
+ */
+int adaptive_maxpool3d_fwd(const void* x, void* y, int64_t* idx,
+                           int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                           int od, int oh, int ow, int dtype, cudaStream_t stream);
+
+/*
+ * Backward [AMPB]: grad_in[n, c, j] = sum of grad_out[n, c, o] over the
+ * outputs o of that plane whose idx[n, c, o] == j, summed in ascending
+ * (od, oh, ow) order in binary32 (first term as the initial value) and
+ * rounded once to the type; +0 where no output selects j. Every element of
+ * grad_in is written.
+ *
+ * grad_out, idx: [N, C, od, oh, ow]; grad_in: [N, C, D, H, W].
+ * Window: either fixed (kd..sw all >= 1, and (od, oh, ow) must equal the
+ * fixed output sizes) or adaptive (kd..sw all 0; windows derived from
+ * (D, H, W) -> (od, oh, ow)).
+ * Precondition: idx comes from the matching forward (each index lies in its
+ * own window). The gather paths only look at windows that cover an input,
+ * so an index outside its window is ignored; the ATOMIC path drops indices
+ * outside [0, D*H*W).
+ * algo: mp3d_bwd_algo. ATOMIC with f16/bf16 needs a workspace of
+ * maxpool3d_bwd_workspace_bytes(...) bytes (binary32 accumulators, 16-byte
+ * aligned); every other case needs none (workspace may be NULL).
+ */
+int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in,
+                  int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                  int od, int oh, int ow,
+                  int kd, int kh, int kw, int sd, int sh, int sw,
+                  int dtype, int algo, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/* Workspace bytes maxpool3d_bwd needs: 4*N*C*D*H*W for ATOMIC with f16 or
+ * bf16, else 0. Returns 0 for invalid arguments as well. */
+size_t maxpool3d_bwd_workspace_bytes(int64_t N, int64_t C, int64_t D, int64_t H,
+                                     int64_t W, int dtype, int algo);
+
+/* Dispatch queries: validate exactly like the matching entry point, make
+ * no CUDA call, and store the mp3d_path that the call would launch in
+ * *path. Return the status the call would return for its arguments. */
+int maxpool3d_fwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                       int kd, int kh, int kw, int sd, int sh, int sw,
+                       int dtype, int* path);
+int adaptive_maxpool3d_fwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                                int od, int oh, int ow, int dtype, int* path);
+int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                       int od, int oh, int ow,
+                       int kd, int kh, int kw, int sd, int sh, int sw,
+                       int dtype, int algo, int* path);
+
+/* Static description of a status code (never NULL). */
+const char* mp3d_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MP3D_H */

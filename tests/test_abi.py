@@ -1,0 +1,159 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function the header declares, rejects bad arguments before any CUDA call,
+and plans the expected kernel path for each workload."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import bwd_maxpool3d_fwd_gb300 as mp
+from bwd_maxpool3d_fwd_gb300 import build as mp_build
+from bwd_maxpool3d_fwd_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, NULLPTR, SHAPE, WINDOW, DTYPE, WORKSPACE, CUDA, ALGO, ALIGN, ALIAS = range(10)
+
+
+@pytest.fixture(scope="module")
+def L():
+    mp_build.build()
+    return mp.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mp3d.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^(?:int|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_symbols_exported(L):
+    names = header_functions()
+    assert {"maxpool3d_fwd", "adaptive_maxpool3d_fwd", "maxpool3d_bwd"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in mp3d.h but not exported"
+
+
+def test_status_strings(L):
+    for s in range(10):
+        assert mp.mp3d_status_string(s)
+    assert mp.mp3d_status_string(99) == "unknown status"
+
+
+# Host buffers are enough: every call below fails validation before any
+# CUDA call, so no pointer is ever dereferenced.
+@pytest.fixture(scope="module")
+def bufs():
+    a = (ctypes.c_char * 4096)()
+    b = (ctypes.c_char * 4096)()
+    c = (ctypes.c_char * 4096)()
+    return ctypes.addressof(a), ctypes.addressof(b), ctypes.addressof(c), (a, b, c)
+
+
+def fwd(L, x, y, i, N=1, C=1, D=4, H=4, W=4, k=(2, 2, 2), s=(2, 2, 2), dt=0):
+    return L.maxpool3d_fwd(x, y, i, N, C, D, H, W, *k, *s, dt, None)
+
+
+def test_fwd_argument_errors(L, bufs):
+    x, y, i, _ = bufs
+    assert fwd(L, None, y, i) == NULLPTR
+    assert fwd(L, x, None, i) == NULLPTR
+    assert fwd(L, x, y, None) == NULLPTR
+    assert fwd(L, x, y, i, D=0) == SHAPE
+    assert fwd(L, x, y, i, N=-1) == SHAPE
+    assert fwd(L, x, y, i, k=(0, 2, 2)) == WINDOW
+    assert fwd(L, x, y, i, s=(2, 0, 2)) == WINDOW
+    assert fwd(L, x, y, i, k=(5, 2, 2)) == WINDOW
+    assert fwd(L, x, y, i, dt=3) == DTYPE
+    assert fwd(L, x + 1, y, i, dt=1) == ALIGN
+    assert fwd(L, x, y, i + 4) == ALIGN
+    assert fwd(L, x, x + 64, i) == ALIAS
+    assert fwd(L, x, y, y + 8) == ALIAS
+    big = 1 << 11
+    assert fwd(L, x, y, i, D=big, H=big, W=big) == SHAPE          # plane volume >= 2^31
+    # empty input: a no-op (no CUDA call), even with NULL pointers
+    assert fwd(L, None, None, None, N=0) == OK
+    assert fwd(L, None, None, None, C=0, k=(0, 1, 1)) == WINDOW   # still validated
+
+
+def test_adaptive_argument_errors(L, bufs):
+    x, y, i, _ = bufs
+    f = L.adaptive_maxpool3d_fwd
+    assert f(x, y, i, 1, 1, 4, 4, 4, 0, 2, 2, 0, None) == SHAPE
+    assert f(x, y, i, 1, 1, 4, 4, 4, 2, 2, 2, 5, None) == DTYPE
+    assert f(None, y, i, 1, 1, 4, 4, 4, 2, 2, 2, 0, None) == NULLPTR
+    assert f(None, None, None, 0, 3, 4, 4, 4, 9, 9, 9, 0, None) == OK   # O > I accepted
+
+
+def bwd(L, g, i, gi, od=(2, 2, 2), k=(2, 2, 2), s=(2, 2, 2), dt=0, algo=0, ws=None, wsb=0,
+        D=4, H=4, W=4, N=1, C=1):
+    return L.maxpool3d_bwd(g, i, gi, N, C, D, H, W, *od, *k, *s, dt, algo, ws, wsb, None)
+
+
+def test_bwd_argument_errors(L, bufs):
+    g, i, gi, _ = bufs
+    assert bwd(L, None, i, gi) == NULLPTR
+    assert bwd(L, g, i, gi, od=(3, 2, 2)) == WINDOW         # sizes must match the window
+    assert bwd(L, g, i, gi, k=(2, 0, 2)) == WINDOW           # partly adaptive
+    assert bwd(L, g, i, gi, od=(0, 2, 2), k=(0, 0, 0), s=(0, 0, 0)) == SHAPE
+    assert bwd(L, g, i, gi, algo=3) == ALGO
+    assert bwd(L, g, i, gi, dt=9) == DTYPE
+    assert bwd(L, g, i, gi, dt=1, algo=2) == WORKSPACE       # f16 atomic needs binary32 room
+    assert bwd(L, g, i, gi, dt=1, algo=2, ws=g + 2048, wsb=64) == WORKSPACE
+    assert bwd(L, g, i, g + 16) == ALIAS
+
+
+def test_workspace_bytes(L):
+    n = 2 * 3 * 4 * 5 * 6
+    assert L.maxpool3d_bwd_workspace_bytes(2, 3, 4, 5, 6, 1, 2) == 4 * n
+    assert L.maxpool3d_bwd_workspace_bytes(2, 3, 4, 5, 6, 2, 2) == 4 * n
+    assert L.maxpool3d_bwd_workspace_bytes(2, 3, 4, 5, 6, 0, 2) == 0
+    assert L.maxpool3d_bwd_workspace_bytes(2, 3, 4, 5, 6, 1, 0) == 0
+    assert L.maxpool3d_bwd_workspace_bytes(2, 3, 0, 5, 6, 1, 2) == 0
+
+
+def test_stated_output_sizes():
+    for w in workloads.WORKLOADS:
+        if w.mode == "fixed":
+            assert mp.pool_out_size((w.D, w.H, w.W), w.kernel, w.stride) == tuple(w.out)
+
+
+def test_plans_per_workload(L):
+    expect_fwd = {0: {"fwd_generic", "fwd_s2"}, 1: {"fwd_generic", "fwd_s2"},
+                  2: {"fwd_generic", "fwd_s2"},
+                  3: {"fwd_generic", "fwd_s2"}, 4: {"fwd_global"}}
+    expect_bwd = {0: {"bwd_disjoint"}, 1: {"bwd_overlap_mask", "bwd_overlap_direct"},
+                  2: {"bwd_disjoint"}, 3: {"bwd_overlap_mask", "bwd_overlap_direct"},
+                  4: {"bwd_disjoint"}}
+    for n, w in enumerate(workloads.WORKLOADS):
+        if w.mode == "fixed":
+            pf = mp.maxpool3d_fwd_plan(w.in_shape, w.kernel, w.stride, w.dtype)
+            pb = mp.maxpool3d_bwd_plan(w.in_shape, w.out, w.kernel, w.stride, w.dtype)
+        else:
+            pf = mp.adaptive_maxpool3d_fwd_plan(w.in_shape, w.out, w.dtype)
+            pb = mp.maxpool3d_bwd_plan(w.in_shape, w.out, None, None, w.dtype)
+        assert pf in expect_fwd[n], (w.name, pf)
+        assert pb in expect_bwd[n], (w.name, pb)
+        pa = mp.maxpool3d_bwd_plan(w.in_shape, w.out, w.kernel if w.mode == "fixed" else None,
+                                   w.stride if w.mode == "fixed" else None, w.dtype,
+                                   mp.BWD_ATOMIC)
+        assert pa == "bwd_atomic"
+
+
+def test_plan_rules(L):
+    # fixed kernel == input on every axis: a global reduction
+    assert mp.maxpool3d_fwd_plan((2, 2, 3, 4, 5), (3, 4, 5), (1, 1, 1), torch.float32) == "fwd_global"
+    # kernel <= stride everywhere: disjoint, including gaps (kernel < stride)
+    assert mp.maxpool3d_bwd_plan((1, 1, 9, 9, 9), (3, 3, 3), (2, 2, 2), (3, 3, 3),
+                                 torch.float16) == "bwd_disjoint"
+    # adaptive output larger than the input: overlapping
+    assert mp.maxpool3d_bwd_plan((1, 1, 3, 3, 3), (5, 5, 5), None, None,
+                                 torch.float32) != "bwd_disjoint"
+    assert mp.maxpool3d_fwd_plan((0, 4, 3, 3, 3), (2, 2, 2), (1, 1, 1), torch.float32) == "noop"
+
+
+def test_binding_rejects_cpu_tensors(L):
+    x = torch.zeros((1, 1, 4, 4, 4))
+    with pytest.raises(ValueError):
+        mp.maxpool3d_fwd(x, x, x, (2, 2, 2), (2, 2, 2))
