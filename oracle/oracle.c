@@ -61,26 +61,28 @@ enum {
 /* of binary32), written from the format definitions.                  */
 /* ------------------------------------------------------------------ */
 
-/* binary16 -> binary32: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+/* binary16 -> binary32: sign, 5-bit exponent (bias 15), 10-bit fraction.
+ * Normal numbers keep sign and fraction and move the exponent from bias 15
+ * to bias 127; subnormals are frac * 2^-24 (exact in binary32); infinity
+ * and NaN keep sign and fraction (the NaN payload moves to the top of the
+ * binary32 fraction). */
 float oracle_f16_to_f32(uint16_t h)
 {
-    int sign = (h >> 15) & 1;
-    int e = (h >> 10) & 0x1F;
-    int frac = h & 0x3FF;
-    double mag;
-    if (e == 0x1F) {
-        /* Infinity or NaN: keep the sign and move the fraction (payload)
-         * into the top of the binary32 fraction. */
-        uint32_t bits = ((uint32_t)sign << 31) | (0xFFu << 23) | ((uint32_t)frac << 13);
-        float f;
-        memcpy(&f, &bits, 4);
-        return f;
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t e = (h >> 10) & 0x1F;
+    uint32_t frac = h & 0x3FF;
+    uint32_t bits;
+    float f;
+    if (e == 0) {
+        f = (float)frac * 0x1p-24f;                         /* zero or subnormal */
+        return sign ? -f : f;
     }
-    if (e == 0)
-        mag = ldexp((double)frac, -24);                 /* zero or subnormal */
+    if (e == 0x1F)
+        bits = sign | (0xFFu << 23) | (frac << 13);         /* infinity or NaN */
     else
-        mag = ldexp((double)(1024 + frac), e - 25);     /* normal            */
-    return (float)(sign ? -mag : mag);                  /* exact */
+        bits = sign | ((e - 15 + 127) << 23) | (frac << 13); /* normal */
+    memcpy(&f, &bits, 4);
+    return f;
 }
 
 /* bfloat16 -> binary32: bfloat16 is the high half of a binary32 pattern. */

@@ -1,0 +1,227 @@
+"""CUDA path against the oracle, element by element (needs a GPU).
+
+Forward values and indices, and the gather backward, must match the oracle
+bit for bit; the atomic ablation must be within 1e-6 of the sum of the
+absolute contributions (f32) or 1 ulp (f16, bf16)."""
+import pytest
+import torch
+
+import bwd_maxpool3d_fwd_gb300 as mp
+import oracle
+from gpu_helpers import (DEV, DTYPES, assert_bits_equal, bits, gpu_bwd, gpu_fwd, ordered,
+                         random_input)
+
+pytestmark = pytest.mark.gpu
+
+KINDS = ("normal", "ties", "special")
+
+
+def _fixed_cases(seed, n):
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    for _ in range(n):
+        k = [int(v) for v in torch.randint(1, 5, (3,), generator=g)]
+        s = [int(v) for v in torch.randint(1, 4, (3,), generator=g)]
+        D = k[0] + int(torch.randint(0, 14, (1,), generator=g))
+        H = k[1] + int(torch.randint(0, 40, (1,), generator=g))
+        W = k[2] + int(torch.randint(0, 150, (1,), generator=g))
+        out.append((tuple(k), tuple(s), (2, 3, D, H, W)))
+    return out
+
+
+# Workload-like windows on shapes that span several tiles plus ragged tails.
+FIXED_CASES = [
+    ((2, 2, 2), (2, 2, 2), (2, 3, 9, 37, 70)),
+    ((3, 3, 3), (2, 2, 2), (2, 3, 9, 29, 117)),
+    ((3, 3, 3), (2, 2, 2), (1, 2, 16, 112, 112)),
+    ((2, 2, 2), (2, 2, 2), (1, 2, 32, 64, 64)),
+    ((3, 3, 3), (1, 1, 1), (1, 2, 6, 20, 33)),
+    ((1, 1, 1), (1, 1, 1), (1, 2, 3, 5, 7)),
+    ((2, 3, 1), (3, 2, 4), (2, 2, 11, 13, 17)),
+] + _fixed_cases(101, 24)
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(FIXED_CASES)))
+def test_fixed_fwd_bwd(case, dtype):
+    k, s, shape = FIXED_CASES[case]
+    gen = torch.Generator().manual_seed(1000 + case)
+    kind = KINDS[case % 3]
+    x = random_input(gen, shape, dtype, kind)
+    y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    y, idx = gpu_fwd(x, kernel=k, stride=s)
+    assert torch.equal(idx, i_ref), f"idx differs ({k}, {s}, {shape}, {kind})"
+    assert_bits_equal(y, y_ref, "y")
+    g = torch.randn(y_ref.shape, generator=gen).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    gin = gpu_bwd(g, i_ref, shape, k, s)
+    assert_bits_equal(gin, gin_ref, "grad_in")
+
+
+def _adaptive_cases():
+    g = torch.Generator().manual_seed(202)
+    out = [((2, 3, 8, 8, 8), (4, 4, 4)), ((2, 3, 30, 50, 50), (8, 12, 12)),
+           ((1, 3, 8, 14, 14), (1, 1, 1)), ((1, 1, 7, 7, 7), (8, 8, 8)),
+           ((2, 2, 7, 7, 7), (3, 3, 3)), ((1, 2, 10, 10, 10), (3, 4, 6)),
+           ((1, 1, 3, 5, 9), (7, 9, 12))]
+    for _ in range(14):
+        I = [int(v) for v in torch.randint(1, 40, (3,), generator=g)]
+        O = [int(torch.randint(1, i + 4, (1,), generator=g)) for i in I]
+        out.append(((2, 2) + tuple(I), tuple(O)))
+    return out
+
+
+ADAPTIVE_CASES = _adaptive_cases()
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(ADAPTIVE_CASES)))
+def test_adaptive_fwd_bwd(case, dtype):
+    shape, out = ADAPTIVE_CASES[case]
+    gen = torch.Generator().manual_seed(2000 + case)
+    kind = KINDS[case % 3]
+    x = random_input(gen, shape, dtype, kind)
+    y_ref, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    y, idx = gpu_fwd(x, out_size=out)
+    assert torch.equal(idx, i_ref), f"idx differs ({shape} -> {out}, {kind})"
+    assert_bits_equal(y, y_ref, "y")
+    g = torch.randn(y_ref.shape, generator=gen).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    gin = gpu_bwd(g, i_ref, shape)
+    assert_bits_equal(gin, gin_ref, "grad_in")
+
+
+def _atomic_tolerance_ok(gin, gin_ref, g, idx, dtype):
+    if dtype == torch.float32:
+        P = g.shape[0] * g.shape[1]
+        sabs = torch.zeros(gin.numel(), dtype=torch.float64)
+        flat_idx = idx.reshape(P, -1) + (torch.arange(P) * gin[0, 0].numel()).unsqueeze(1)
+        sabs.index_add_(0, flat_idx.reshape(-1), g.double().abs().reshape(-1))
+        err = (gin.double().reshape(-1) - gin_ref.double().reshape(-1)).abs()
+        return bool((err <= 1e-6 * sabs + 1e-30).all())
+    return bool(((ordered(gin) - ordered(gin_ref)).abs() <= 1).all())
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", [1, 2, 4, 7, 9])
+def test_atomic_ablation(case, dtype):
+    k, s, shape = FIXED_CASES[case]
+    gen = torch.Generator().manual_seed(3000 + case)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    gin = gpu_bwd(g, i_ref, shape, k, s, algo=mp.BWD_ATOMIC)
+    assert _atomic_tolerance_ok(gin, gin_ref, g, i_ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+def test_gather_is_deterministic(dtype):
+    k, s, shape = FIXED_CASES[1]
+    gen = torch.Generator().manual_seed(77)
+    x = random_input(gen, shape, dtype, "ties")
+    _, idx = oracle.maxpool3d_fwd(x, k, s)
+    g = torch.randn(idx.shape, generator=gen).to(dtype)
+    first = bits(gpu_bwd(g, idx, shape, k, s))
+    for _ in range(5):
+        assert torch.equal(bits(gpu_bwd(g, idx, shape, k, s)), first)
+
+
+def test_gpu_roundings_match_oracle_conversions():
+    # binary32 -> binary16 / bfloat16 rounding of the CUDA path (exercised
+    # through an overlap sum of two terms) against the oracle's encoders.
+    gen = torch.Generator().manual_seed(9)
+    for dtype, enc in ((torch.float16, oracle.f32_to_f16), (torch.bfloat16, oracle.f32_to_bf16)):
+        n = 4096
+        a = torch.randn(n, generator=gen).to(dtype)
+        b = (torch.randn(n, generator=gen) * 1e-3).to(dtype)
+        g = torch.stack([a, b], dim=1).reshape(n, 1, 1, 1, 2)
+        idx = torch.ones_like(g, dtype=torch.int64)
+        gin = gpu_bwd(g.contiguous(), idx, (n, 1, 1, 1, 3), (1, 1, 2), (1, 1, 1))
+        got = bits(gin[:, 0, 0, 0, 1]).long() & 0xFFFF
+        s32 = a.float() + b.float()                       # the binary32 sum
+        want = torch.tensor([enc(float(v)) for v in s32])
+        assert torch.equal(got, want.long())
+
+
+def test_empty_input_is_noop():
+    x = torch.empty((0, 3, 4, 4, 4), device=DEV)
+    y = torch.empty((0, 3, 2, 2, 2), device=DEV)
+    idx = torch.empty((0, 3, 2, 2, 2), dtype=torch.int64, device=DEV)
+    mp.maxpool3d_fwd(x, y, idx, (2, 2, 2), (2, 2, 2))
+    mp.maxpool3d_bwd(y, idx, x, (2, 2, 2), (2, 2, 2))
+    torch.cuda.synchronize()
+
+
+def test_unaligned_pointers_take_scalar_paths():
+    # Views that start one element into a buffer: not 16-byte aligned.
+    gen = torch.Generator().manual_seed(31)
+    for dtype in DTYPES:
+        shape, k, s = (2, 3, 9, 17, 40), (3, 3, 3), (2, 2, 2)
+        x = random_input(gen, shape, dtype, "ties")
+        y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+        g = torch.randn(y_ref.shape, generator=gen).to(dtype)
+        gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+        xb = torch.empty(x.numel() + 1, dtype=dtype, device=DEV)
+        xd = xb[1:].view(shape)
+        xd.copy_(x.to(DEV))
+        yb = torch.empty(y_ref.numel() + 1, dtype=dtype, device=DEV)
+        yd = yb[1:].view(y_ref.shape)
+        idx = torch.empty(y_ref.shape, dtype=torch.int64, device=DEV)
+        mp.maxpool3d_fwd(xd, yd, idx, k, s)
+        gb = torch.empty(g.numel() + 1, dtype=dtype, device=DEV)
+        gd = gb[1:].view(g.shape)
+        gd.copy_(g.to(DEV))
+        ginb = torch.empty(x.numel() + 1, dtype=dtype, device=DEV)
+        gind = ginb[1:].view(shape)
+        mp.maxpool3d_bwd(gd, idx, gind, k, s)
+        torch.cuda.synchronize()
+        assert torch.equal(idx.cpu(), i_ref)
+        assert_bits_equal(yd.cpu(), y_ref, "y (unaligned)")
+        assert_bits_equal(gind.cpu(), gin_ref, "grad_in (unaligned)")
+
+
+@pytest.mark.parametrize("algo", [mp.BWD_AUTO, mp.BWD_ATOMIC])
+def test_guard_bands_untouched(algo):
+    # Outputs live inside larger buffers filled with a sentinel; nothing
+    # outside the output ranges may change.
+    gen = torch.Generator().manual_seed(41)
+    for dtype in DTYPES:
+        for k, s, shape in (FIXED_CASES[0], FIXED_CASES[1], FIXED_CASES[6]):
+            x = random_input(gen, shape, dtype, "normal").to(DEV)
+            out = mp.pool_out_size(shape[2:], k, s)
+            oshape = shape[:2] + out
+            no, ni = 1, 1
+            for v in oshape:
+                no *= v
+            for v in shape:
+                ni *= v
+            pad = 64
+            yb = torch.full((no + 2 * pad,), 7.0, dtype=dtype, device=DEV)
+            ib = torch.full((no + 2 * pad,), -7, dtype=torch.int64, device=DEV)
+            gb = torch.full((ni + 2 * pad,), 5.0, dtype=dtype, device=DEV)
+            y, idx, gin = yb[pad:pad + no].view(oshape), ib[pad:pad + no].view(oshape), \
+                gb[pad:pad + ni].view(shape)
+            mp.maxpool3d_fwd(x, y, idx, k, s)
+            g = torch.randn(oshape, generator=gen).to(dtype).to(DEV)
+            nbytes = mp.maxpool3d_bwd_workspace_bytes(shape, dtype, algo)
+            ws = torch.empty(nbytes // 4, dtype=torch.float32, device=DEV) if nbytes else None
+            mp.maxpool3d_bwd(g, idx, gin, k, s, algo=algo, workspace=ws)
+            torch.cuda.synchronize()
+            for buf, val in ((yb, 7.0), (ib, -7), (gb, 5.0)):
+                assert bool((buf[:pad] == val).all()) and bool((buf[-pad:] == val).all())
+
+
+def test_large_plane_offsets():
+    # In-plane offsets above 2^24 (not exact in binary32) must stay exact.
+    shape = (1, 1, 64, 512, 1024)
+    gen = torch.Generator().manual_seed(51)
+    x = torch.randn(shape, generator=gen).to(torch.bfloat16)
+    for k, s in (((2, 2, 2), (2, 2, 2)), ((3, 3, 3), (2, 2, 2))):
+        y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+        y, idx = gpu_fwd(x, kernel=k, stride=s)
+        assert torch.equal(idx, i_ref)
+        assert_bits_equal(y, y_ref, "y")
+        g = torch.randn(y_ref.shape, generator=gen).to(torch.bfloat16)
+        assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
+                          "grad_in")

@@ -30,7 +30,8 @@ MUTANTS = {
         " acc[target] = load_f32(dtype, gin, p * in_vol); }"),
     "bwd_empty_is_negative_zero": ("seen[j] ? acc[j] : 0.0f", "seen[j] ? acc[j] : -0.0f"),
     "round_ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
-    "f16_subnormal_scale": ("mag = ldexp((double)frac, -24);", "mag = ldexp((double)frac, -25);"),
+    "f16_subnormal_scale": ("(float)frac * 0x1p-24f", "(float)frac * 0x1p-25f"),
+    "f16_exponent_bias": ("((e - 15 + 127) << 23)", "((e - 14 + 127) << 23)"),
     "bf16_subnormal_limit": ("r = round_to_format(fabs((double)f), 7, -126);",
                              "r = round_to_format(fabs((double)f), 7, -125);"),
 }
