@@ -1,0 +1,530 @@
+"""Benchmark: 3-D max pooling forward + backward, effective HBM GB/s.
+
+One step = the whole path on one batch: the forward (max + argmax) and the
+backward (gradient routing) of the workload, through the C ABI. The timed
+workload is the fixed-window k3 s2 fp16 one (32x128x16x112x112 -> 7x55x55):
+the largest, and one of the two with a bandwidth target. Other workloads are
+reported per kernel under "per_config".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line. Under torchrun each rank runs its own shard (an
+independent instance of the workload, weak scaling; no collective on the data
+path) and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bwd_maxpool3d_fwd_gb300 import workloads  # noqa: E402
+
+HEADLINE = 3
+METRIC = "max-pool3d fwd+bwd effective HBM GB/s and % of GB300 peak, per config"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 512 << 20
+DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+# ---------------------------------------------------------------- bytes
+
+def covered_extent(I, k, s, O):
+    return (O - 1) * s + k
+
+
+def algorithmic_bytes(w):
+    """Minimal bytes: forward = covered input read + y + int64 idx written;
+    backward = grad_out + idx read + full grad_in written."""
+    es = w.elem_bytes
+    P = w.planes
+    ovol = w.out[0] * w.out[1] * w.out[2]
+    if w.mode == "fixed":
+        cov = 1
+        for I, k, s, O in zip((w.D, w.H, w.W), w.kernel, w.stride, w.out):
+            cov *= covered_extent(I, k, s, O)
+    else:
+        cov = w.D * w.H * w.W        # adaptive windows cover every input
+    vol = w.D * w.H * w.W
+    fwd = P * (cov * es + ovol * es + ovol * 8)
+    bwd = P * (ovol * es + ovol * 8 + vol * es)
+    return fwd, bwd
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Runner:
+    """Device buffers and the two entry-point calls for one workload."""
+
+    def __init__(self, w, x_cpu, g_cpu, dev, algo=None):
+        import bwd_maxpool3d_fwd_gb300 as mp
+        self.mp = mp
+        self.w = w
+        self.dev = dev
+        self.x = x_cpu.to(dev)
+        self.g = g_cpu.to(dev)
+        self.y = torch.empty(w.out_shape, dtype=w.dtype, device=dev)
+        self.idx = torch.empty(w.out_shape, dtype=torch.int64, device=dev)
+        self.gin = torch.empty(w.in_shape, dtype=w.dtype, device=dev)
+        self.algo = mp.BWD_AUTO if algo is None else algo
+        self.k = w.kernel if w.mode == "fixed" else None
+        self.s = w.stride if w.mode == "fixed" else None
+        nbytes = mp.maxpool3d_bwd_workspace_bytes(w.in_shape, w.dtype, self.algo)
+        self.ws = torch.empty(nbytes // 4, dtype=torch.float32, device=dev) if nbytes else None
+
+    def paths(self):
+        mp, w = self.mp, self.w
+        if w.mode == "fixed":
+            pf = mp.maxpool3d_fwd_plan(w.in_shape, w.kernel, w.stride, w.dtype)
+        else:
+            pf = mp.adaptive_maxpool3d_fwd_plan(w.in_shape, w.out, w.dtype)
+        pb = mp.maxpool3d_bwd_plan(w.in_shape, w.out, self.k, self.s, w.dtype, self.algo)
+        return pf, pb
+
+    def launches_per_step(self):
+        pf, pb = self.paths()
+        nf = 0 if pf == "noop" else 1
+        if pb == "noop":
+            nb = 0
+        elif pb == "bwd_atomic":
+            nb = 2 if self.w.dtype == torch.float32 else 3
+        else:
+            nb = 1
+        return nf, nb
+
+    def fwd(self, x=None, y=None, idx=None):
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        idx = self.idx if idx is None else idx
+        if self.w.mode == "fixed":
+            self.mp.maxpool3d_fwd(x, y, idx, self.w.kernel, self.w.stride)
+        else:
+            self.mp.adaptive_maxpool3d_fwd(x, y, idx, self.w.out)
+
+    def bwd(self, g=None, idx=None, gin=None):
+        g = self.g if g is None else g
+        idx = self.idx if idx is None else idx
+        gin = self.gin if gin is None else gin
+        self.mp.maxpool3d_bwd(g, idx, gin, self.k, self.s, algo=self.algo, workspace=self.ws)
+
+
+def l2_flush(buf):
+    buf.add_(1)
+
+
+def time_per_kernel(r, iters, warmup, flush):
+    """Median fwd and bwd device times (ms), each launch preceded by an L2
+    flush, CUDA events on the launching stream."""
+    stream = torch.cuda.current_stream()
+    fb = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=r.dev) if flush else None
+    for _ in range(warmup):
+        r.fwd()
+        r.bwd()
+    tf, tb = [], []
+    for _ in range(iters):
+        for kind, fn, out in (("fwd", r.fwd, tf), ("bwd", r.bwd, tb)):
+            if fb is not None:
+                l2_flush(fb)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+    return statistics.median(tf), statistics.median(tb)
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel_kind):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_fixed_k3s2_f16_32x128x16x112x112.txt")
+    try:
+        with open(path) as f:
+            kv = dict(ln.split(":", 1) for ln in f if ":" in ln and not ln.startswith("#"))
+    except OSError:
+        return None
+    kv = {k.strip(): v.strip() for k, v in kv.items()}
+    if kv.get("kernel_sources_sha256_12") != kernel_hash():
+        return None
+    v = kv.get(f"{kernel_kind}_dram_bytes_per_launch")
+    return int(v) if v else None
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step(w, x, g):
+    """One pass of the oracle over the given planes: forward then backward."""
+    import oracle
+    if w.mode == "fixed":
+        _, idx = oracle.maxpool3d_fwd(x, w.kernel, w.stride)
+    else:
+        _, idx = oracle.adaptive_maxpool3d_fwd(x, w.out)
+    oracle.maxpool3d_bwd(g, idx, (w.D, w.H, w.W))
+
+
+def oracle_sample(w, nplanes):
+    planes = list(range(nplanes))
+    return workloads.make_x(w, planes=planes), workloads.make_grad_out(w, planes=planes)
+
+
+def cpu_plane_seconds(w):
+    x, g = oracle_sample(w, 4)
+    t = time.perf_counter()
+    oracle_step(w, x, g)
+    return (time.perf_counter() - t) / 4
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The oracle (single-threaded C) on a bounded sample of planes of the
+    same workload, sized for about target_s seconds of CPU work."""
+    per_plane = cpu_plane_seconds(w)
+    n = int(max(1, min(w.planes, target_s / max(per_plane, 1e-6))))
+    x, g = oracle_sample(w, n)
+    t = time.perf_counter()
+    oracle_step(w, x, g)
+    dt = time.perf_counter() - t
+    fb, bb = algorithmic_bytes(w)
+    sample_bytes = (fb + bb) * n / w.planes
+    return {"value": round(sample_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} of {w.planes} planes of {w.name}, forward + backward, "
+                      f"{dt:.1f} s on 1 host core (host has {os.cpu_count()} cores)"}
+
+
+def reference_arm(args):
+    """The oracle as the reference implementation, timed on the host cores."""
+    w = workloads.WORKLOADS[args.workload]
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    per_plane = cpu_plane_seconds(w)
+    budget = 90.0                                  # whole run, seconds
+    n = int(max(1, min(w.planes, budget / max(per_plane, 1e-6) / (args.steps + args.warmup))))
+    x, g = oracle_sample(w, n)
+    for _ in range(args.warmup):
+        oracle_step(w, x, g)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, x, g)
+    dt = time.perf_counter() - t
+    fb, bb = algorithmic_bytes(w)
+    step_bytes = (fb + bb) * n / w.planes
+    value = step_bytes * args.steps / dt / 1e9
+    sample = (f"{n} of {w.planes} planes of {w.name} per step, forward + backward, "
+              f"1 host core of {os.cpu_count()}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "planes_per_step": n},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    """(rank, world, local_rank) from the torchrun environment; a process
+    group only when world > 1 (used for a barrier and the max over ranks)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(w, rank):
+    """Each rank's shard is an independent instance of the workload."""
+    import dataclasses
+    return dataclasses.replace(w, seed=w.seed + 7919 * rank)
+
+
+def smi_id(dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except (AttributeError, RuntimeError):
+        return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------- e2e
+
+def e2e(r, x_cpu, g_cpu, steps=5, warmup=2):
+    """Same metric through the public API with host buffers: each step copies
+    the inputs from pinned host memory, runs forward + backward, and copies
+    every result (y, idx, grad_in) back to pinned host memory."""
+    w = r.w
+    xh, gh = x_cpu.pin_memory(), g_cpu.pin_memory()
+    yh = torch.empty(w.out_shape, dtype=w.dtype).pin_memory()
+    ih = torch.empty(w.out_shape, dtype=torch.int64).pin_memory()
+    ginh = torch.empty(w.in_shape, dtype=w.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        r.x.copy_(xh, non_blocking=True)
+        r.g.copy_(gh, non_blocking=True)
+        r.fwd()
+        r.bwd()
+        yh.copy_(r.y, non_blocking=True)
+        ih.copy_(r.idx, non_blocking=True)
+        ginh.copy_(r.gin, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / steps
+    fb, bb = algorithmic_bytes(w)
+    h2d = xh.numel() * xh.element_size() + gh.numel() * gh.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in (yh, ih, ginh))
+    return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
+
+
+# ---------------------------------------------------------------- main arm
+
+def per_config(dev, peak):
+    """Each workload's forward and backward timed alone (median of 20, L2
+    flushed before every launch), as GB/s and fraction of the HBM peak."""
+    out = {}
+    for n, w in enumerate(workloads.WORKLOADS):
+        r = Runner(w, workloads.make_x(w), workloads.make_grad_out(w), dev)
+        tf, tb = time_per_kernel(r, iters=20, warmup=3, flush=True)
+        fb, bb = algorithmic_bytes(w)
+        pf, pb = r.paths()
+        fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
+        out[w.name] = {
+            "fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2),
+            "fwd_bytes": fb, "bwd_bytes": bb,
+            "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
+            "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
+            "fwd_frac_of_nominal_8000": round(fg / NOMINAL_HBM_GBS, 4),
+            "bwd_frac_of_nominal_8000": round(bg / NOMINAL_HBM_GBS, 4),
+            "fwd_path": pf, "bwd_path": pb}
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
+def our_arm(args):
+    rank, world, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import bwd_maxpool3d_fwd_gb300 as mp
+    mp.lib()                                     # fail loudly if the library is missing
+    base = workloads.WORKLOADS[args.workload]
+    w = shard_seed(base, rank)
+    x_cpu, g_cpu = workloads.make_x(w), workloads.make_grad_out(w)
+    r = Runner(w, x_cpu, g_cpu, dev)
+    peak, peak_kind = hbm_peak()
+    fb, bb = algorithmic_bytes(w)
+    nf, nb = r.launches_per_step()
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        r.fwd()
+        r.bwd()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(smi_id(dev)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(1.0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        r.fwd()
+        e1.record(stream)
+        r.bwd()
+        e2.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+
+    step_bytes = fb + bb
+    value = step_bytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    kind, kbytes, kms = ("bwd", bb, bwd_ms) if bwd_ms >= fwd_ms else ("fwd", fb, fwd_ms)
+    pf, pb = r.paths()
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kind),
+                "kernel": pb if kind == "bwd" else pf, "peak_source": peak_kind,
+                "bytes_per_launch": kbytes,
+                "fwd": {"path": pf, "us": round(fwd_ms * 1e3, 2), "bytes": fb,
+                        "gbs": round(fb / (fwd_ms * 1e-3) / 1e9, 1),
+                        "frac": round(fb / (fwd_ms * 1e-3) / 1e9 / peak, 4)},
+                "bwd": {"path": pb, "us": round(bwd_ms * 1e3, 2), "bytes": bb,
+                        "gbs": round(bb / (bwd_ms * 1e-3) / 1e9, 1),
+                        "frac": round(bb / (bwd_ms * 1e-3) / 1e9 / peak, 4)}}
+    e2e_res = e2e(r, x_cpu, g_cpu)
+    del r
+    torch.cuda.empty_cache()
+    cfg = per_config(dev, peak) if (rank == 0 and not args.no_per_config) else None
+    cpu = cpu_baseline(base) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
+        "data": "synthetic (seeded generators; shapes and value recipes of the workload)",
+        "config": {"workload": base.name, "input": list(base.in_shape),
+                   "output": list(base.out_shape), "kernel": list(base.kernel),
+                   "stride": list(base.stride),
+                   "l2": "inputs larger than L2 (input 1644 MB); no flush between steps",
+                   "parallelism": f"independent shards x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e_res,
+        "gpu_launches": (nf + nb) * args.steps, "clocks": clocks,
+        "per_config": cfg,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=HEADLINE)
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = reference_arm(args) if args.impl == "reference" else our_arm(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
