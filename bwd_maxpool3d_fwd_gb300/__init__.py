@@ -164,3 +164,23 @@ def maxpool3d_bwd_plan(in_shape, out_size, kernel, stride, dtype, algo=BWD_AUTO)
     _check(lib().maxpool3d_bwd_plan(*in_shape, *out_size, *k, *s, DTYPE_CODE[dtype], algo,
                                     ctypes.byref(p)), "maxpool3d_bwd_plan")
     return PATHS[p.value]
+
+
+def maxpool3d_bwd_noalloc(grad_out, idx, grad_in, kernel=None, stride=None, stream=None):
+    """Atomic-form backward that allocates nothing: for callers that cannot
+    allocate device memory while running. The binary32 accumulators (f16,
+    bf16) live in a 32 MiB array inside the library, so N*C*D*H*W is limited
+    to 8 Mi elements for those types; calls that overlap on the GPU race."""
+    _cuda(grad_out, idx, grad_in)
+    L = lib()
+    f = L.maxpool3d_bwd_noalloc
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 5 + [ctypes.c_int] * 10 + [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    N, C, D, H, W = grad_in.shape
+    od, oh, ow = grad_out.shape[2:]
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    with torch.cuda.device(grad_in.device):
+        st = f(grad_out.data_ptr(), idx.data_ptr(), grad_in.data_ptr(), N, C, D, H, W,
+               od, oh, ow, *k, *s, _code(grad_out), _stream(grad_in, stream))
+    _check(st, "maxpool3d_bwd_noalloc")

@@ -339,6 +339,8 @@ const char* mp3d_status_string(int status) {
     case MP3D_ERR_ALGO: return "unknown backward algorithm";
     case MP3D_ERR_ALIGN: return "pointer not aligned to its element size";
     case MP3D_ERR_ALIAS: return "an output buffer overlaps another buffer";
+    case MP3D_ERR_SCRATCH: return "problem larger than the built-in scratch of maxpool3d_bwd_noalloc "
+                                  "(8 Mi binary32 accumulators for f16/bf16)";
     default: return "unknown status";
     }
 }

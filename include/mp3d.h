@@ -72,7 +72,8 @@ typedef enum {
     MP3D_ERR_CUDA = 6,       /* a CUDA launch or query failed               */
     MP3D_ERR_ALGO = 7,       /* algo not in mp3d_bwd_algo                   */
     MP3D_ERR_ALIGN = 8,      /* a pointer not aligned to its element size   */
-    MP3D_ERR_ALIAS = 9       /* an output overlaps an input or another output */
+    MP3D_ERR_ALIAS = 9,      /* an output overlaps an input or another output */
+    MP3D_ERR_SCRATCH = 10    /* too large for maxpool3d_bwd_noalloc's built-in scratch */
 } mp3d_status;
 
 /* Kernel paths reported by the *_plan queries (for logging and tests). */
@@ -154,6 +155,38 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                        int od, int oh, int ow,
                        int kd, int kh, int kw, int sd, int sh, int sw,
                        int dtype, int algo, int* path);
+
+/*
+ * Backward without any device allocation (atomic form). The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they run, such as a plugin inside an engine
+ * that owns all device memory and forbids cudaMalloc while executing, or a
+ * deployment with a fixed memory budget. Those callers cannot provide the
+ * binary32 workspace that maxpool3d_bwd needs for algo ATOMIC with f16/bf16.
+ *
+ * Computes what maxpool3d_bwd computes with algo = MP3D_BWD_ATOMIC (zero
+ * fill, binary32 atomicAdd scatter, one rounding for f16/bf16), but keeps
+ * the binary32 accumulators in an array built into the library: 8 Mi
+ * floats (32 MiB), held on every GPU that loads the library until the
+ * process exits. Same arguments as maxpool3d_bwd minus algo and workspace.
+ *  - f16/bf16: N*C*D*H*W must be at most 8,388,608 (8 Mi); larger problems
+ *    return MP3D_ERR_SCRATCH before any launch. f32 accumulates in grad_in
+ *    directly, uses no scratch and has no such limit.
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current) and caches it; make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array. Each call clears the part
+ *    it uses before accumulating, so calls in sequence are independent, but
+ *    calls that can overlap on the GPU (different streams without ordering,
+ *    or several host threads) race on the array and give wrong results.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    call.
+ */
+int maxpool3d_bwd_noalloc(const void* grad_out, const int64_t* idx, void* grad_in,
+                          int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                          int od, int oh, int ow,
+                          int kd, int kh, int kw, int sd, int sh, int sw,
+                          int dtype, cudaStream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char* mp3d_status_string(int status);
