@@ -147,10 +147,10 @@ Geo as_fixed(const Geo& g) {
     return f;
 }
 
-int fwd_path(const Geo& g, int dtype) {
+int fwd_path(const Geo& g, int dtype, bool aligned16 = true) {
     if (g.P == 0) return MP3D_PATH_NOOP;
     if (is_global(g)) return MP3D_PATH_FWD_GLOBAL;
-    if (fwd_s2_supported(g, dtype)) return MP3D_PATH_FWD_S2;
+    if (fwd_s2_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_S2;
     return MP3D_PATH_FWD_GENERIC;
 }
 
@@ -163,7 +163,7 @@ int bwd_path(const Geo& g, int algo) {
 }
 
 int run_fwd(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, cudaStream_t s) {
-    const int path = fwd_path(g, dtype);
+    const int path = fwd_path(g, dtype, (uintptr_t)x % 16 == 0);
     log_path("fwd", path, g, dtype);
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
     int sms = 0;

@@ -121,30 +121,6 @@ k_bwd_disjoint(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __r
     }
 }
 
-template <typename T>
-static cudaError_t bwd_disjoint_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
-                                  int sms, cudaStream_t s) {
-    constexpr int VEC = 16 / sizeof(T);
-    const long long total = g.P * (long long)g.vol;
-    if ((uintptr_t)gi % 16 == 0) {
-        const int grid = grid_for((total + VEC - 1) / VEC, 256, sms, 8);
-        k_bwd_disjoint<T, VEC><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g);
-    } else {
-        const int grid = grid_for(total, 256, sms, 8);
-        k_bwd_disjoint<T, 1><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g);
-    }
-    return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi, const Geo& g,
-                                int dtype, int sms, cudaStream_t s) {
-    switch (dtype) {
-    case F32: return bwd_disjoint_t<float>(go, idx, gi, g, sms, s);
-    case F16: return bwd_disjoint_t<__half>(go, idx, gi, g, sms, s);
-    default: return bwd_disjoint_t<__nv_bfloat16>(go, idx, gi, g, sms, s);
-    }
-}
-
 // ------------------------------------------------------------------ overlap, direct
 // One thread per input element: enumerate the covering windows in
 // ascending (od, oh, ow) order, read each one's stored index, and sum the
@@ -264,12 +240,381 @@ cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, floa
     }
 }
 
-// ------------------------------------------------------------------ overlap, shared masks
-bool bwd_mask_supported(const Geo&) { return false; }
+// ------------------------------------------------------------------ global
+// Disjoint special case where one window covers each whole plane (output
+// 1x1x1): one warp per plane writes the plane with 16-byte stores, the
+// gradient at the stored index and zero elsewhere.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256)
+k_bwd_global(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
+             long long P, int vol) {
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const T zero = Elem<T>::from_f(0.0f);
+    const int nvec = vol / VEC;
+    for (long long p = warp0; p < P; p += nwarps) {
+        const int64_t best = __ldg(idx + p);
+        const T gv = go[p];
+        T* out = gi + p * vol;
+        if (VEC > 1) {
+            uint4* ov = reinterpret_cast<uint4*>(out);
+            for (int v = lane; v < nvec; v += 32) {
+                Vec16<T> c;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) c.e[j] = (v * VEC + j == best) ? gv : zero;
+                ov[v] = c.u;
+            }
+        }
+        for (int e = nvec * VEC + lane; e < vol; e += 32) out[e] = (e == best) ? gv : zero;
+    }
+}
 
-cudaError_t launch_bwd_overlap_mask(const void*, const int64_t*, void*, const Geo&, int, int,
-                                    cudaStream_t) {
-    return cudaErrorNotSupported;
+// ------------------------------------------------------------------ disjoint, row chunks
+// Disjoint windows, rows of W elements that split into 16-byte chunks.
+// Block y walks planes; threads walk the chunks of a plane. A chunk lies in
+// one row (d, h), so its row window (od, oh) is found once; with SW a
+// divisor of VEC the chunk's element i falls in window ow0 + i / SW at
+// offset i % SW. The indices and gradients of those VEC / SW windows are
+// loaded together, then each element takes its window's gradient if the
+// stored index is its own offset, else zero.
+template <typename T, int VEC, int SW>
+__global__ void __launch_bounds__(256)
+k_bwd_disjoint_rows(const T* __restrict__ go, const int64_t* __restrict__ idx,
+                    T* __restrict__ gi, Geo g, FastDiv fHW, FastDiv fW, FastDiv fSD, FastDiv fSH) {
+    constexpr int NWIN = VEC / SW;
+    const int nchunks = g.vol / VEC;
+    const T zero = Elem<T>::from_f(0.0f);
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += gridDim.x * blockDim.x) {
+            const int r0 = c * VEC;
+            const int d = fHW.div(r0);
+            const int rr = r0 - d * g.H * g.W;
+            const int h = fW.div(rr);
+            const int w0 = rr - h * g.W;
+            const int od = fSD.div(d), dr = d - od * g.sd;
+            const int oh = fSH.div(h), hr = h - oh * g.sh;
+            Vec16<T> out;
+            if (od < g.OD && dr < g.kd && oh < g.OH && hr < g.kh) {
+                const int ow0 = w0 / SW;
+                const long long rowo = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW;
+                int64_t li[NWIN];
+                T lg[NWIN];
+#pragma unroll
+                for (int j = 0; j < NWIN; ++j) {
+                    const bool ok = ow0 + j < g.OW;
+                    li[j] = ok ? __ldg(idx + rowo + ow0 + j) : -1;
+                    lg[j] = ok ? go[rowo + ow0 + j] : zero;
+                }
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    const bool hit = (i % SW) < g.kw && li[i / SW] == (int64_t)(r0 + i);
+                    out.e[i] = hit ? lg[i / SW] : zero;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) out.e[i] = zero;
+            }
+            *reinterpret_cast<uint4*>(gi + p * g.vol + r0) = out.u;
+        }
+    }
+}
+// ------------------------------------------------------------------ overlap, shared masks
+// Overlapping windows, deterministic gather in two phases per tile of TD
+// depth slices of one plane:
+//  1. Every window that can cover the tile reads its stored index; if the
+//     index falls in the tile, the window sets one bit in a per-input byte
+//     in shared memory. The bit (slot) is the window's rank among the
+//     input's covering windows in ascending (od, oh, ow) order:
+//     slot = (jd*Ch + jh)*Cw + jw with jd = od - (first window covering d)
+//     and likewise for h, w. Setting bits with atomicOr is order-free.
+//  2. Every input reads its byte: zero means no window picked it (+0); else
+//     it walks the set bits in ascending order, which is ascending
+//     (od, oh, ow), and sums the matching gradients in binary32, starting
+//     from the first, then rounds once.
+// The result equals enumerating the covering windows in order and checking
+// each stored index, with one index read per window instead of one per
+// (input, covering window) pair.
+struct AxisMap {
+    int I, O, K, S;
+    int adaptive;
+    FastDiv fS;   // fixed: divide by S
+    FastDiv fI;   // adaptive: divide by I
+    FastDiv fO;   // adaptive: divide by O
+    __device__ __forceinline__ int lo(int x) const {
+        if (adaptive) return fI.div(x * O);
+        return x < K ? 0 : fS.div(x - K) + 1;
+    }
+    __device__ __forceinline__ int hi(int x) const {
+        if (adaptive) return fI.div((x + 1) * O - 1);
+        const int h = fS.div(x);
+        return h < O - 1 ? h : O - 1;
+    }
+    __device__ __forceinline__ bool covers(int o, int x) const {
+        if (adaptive) return fO.div(o * I) <= x && x < fO.div((o + 1) * I + O - 1);
+        return o * S <= x && x < o * S + K;
+    }
+};
+
+struct MaskGeo {
+    int TD, ntiles;
+    int Ch, Cw;          // slot radix along h and w
+    AxisMap ad, ah, aw;
+    FastDiv fHW, fW, fOW, fOHOW;
+};
+
+template <typename T>
+__device__ __forceinline__ T gather_bits(const T* __restrict__ go, long long gobase, const Geo& g,
+                                         const MaskGeo& mg, int d, int local_hw, uint32_t bits) {
+    const int h = mg.fW.div(local_hw);
+    const int w = local_hw - h * g.W;
+    const int ld = mg.ad.lo(d), lh = mg.ah.lo(h), lw = mg.aw.lo(w);
+    float acc = 0.0f;
+    bool any = false;
+    while (bits) {
+        const int slot = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int jd = slot / (mg.Ch * mg.Cw);
+        const int rem = slot - jd * mg.Ch * mg.Cw;
+        const int jh = rem / mg.Cw;
+        const int jw = rem - jh * mg.Cw;
+        const long long o = gobase + ((long long)(ld + jd) * g.OH + (lh + jh)) * g.OW + (lw + jw);
+        const float v = Elem<T>::to_f(go[o]);
+        acc = any ? acc + v : v;
+        any = true;
+    }
+    return Elem<T>::from_f(acc);
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256)
+k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
+                   Geo g, MaskGeo mg) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* mask32 = reinterpret_cast<uint32_t*>(smem);
+    const int HW = g.H * g.W;
+    const int d0 = blockIdx.x * mg.TD;
+    const int d1 = min(d0 + mg.TD, g.D);
+    const int n = (d1 - d0) * HW;
+    const T zero = Elem<T>::from_f(0.0f);
+    const int od_lo = mg.ad.lo(d0), od_hi = mg.ad.hi(d1 - 1);
+    const int ohow = g.OH * g.OW;
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        uint4* m16 = reinterpret_cast<uint4*>(smem);
+        for (int i = threadIdx.x; i < (n + 15) / 16; i += blockDim.x) m16[i] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        const long long obase = p * (long long)g.ovol;
+        if (od_lo <= od_hi) {
+            const int wend = (od_hi + 1) * ohow;
+            for (int wi = od_lo * ohow + threadIdx.x; wi < wend; wi += blockDim.x) {
+                const long long local64 = __ldg(idx + obase + wi) - (long long)d0 * HW;
+                if (local64 < 0 || local64 >= n) continue;
+                const int local = (int)local64;
+                const int od = mg.fOHOW.div(wi);
+                const int rem = wi - od * ohow;
+                const int oh = mg.fOW.div(rem);
+                const int ow = rem - oh * g.OW;
+                const int dd = mg.fHW.div(local);
+                const int r = local - dd * HW;
+                const int h = mg.fW.div(r);
+                const int w = r - h * g.W;
+                const int d = d0 + dd;
+                if (!mg.ad.covers(od, d) || !mg.ah.covers(oh, h) || !mg.aw.covers(ow, w)) continue;
+                const int slot = ((od - mg.ad.lo(d)) * mg.Ch + (oh - mg.ah.lo(h))) * mg.Cw +
+                                 (ow - mg.aw.lo(w));
+                atomicOr(&mask32[local >> 2], 1u << ((local & 3) * 8 + slot));
+            }
+        }
+        __syncthreads();
+        T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
+        const int nchunks = (VEC > 1) ? n / VEC : 0;
+        for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+            const int r0 = c * VEC;
+            uint32_t mw[VEC / 4 > 0 ? VEC / 4 : 1];
+#pragma unroll
+            for (int k = 0; k < VEC / 4; ++k) mw[k] = mask32[(r0 >> 2) + k];
+            uint32_t anyb = 0;
+#pragma unroll
+            for (int k = 0; k < VEC / 4; ++k) anyb |= mw[k];
+            Vec16<T> o;
+            if (anyb == 0) {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) o.e[i] = zero;
+            } else {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    const uint32_t b = (mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu;
+                    if (b == 0) {
+                        o.e[i] = zero;
+                    } else {
+                        const int local = r0 + i;
+                        const int dd = mg.fHW.div(local);
+                        o.e[i] = gather_bits<T>(go, obase, g, mg, d0 + dd, local - dd * HW, b);
+                    }
+                }
+            }
+            *reinterpret_cast<uint4*>(out + r0) = o.u;
+        }
+        for (int e = nchunks * VEC + threadIdx.x; e < n; e += blockDim.x) {
+            const uint32_t b = (mask32[e >> 2] >> ((e & 3) * 8)) & 0xFFu;
+            if (b == 0) {
+                out[e] = zero;
+            } else {
+                const int dd = mg.fHW.div(e);
+                out[e] = gather_bits<T>(go, obase, g, mg, d0 + dd, e - dd * HW, b);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ launch: disjoint
+
+template <typename T, int SW>
+static cudaError_t bwd_rows_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                              cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
+    const int nchunks = g.vol / VEC;
+    dim3 grid((unsigned)((nchunks + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
+    k_bwd_disjoint_rows<T, VEC, SW><<<grid, 256, 0, s>>>(
+        (const T*)go, idx, (T*)gi, g, FastDiv((uint32_t)(g.H * g.W)), FastDiv((uint32_t)g.W),
+        FastDiv((uint32_t)g.sd), FastDiv((uint32_t)g.sh));
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t bwd_disjoint_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                  int sms, cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
+    const long long total = g.P * (long long)g.vol;
+    const bool aligned = (uintptr_t)gi % 16 == 0;
+    const bool plane_vec = aligned && ((long long)g.vol * sizeof(T)) % 16 == 0;
+    if (g.ovol == 1 && g.kd == g.D && g.kh == g.H && g.kw == g.W) {
+        const int grid = grid_for(g.P * 32, 256, sms, 8);
+        if (plane_vec)
+            k_bwd_global<T, VEC><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g.P, g.vol);
+        else
+            k_bwd_global<T, 1><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g.P, g.vol);
+        return cudaGetLastError();
+    }
+    if (aligned && g.W % VEC == 0) {
+        switch (g.sw) {
+        case 1: return bwd_rows_t<T, 1>(go, idx, gi, g, s);
+        case 2: return bwd_rows_t<T, 2>(go, idx, gi, g, s);
+        case 4: return bwd_rows_t<T, 4>(go, idx, gi, g, s);
+        case 8: if (VEC == 8) return bwd_rows_t<T, VEC>(go, idx, gi, g, s); break;
+        default: break;
+        }
+    }
+    if (aligned) {
+        const int grid = grid_for((total + VEC - 1) / VEC, 256, sms, 8);
+        k_bwd_disjoint<T, VEC><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g);
+    } else {
+        const int grid = grid_for(total, 256, sms, 8);
+        k_bwd_disjoint<T, 1><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                int dtype, int sms, cudaStream_t s) {
+    switch (dtype) {
+    case F32: return bwd_disjoint_t<float>(go, idx, gi, g, sms, s);
+    case F16: return bwd_disjoint_t<__half>(go, idx, gi, g, sms, s);
+    default: return bwd_disjoint_t<__nv_bfloat16>(go, idx, gi, g, sms, s);
+    }
+}
+
+// ------------------------------------------------------------------ launch: masks
+
+static constexpr int kMaskBytes = 56 * 1024;   // shared bytes for one tile's masks
+
+// Most windows that can cover one position along an axis.
+static int max_cover(int I, int O, int K, int S, bool adaptive) {
+    int c;
+    if (adaptive) c = (O + I - 1) / I + 1;
+    else c = K <= S ? 1 : (K + S - 1) / S;
+    return c < O ? c : O;
+}
+
+static AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
+    AxisMap a;
+    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
+    a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
+    a.fI = FastDiv((uint32_t)I);
+    a.fO = FastDiv((uint32_t)O);
+    return a;
+}
+
+bool bwd_mask_supported(const Geo& g) {
+    const bool a = g.adaptive != 0;
+    const long long slots = (long long)max_cover(g.D, g.OD, g.kd, g.sd, a) *
+                            max_cover(g.H, g.OH, g.kh, g.sh, a) *
+                            max_cover(g.W, g.OW, g.kw, g.sw, a);
+    if (slots > 8) return false;
+    if ((long long)g.H * g.W > kMaskBytes) return false;
+    if (a) {   // products used by the adaptive window arithmetic stay below 2^31
+        const long long lim = (1LL << 31) - 1;
+        if ((long long)g.D * g.OD + g.OD > lim || (long long)g.H * g.OH + g.OH > lim ||
+            (long long)g.W * g.OW + g.OW > lim)
+            return false;
+    }
+    return true;
+}
+
+template <typename T, int VEC>
+static cudaError_t bwd_mask_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                   const MaskGeo& mg, cudaStream_t s) {
+    const int HW = g.H * g.W;
+    const size_t smem = (((size_t)mg.TD * HW) + 15) / 16 * 16;
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_overlap_mask<T, VEC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)mg.ntiles, (unsigned)(g.P < 65535 ? g.P : 65535));
+    k_bwd_overlap_mask<T, VEC><<<grid, 256, smem, s>>>((const T*)go, idx, (T*)gi, g, mg);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t bwd_mask_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                              cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
+    const bool a = g.adaptive != 0;
+    const int HW = g.H * g.W;
+    MaskGeo mg;
+    mg.Ch = max_cover(g.H, g.OH, g.kh, g.sh, a);
+    mg.Cw = max_cover(g.W, g.OW, g.kw, g.sw, a);
+    mg.ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
+    mg.ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
+    mg.aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
+    mg.fHW = FastDiv((uint32_t)HW);
+    mg.fW = FastDiv((uint32_t)g.W);
+    mg.fOW = FastDiv((uint32_t)g.OW);
+    mg.fOHOW = FastDiv((uint32_t)(g.OH * g.OW));
+    int td = kMaskBytes / HW;
+    if (td > g.D) td = g.D;
+    if (td < 1) td = 1;
+    // 16-byte stores need every tile (and plane) to start on a 16-byte boundary.
+    bool vec = (uintptr_t)gi % 16 == 0 && ((long long)g.vol * sizeof(T)) % 16 == 0;
+    if (vec) {
+        int t = td;
+        while (t > 0 && ((long long)t * HW * sizeof(T)) % 16 != 0) --t;
+        if (t > 0 || td == g.D) td = t > 0 ? t : td;
+        vec = ((long long)td * HW * sizeof(T)) % 16 == 0 || td == g.D;
+    }
+    mg.TD = td;
+    mg.ntiles = (g.D + td - 1) / td;
+    if (vec) return bwd_mask_launch<T, VEC>(go, idx, gi, g, mg, s);
+    return bwd_mask_launch<T, 1>(go, idx, gi, g, mg, s);
+}
+
+cudaError_t launch_bwd_overlap_mask(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                    int dtype, int, cudaStream_t s) {
+    switch (dtype) {
+    case F32: return bwd_mask_t<float>(go, idx, gi, g, s);
+    case F16: return bwd_mask_t<__half>(go, idx, gi, g, s);
+    default: return bwd_mask_t<__nv_bfloat16>(go, idx, gi, g, s);
+    }
 }
 
 }  // namespace mp3d

@@ -70,6 +70,31 @@ __device__ __forceinline__ int cover_hi(int x, int I, int O, int K, int S, bool 
     return h < O - 1 ? h : O - 1;
 }
 
+// ---------------------------------------------------------------- division
+// Division of a non-negative int below 2^31 by a fixed divisor d >= 1 as a
+// multiply-high and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 * (2^l - d) / d) + 1, n / d = (mulhi(n, m) + n) >> l; the
+// sum cannot overflow because mulhi(n, m) <= n < 2^31.
+struct FastDiv {
+    uint32_t d, m, l;
+    FastDiv() : d(1), m(1), l(0) {}
+    explicit FastDiv(uint32_t div) : d(div) {
+        l = 0;
+        while ((1ull << l) < div) ++l;
+        m = (uint32_t)((((1ull << l) - div) << 32) / div + 1);
+    }
+    __host__ __device__ __forceinline__ int div(int n) const {
+#ifdef __CUDA_ARCH__
+        const uint32_t t = __umulhi((uint32_t)n, m);
+#else
+        const uint32_t t = (uint32_t)(((uint64_t)(uint32_t)n * m) >> 32);
+#endif
+        return (int)((t + (uint32_t)n) >> l);
+    }
+    __host__ __device__ __forceinline__ int mod(int n, int q) const { return n - q * (int)d; }
+};
+
 // ---------------------------------------------------------------- vectors
 
 // Element-wise access to a 16-byte vector of T.

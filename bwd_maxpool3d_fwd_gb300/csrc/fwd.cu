@@ -155,9 +155,275 @@ cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g
 }
 
 // ------------------------------------------------------------------ stride 2
-bool fwd_s2_supported(const Geo&, int) { return false; }
+// Fast fixed-window forward for 16-bit types with stride 2 along W.
+//
+// Each thread owns one 16-byte chunk of a row (8 elements, so the 4 outputs
+// whose windows start in it), an oh-tile of TOH output rows and a range of
+// output depths. It walks the depth once: for every slice d it loads the
+// tile's rows of its chunk (plus the one element past the chunk that a
+// size-3 window needs), reduces along W, then H, then folds the slice into
+// the accumulators of the (at most two) output depths whose windows contain
+// d. Values travel as packed pairs (two adjacent outputs per 32-bit word)
+// and are compared two at a time with set.gt on f16x2/bf16x2; each lane
+// carries a small code of its winner's (dl, hl, wl) position in the window.
+//
+// Tie rule: reductions run W first, then H, then D, and replace only on a
+// strictly greater value, so the winner is the smallest d, then h, then w
+// among equal maxima: the first occurrence in (d, h, w) row-major order.
+// +0 and -0 compare equal. NaN and infinities are not handled by packed
+// compares; a running x*0 + acc over every loaded word turns NaN once any
+// NaN or infinity was seen, and then the thread recomputes the affected
+// outputs with the exact scalar scan (same rule as the generic kernel).
 
-cudaError_t launch_fwd_s2(const void*, void*, int64_t*, const Geo&, int, int, cudaStream_t) {
+template <typename T> struct Pair;
+template <> struct Pair<__half> {
+    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("set.gt.u32.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
+        uint32_t r;
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
+        return r;
+    }
+    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
+        return ((acc & 0x7FFFu) > 0x7C00u) || (((acc >> 16) & 0x7FFFu) > 0x7C00u);
+    }
+};
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
+        uint32_t r;
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
+        return r;
+    }
+    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
+        return ((acc & 0x7FFFu) > 0x7F80u) || (((acc >> 16) & 0x7FFFu) > 0x7F80u);
+    }
+};
+
+// Replace (mv, mc) lane by lane where v is strictly greater.
+template <typename T>
+__device__ __forceinline__ void merge2(uint32_t& mv, uint32_t& mc, uint32_t v, uint32_t c) {
+    const uint32_t m = Pair<T>::gt(v, mv);
+    mv = (v & m) | (mv & ~m);
+    mc = (c & m) | (mc & ~m);
+}
+
+// Exact scalar max/argmax over a fixed window (the fallback).
+template <typename T>
+__device__ __noinline__ void exact_window(const T* __restrict__ xp, int ds, int de, int hs, int he,
+                                          int ws, int we, int W, int HW, T* yo, int64_t* io) {
+    int best = ds * HW + hs * W + ws;
+    float m = Elem<T>::to_f(xp[best]);
+    for (int d = ds; d < de; ++d)
+        for (int h = hs; h < he; ++h)
+            for (int w = ws; w < we; ++w) {
+                const int off = d * HW + h * W + w;
+                const float v = Elem<T>::to_f(xp[off]);
+                if (beats(v, m)) {
+                    m = v;
+                    best = off;
+                }
+            }
+    *yo = xp[best];
+    *io = best;
+}
+
+constexpr uint32_t kLanes = 0x00010001u;   // a constant in both 16-bit lanes
+
+template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH>
+__global__ void __launch_bounds__(128)
+k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
+         int nq, int nt, int nc, long long nthreads) {
+    constexpr int NR = (TOH - 1) * SH + KH;          // rows of a full oh-tile
+    static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
+    const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (tid >= nthreads) return;
+    const int c = (int)(tid % nc);
+    long long t2 = tid / nc;
+    const int t = (int)(t2 % nt);
+    t2 /= nt;
+    const int q = (int)(t2 % nq);
+    const long long p = t2 / nq;
+
+    const int ow0 = 4 * c, w0 = 8 * c;
+    const int oh0 = t * TOH;
+    const int nh = min(TOH, g.OH - oh0);
+    const int od0 = q * odg;
+    const int nd = min(odg, g.OD - od0);
+    const int HW = g.H * g.W;
+    const T* xp = x + p * g.vol;
+    const bool has_extra = (KW > 2) && (w0 + 8 < g.W);
+    const int hbeg = oh0 * SH;
+    const int nrows = (nh - 1) * SH + KH;
+
+    uint32_t poison = 0;
+    uint32_t cv[TOH][2], cc[TOH][2], pv[TOH][2], pc[TOH][2];
+#pragma unroll
+    for (int j = 0; j < TOH; ++j)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) cv[j][k] = cc[j][k] = pv[j][k] = pc[j][k] = 0;
+
+    auto emit = [&](int od, uint32_t (&v)[TOH][2], uint32_t (&cd)[TOH][2]) {
+        const bool exact = Pair<T>::is_poisoned(poison);
+#pragma unroll
+        for (int j = 0; j < TOH; ++j) {
+            if (j >= nh) break;
+            const int oh = oh0 + j;
+            const long long obase = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW;
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int lane = 0; lane < 2; ++lane) {
+                    const int ow = ow0 + 2 * k + lane;
+                    if (ow >= g.OW) continue;
+                    if (exact) {
+                        exact_window<T>(xp, od * SD, od * SD + KD, oh * SH, oh * SH + KH, ow * 2,
+                                        ow * 2 + KW, g.W, HW, y + obase + ow, idx + obase + ow);
+                        continue;
+                    }
+                    const uint32_t code = (cd[j][k] >> (16 * lane)) & 0xFFFFu;
+                    const int wl = code & 3, hl = (code >> 2) & 3, dl = (code >> 4) & 3;
+                    const uint16_t bitsv = (uint16_t)((v[j][k] >> (16 * lane)) & 0xFFFFu);
+                    reinterpret_cast<uint16_t*>(y)[obase + ow] = bitsv;
+                    idx[obase + ow] = (int64_t)(od * SD + dl) * HW + (oh * SH + hl) * g.W + ow * 2 + wl;
+                }
+        }
+    };
+
+    for (int od = od0; od <= od0 + nd; ++od) {
+#pragma unroll
+        for (int i = 0; i < SD; ++i) {
+            const bool role_cur = (od < od0 + nd) && (i < KD);
+            const bool role_prev = (od > od0) && (SD + i < KD);
+            if (!role_cur && !role_prev) continue;
+            const int d = od * SD + i;
+            uint32_t hv[TOH][2], hc[TOH][2];
+#pragma unroll
+            for (int j = 0; j < TOH; ++j) hv[j][0] = hv[j][1] = hc[j][0] = hc[j][1] = 0;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r >= nrows) break;
+                const T* row = xp + (long long)d * HW + (long long)(hbeg + r) * g.W + w0;
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row));
+                uint32_t e8 = 0;
+                if (KW > 2 && has_extra) e8 = __ldg(reinterpret_cast<const unsigned short*>(row + 8));
+                poison = Pair<T>::poison(poison, raw.x);
+                poison = Pair<T>::poison(poison, raw.y);
+                poison = Pair<T>::poison(poison, raw.z);
+                poison = Pair<T>::poison(poison, raw.w);
+                if (KW > 2) poison = Pair<T>::poison(poison, e8);
+                // W: outputs (0,1) from words x,y (+z), outputs (2,3) from z,w (+e8)
+                uint32_t wv[2], wc[2];
+                wv[0] = __byte_perm(raw.x, raw.y, 0x5410);
+                wc[0] = 0;
+                merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 1u * kLanes);
+                wv[1] = __byte_perm(raw.z, raw.w, 0x5410);
+                wc[1] = 0;
+                merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 1u * kLanes);
+                if (KW > 2) {
+                    merge2<T>(wv[0], wc[0], __byte_perm(raw.y, raw.z, 0x5410), 2u * kLanes);
+                    merge2<T>(wv[1], wc[1], __byte_perm(raw.w, e8, 0x5410), 2u * kLanes);
+                }
+                // H: row r is row hl = r - j*SH of output row j
+#pragma unroll
+                for (int j = 0; j < TOH; ++j) {
+                    const int hl = r - j * SH;
+                    if (hl < 0 || hl >= KH) continue;
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        if (hl == 0) {
+                            hv[j][k] = wv[k];
+                            hc[j][k] = wc[k];
+                        } else {
+                            merge2<T>(hv[j][k], hc[j][k], wv[k], wc[k] | ((uint32_t)hl << 2) * kLanes);
+                        }
+                    }
+                }
+            }
+            // D: slice d is depth dl = i of od, and dl = SD + i of od - 1
+#pragma unroll
+            for (int j = 0; j < TOH; ++j)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    if (role_prev)
+                        merge2<T>(pv[j][k], pc[j][k], hv[j][k], hc[j][k] | ((uint32_t)(SD + i) << 4) * kLanes);
+                    if (role_cur) {
+                        if (i == 0) {
+                            cv[j][k] = hv[j][k];
+                            cc[j][k] = hc[j][k];
+                        } else {
+                            merge2<T>(cv[j][k], cc[j][k], hv[j][k], hc[j][k] | ((uint32_t)i << 4) * kLanes);
+                        }
+                    }
+                }
+            if (role_prev && SD + i == KD - 1) emit(od - 1, pv, pc);
+            if (role_cur && i == KD - 1) emit(od, cv, cc);
+        }
+#pragma unroll
+        for (int j = 0; j < TOH; ++j)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                pv[j][k] = cv[j][k];
+                pc[j][k] = cc[j][k];
+            }
+    }
+}
+
+// Window shapes with a compiled stride-2 kernel: (kd, sd, kh, sh, kw), sw = 2.
+static int s2_variant(const Geo& g) {
+    if (g.adaptive || g.sw != 2) return -1;
+    if (g.kd == 2 && g.sd == 2 && g.kh == 2 && g.sh == 2 && g.kw == 2) return 0;
+    if (g.kd == 3 && g.sd == 2 && g.kh == 3 && g.sh == 2 && g.kw == 3) return 1;
+    return -1;
+}
+
+bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
+    return (dtype == F16 || dtype == BF16) && s2_variant(g) >= 0 && g.W % 8 == 0 && aligned16;
+}
+
+template <typename T, int KD, int SD, int KH, int SH, int KW>
+static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
+                            cudaStream_t s) {
+    constexpr int TOH = 4;
+    const int nc = g.W / 8;
+    const int nt = (g.OH + TOH - 1) / TOH;
+    const long long base = g.P * nt * (long long)nc;
+    // Split the output depths across threads until there are enough threads
+    // to keep every SM busy (about 4096 per SM).
+    const long long target = (long long)sms * 4096;
+    long long want = (target + base - 1) / base;
+    if (want < 1) want = 1;
+    if (want > g.OD) want = g.OD;
+    const int odg = (int)((g.OD + want - 1) / want);
+    const int nq = (g.OD + odg - 1) / odg;
+    const long long n = base * nq;
+    const long long blocks = (n + 127) / 128;
+    k_fwd_s2<T, KD, SD, KH, SH, KW, TOH><<<(unsigned)blocks, 128, 0, s>>>(
+        (const T*)x, (T*)y, idx, g, odg, nq, nt, nc, n);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
+                                   cudaStream_t s) {
+    switch (s2_variant(g)) {
+    case 0: return fwd_s2_t<T, 2, 2, 2, 2, 2>(x, y, idx, g, sms, s);
+    case 1: return fwd_s2_t<T, 3, 2, 3, 2, 3>(x, y, idx, g, sms, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,
+                          cudaStream_t s) {
+    if (dtype == F16) return fwd_s2_dispatch<__half>(x, y, idx, g, sms, s);
+    if (dtype == BF16) return fwd_s2_dispatch<__nv_bfloat16>(x, y, idx, g, sms, s);
     return cudaErrorNotSupported;
 }
 

@@ -17,8 +17,9 @@ cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g
                               int dtype, int sms, cudaStream_t s);
 cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g,
                           int dtype, int sms, cudaStream_t s);
-// Whether the stride-2 kernel handles this geometry and type.
-bool fwd_s2_supported(const Geo& g, int dtype);
+// Whether the stride-2 kernel handles this geometry and type (it needs the
+// input on a 16-byte boundary; plan queries assume an aligned buffer).
+bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16);
 
 // Backward paths (bwd.cu). For the disjoint gather, g.kd..g.sw hold the
 // fixed window (adaptive divisible shapes are passed as kernel = stride =

@@ -225,3 +225,58 @@ def test_large_plane_offsets():
         g = torch.randn(y_ref.shape, generator=gen).to(torch.bfloat16)
         assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
                           "grad_in")
+
+
+# Shapes aimed at the stride-2 forward kernel (16-bit types, rows a multiple
+# of 8 elements): tails in OH (tiles of 4 rows) and OW (chunks of 4 outputs),
+# depths that split into several groups, and NaN/Inf (exact fallback).
+S2_SHAPES = [(1, 3, 2, 2, 8), (2, 2, 3, 5, 16), (1, 2, 7, 9, 24), (1, 1, 5, 17, 40),
+             (2, 3, 16, 34, 112), (1, 2, 33, 6, 64), (3, 1, 4, 11, 8)]
+
+
+@pytest.mark.parametrize("dtype", (torch.float16, torch.bfloat16), ids=str)
+@pytest.mark.parametrize("window", [((2, 2, 2), (2, 2, 2)), ((3, 3, 3), (2, 2, 2))], ids=["k2s2", "k3s2"])
+@pytest.mark.parametrize("shape", S2_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kind", KINDS)
+def test_stride2_forward(shape, window, dtype, kind):
+    k, s = window
+    if any(i < kk for i, kk in zip(shape[2:], k)):
+        pytest.skip("window larger than input")
+    assert mp.maxpool3d_fwd_plan(shape, k, s, dtype) == "fwd_s2"
+    gen = torch.Generator().manual_seed(5000 + 97 * S2_SHAPES.index(shape) + 7 * k[0] + KINDS.index(kind))
+    x = random_input(gen, shape, dtype, kind)
+    y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    y, idx = gpu_fwd(x, kernel=k, stride=s)
+    assert torch.equal(idx, i_ref), f"idx differs ({shape}, {k}, {kind})"
+    assert_bits_equal(y, y_ref, "y")
+
+
+@pytest.mark.parametrize("dtype", (torch.float16, torch.bfloat16), ids=str)
+def test_stride2_forward_subnormals_and_signed_zeros(dtype):
+    gen = torch.Generator().manual_seed(61)
+    shape = (2, 2, 5, 9, 32)
+    tiny = torch.finfo(dtype).smallest_normal
+    x = (torch.randint(-4, 5, shape, generator=gen).float() * tiny / 8).to(dtype)
+    for k, s in (((2, 2, 2), (2, 2, 2)), ((3, 3, 3), (2, 2, 2))):
+        y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+        y, idx = gpu_fwd(x, kernel=k, stride=s)
+        assert torch.equal(idx, i_ref)
+        assert_bits_equal(y, y_ref, "y")
+
+
+DISJOINT_CASES = [((2, 2, 2), (2, 2, 2), (2, 3, 6, 10, 64)), ((1, 2, 1), (3, 2, 4), (2, 2, 7, 9, 32)),
+                  ((1, 1, 1), (1, 1, 1), (1, 2, 3, 4, 16)), ((2, 1, 3), (2, 3, 8), (1, 3, 9, 5, 48)),
+                  ((3, 3, 2), (3, 3, 2), (2, 2, 9, 12, 8))]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(DISJOINT_CASES)))
+def test_disjoint_backward_row_chunks(case, dtype):
+    k, s, shape = DISJOINT_CASES[case]
+    assert mp.maxpool3d_bwd_plan(shape, mp.pool_out_size(shape[2:], k, s), k, s, dtype) == "bwd_disjoint"
+    gen = torch.Generator().manual_seed(7000 + case)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
+                      "grad_in")
