@@ -434,6 +434,9 @@ def our_arm(args):
     import bwd_maxpool3d_fwd_gb300 as mp
     mp.lib()                                     # fail loudly if the library is missing
     base = workloads.WORKLOADS[args.workload]
+    if args.planes:
+        import dataclasses
+        base = dataclasses.replace(base, N=1, C=min(args.planes, base.planes))
     w = shard_seed(base, rank)
     x_cpu, g_cpu = workloads.make_x(w), workloads.make_grad_out(w)
     r = Runner(w, x_cpu, g_cpu, dev)
@@ -501,7 +504,8 @@ def our_arm(args):
         "config": {"workload": base.name, "input": list(base.in_shape),
                    "output": list(base.out_shape), "kernel": list(base.kernel),
                    "stride": list(base.stride),
-                   "l2": "inputs larger than L2 (input 1644 MB); no flush between steps",
+                   "l2": ("inputs larger than L2 (%d MB input); no flush between steps"
+                          % (base.planes * base.D * base.H * base.W * base.elem_bytes // 10**6)),
                    "parallelism": f"independent shards x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e_res,
         "gpu_launches": (nf + nb) * args.steps, "clocks": clocks,
@@ -518,6 +522,9 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=HEADLINE)
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--planes", type=int, default=0,
+                    help="run only the first N planes of the workload (same per-plane shape; "
+                         "for profiling small cases)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

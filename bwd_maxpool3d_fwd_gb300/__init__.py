@@ -63,6 +63,16 @@ def lib() -> ctypes.CDLL:
     return L
 
 
+def mp3d_device_error_flags(clear: bool = True) -> int:
+    """Device error flags (nonzero only if a kernel's bounded wait gave up)."""
+    f = lib().mp3d_device_error_flags
+    f.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+    f.restype = ctypes.c_int
+    v = ctypes.c_uint(0)
+    _check(f(ctypes.byref(v), 1 if clear else 0), "mp3d_device_error_flags")
+    return v.value
+
+
 def mp3d_status_string(status: int) -> str:
     return lib().mp3d_status_string(status).decode()
 

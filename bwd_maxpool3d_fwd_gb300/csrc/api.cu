@@ -326,6 +326,11 @@ int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
 }
 
+int mp3d_device_error_flags(unsigned int* flags, int clear) {
+    if (!flags) return MP3D_ERR_NULLPTR;
+    return read_device_error(flags, clear != 0) == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
 const char* mp3d_status_string(int status) {
     switch (status) {
     case MP3D_OK: return "ok";

@@ -356,30 +356,50 @@ struct AxisMap {
     }
 };
 
+// Raw bits of an element in a 32-bit word, and back.
+template <typename T> struct Elem16 {
+    static __device__ __forceinline__ uint32_t bits(T v) {
+        if (sizeof(T) == 4) return __float_as_uint(*reinterpret_cast<float*>(&v));
+        return (uint32_t)*reinterpret_cast<unsigned short*>(&v);
+    }
+    static __device__ __forceinline__ T from_bits(uint32_t b) {
+        T v;
+        if (sizeof(T) == 4) {
+            float f = __uint_as_float(b);
+            v = *reinterpret_cast<T*>(&f);
+        } else {
+            unsigned short h = (unsigned short)b;
+            v = *reinterpret_cast<T*>(&h);
+        }
+        return v;
+    }
+};
+
 struct MaskGeo {
     int TD, ntiles;
-    int Ch, Cw;          // slot radix along h and w
+    int lch, lcw;        // log2 of the slot radix along h and w (powers of two)
+    int grows;           // window rows (od values) staged per tile, at most
     AxisMap ad, ah, aw;
     FastDiv fHW, fW, fOW, fOHOW;
 };
 
+// Sum of the gradients of the windows whose bits are set, in ascending bit
+// order (ascending (od, oh, ow)), from the tile's staged gradients.
 template <typename T>
-__device__ __forceinline__ T gather_bits(const T* __restrict__ go, long long gobase, const Geo& g,
+__device__ __forceinline__ T gather_bits(const T* __restrict__ gtile, int od_lo, const Geo& g,
                                          const MaskGeo& mg, int d, int local_hw, uint32_t bits) {
     const int h = mg.fW.div(local_hw);
     const int w = local_hw - h * g.W;
-    const int ld = mg.ad.lo(d), lh = mg.ah.lo(h), lw = mg.aw.lo(w);
+    const int ld = mg.ad.lo(d) - od_lo, lh = mg.ah.lo(h), lw = mg.aw.lo(w);
     float acc = 0.0f;
     bool any = false;
     while (bits) {
         const int slot = __ffs(bits) - 1;
         bits &= bits - 1;
-        const int jd = slot / (mg.Ch * mg.Cw);
-        const int rem = slot - jd * mg.Ch * mg.Cw;
-        const int jh = rem / mg.Cw;
-        const int jw = rem - jh * mg.Cw;
-        const long long o = gobase + ((long long)(ld + jd) * g.OH + (lh + jh)) * g.OW + (lw + jw);
-        const float v = Elem<T>::to_f(go[o]);
+        const int jd = slot >> (mg.lch + mg.lcw);
+        const int jh = (slot >> mg.lcw) & ((1 << mg.lch) - 1);
+        const int jw = slot & ((1 << mg.lcw) - 1);
+        const float v = Elem<T>::to_f(gtile[((ld + jd) * g.OH + (lh + jh)) * g.OW + (lw + jw)]);
         acc = any ? acc + v : v;
         any = true;
     }
@@ -390,24 +410,43 @@ template <typename T, int VEC>
 __global__ void __launch_bounds__(256)
 k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
                    Geo g, MaskGeo mg) {
+    constexpr int UNR = 8;                       // window loads in flight per thread
     extern __shared__ __align__(16) unsigned char smem[];
-    uint32_t* mask32 = reinterpret_cast<uint32_t*>(smem);
     const int HW = g.H * g.W;
     const int d0 = blockIdx.x * mg.TD;
     const int d1 = min(d0 + mg.TD, g.D);
     const int n = (d1 - d0) * HW;
+    const int mask_bytes = (mg.TD * HW + 15) / 16 * 16;
+    const int gtile_bytes = (mg.grows * g.OH * g.OW * (int)sizeof(T) + 15) / 16 * 16;
+    uint32_t* mask32 = reinterpret_cast<uint32_t*>(smem);
+    T* gtile = reinterpret_cast<T*>(smem + mask_bytes);
     const T zero = Elem<T>::from_f(0.0f);
     const int od_lo = mg.ad.lo(d0), od_hi = mg.ad.hi(d1 - 1);
     const int ohow = g.OH * g.OW;
+    const int wbeg = od_lo * ohow;
+    const int wend = (od_hi + 1) * ohow;          // empty when od_lo > od_hi
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
         uint4* m16 = reinterpret_cast<uint4*>(smem);
         for (int i = threadIdx.x; i < (n + 15) / 16; i += blockDim.x) m16[i] = make_uint4(0, 0, 0, 0);
         __syncthreads();
+        // Phase 1: stage the gradients, mark each window's winner.
         const long long obase = p * (long long)g.ovol;
-        if (od_lo <= od_hi) {
-            const int wend = (od_hi + 1) * ohow;
-            for (int wi = od_lo * ohow + threadIdx.x; wi < wend; wi += blockDim.x) {
-                const long long local64 = __ldg(idx + obase + wi) - (long long)d0 * HW;
+        for (int wb = wbeg; wb < wend; wb += UNR * blockDim.x) {
+            int64_t j[UNR];
+            T gv[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int wi = wb + u * blockDim.x + threadIdx.x;
+                const bool ok = wi < wend;
+                j[u] = ok ? __ldg(idx + obase + wi) : -1;
+                gv[u] = ok ? go[obase + wi] : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int wi = wb + u * blockDim.x + threadIdx.x;
+                if (wi >= wend) continue;
+                gtile[wi - wbeg] = gv[u];
+                const long long local64 = j[u] - (long long)d0 * HW;
                 if (local64 < 0 || local64 >= n) continue;
                 const int local = (int)local64;
                 const int od = mg.fOHOW.div(wi);
@@ -420,40 +459,76 @@ k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
                 const int w = r - h * g.W;
                 const int d = d0 + dd;
                 if (!mg.ad.covers(od, d) || !mg.ah.covers(oh, h) || !mg.aw.covers(ow, w)) continue;
-                const int slot = ((od - mg.ad.lo(d)) * mg.Ch + (oh - mg.ah.lo(h))) * mg.Cw +
+                const int slot = (((od - mg.ad.lo(d)) << mg.lch | (oh - mg.ah.lo(h))) << mg.lcw) |
                                  (ow - mg.aw.lo(w));
                 atomicOr(&mask32[local >> 2], 1u << ((local & 3) * 8 + slot));
             }
         }
         __syncthreads();
+        // Phase 2: every input of the tile, from its mask byte. A warp takes
+        // 32 chunks at a time; lanes publish the elements that have bits set
+        // to a per-warp list (in lane, then element order), the 32 lanes sum
+        // the list entries in parallel, and each lane then assembles its
+        // chunk from zeros and its entries and stores it with one 16-byte
+        // store. This keeps the (rare, uneven) sums from serialising a warp.
         T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
         const int nchunks = (VEC > 1) ? n / VEC : 0;
-        for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+        const int lane = threadIdx.x & 31;
+        uint32_t* list = reinterpret_cast<uint32_t*>(smem + mask_bytes + gtile_bytes) +
+                         (threadIdx.x >> 5) * (32 * VEC);
+        for (int cb = threadIdx.x - lane; cb < nchunks; cb += blockDim.x) {
+            const int c = cb + lane;
+            const bool live = c < nchunks;
             const int r0 = c * VEC;
             uint32_t mw[VEC / 4 > 0 ? VEC / 4 : 1];
 #pragma unroll
-            for (int k = 0; k < VEC / 4; ++k) mw[k] = mask32[(r0 >> 2) + k];
-            uint32_t anyb = 0;
+            for (int k = 0; k < VEC / 4; ++k) mw[k] = live ? mask32[(r0 >> 2) + k] : 0u;
+            uint32_t nz = 0;
 #pragma unroll
-            for (int k = 0; k < VEC / 4; ++k) anyb |= mw[k];
-            Vec16<T> o;
-            if (anyb == 0) {
+            for (int i = 0; i < VEC; ++i)
+                nz |= (((mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu) != 0 ? 1u : 0u) << i;
+            const int cnt = __popc(nz);
+            int incl = cnt;
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) o.e[i] = zero;
-            } else {
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const uint32_t b = (mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu;
-                    if (b == 0) {
-                        o.e[i] = zero;
-                    } else {
-                        const int local = r0 + i;
-                        const int dd = mg.fHW.div(local);
-                        o.e[i] = gather_bits<T>(go, obase, g, mg, d0 + dd, local - dd * HW, b);
-                    }
-                }
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
             }
-            *reinterpret_cast<uint4*>(out + r0) = o.u;
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            const int first = incl - cnt;
+            if (total == 0) {
+                if (live) {
+                    Vec16<T> o;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) o.e[i] = zero;
+                    *reinterpret_cast<uint4*>(out + r0) = o.u;
+                }
+                continue;
+            }
+            {
+                int k = first;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i)
+                    if (nz >> i & 1u)
+                        list[k++] = (uint32_t)(r0 + i) << 8 | ((mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu);
+            }
+            __syncwarp();
+            for (int e = lane; e < total; e += 32) {
+                const uint32_t ent = list[e];
+                const int local = (int)(ent >> 8);
+                const int dd = mg.fHW.div(local);
+                const T v = gather_bits<T>(gtile, od_lo, g, mg, d0 + dd, local - dd * HW, ent & 0xFFu);
+                list[e] = (uint32_t)Elem16<T>::bits(v);
+            }
+            __syncwarp();
+            if (live) {
+                Vec16<T> o;
+                int k = first;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) o.e[i] = (nz >> i & 1u) ? Elem16<T>::from_bits(list[k++]) : zero;
+                *reinterpret_cast<uint4*>(out + r0) = o.u;
+            }
+            __syncwarp();
         }
         for (int e = nchunks * VEC + threadIdx.x; e < n; e += blockDim.x) {
             const uint32_t b = (mask32[e >> 2] >> ((e & 3) * 8)) & 0xFFu;
@@ -461,7 +536,7 @@ k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
                 out[e] = zero;
             } else {
                 const int dd = mg.fHW.div(e);
-                out[e] = gather_bits<T>(go, obase, g, mg, d0 + dd, e - dd * HW, b);
+                out[e] = gather_bits<T>(gtile, od_lo, g, mg, d0 + dd, e - dd * HW, b);
             }
         }
         __syncthreads();
@@ -527,7 +602,7 @@ cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi, co
 
 // ------------------------------------------------------------------ launch: masks
 
-static constexpr int kMaskBytes = 56 * 1024;   // shared bytes for one tile's masks
+static constexpr int kMaskBytes = 72 * 1024;   // shared bytes per tile: masks + gradients
 
 // Most windows that can cover one position along an axis.
 static int max_cover(int I, int O, int K, int S, bool adaptive) {
@@ -546,13 +621,50 @@ static AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
     return a;
 }
 
+static int pow2_at_least(int c) {
+    int p = 1;
+    while (p < c) p <<= 1;
+    return p;
+}
+
+static int log2_exact(int p) {
+    int l = 0;
+    while ((1 << l) < p) ++l;
+    return l;
+}
+
+// Window rows (od values) that can cover one tile of td slices, at most.
+static int max_window_rows(const Geo& g, int td) {
+    int best = 0;
+    for (int d0 = 0; d0 < g.D; d0 += td) {
+        const int d1 = (d0 + td < g.D ? d0 + td : g.D) - 1;
+        int lo, hi;
+        if (g.adaptive) {
+            lo = (int)(((long long)d0 * g.OD) / g.D);
+            hi = (int)(((long long)(d1 + 1) * g.OD - 1) / g.D);
+        } else {
+            lo = d0 < g.kd ? 0 : (d0 - g.kd) / g.sd + 1;
+            hi = d1 / g.sd < g.OD - 1 ? d1 / g.sd : g.OD - 1;
+        }
+        if (hi - lo + 1 > best) best = hi - lo + 1;
+    }
+    return best;
+}
+
+static size_t mask_smem_bytes(const Geo& g, int td, int es) {
+    const size_t masks = ((size_t)td * g.H * g.W + 15) / 16 * 16;
+    const size_t gt = ((size_t)max_window_rows(g, td) * g.OH * g.OW * es + 15) / 16 * 16;
+    const size_t lists = 8 * 32 * (16 / es) * 4;     // per-warp entry lists (256 threads)
+    return masks + gt + lists;
+}
+
 bool bwd_mask_supported(const Geo& g) {
     const bool a = g.adaptive != 0;
-    const long long slots = (long long)max_cover(g.D, g.OD, g.kd, g.sd, a) *
-                            max_cover(g.H, g.OH, g.kh, g.sh, a) *
-                            max_cover(g.W, g.OW, g.kw, g.sw, a);
+    const long long slots = (long long)pow2_at_least(max_cover(g.D, g.OD, g.kd, g.sd, a)) *
+                            pow2_at_least(max_cover(g.H, g.OH, g.kh, g.sh, a)) *
+                            pow2_at_least(max_cover(g.W, g.OW, g.kw, g.sw, a));
     if (slots > 8) return false;
-    if ((long long)g.H * g.W > kMaskBytes) return false;
+    if (mask_smem_bytes(g, 1, 4) > (size_t)kMaskBytes) return false;
     if (a) {   // products used by the adaptive window arithmetic stay below 2^31
         const long long lim = (1LL << 31) - 1;
         if ((long long)g.D * g.OD + g.OD > lim || (long long)g.H * g.OH + g.OH > lim ||
@@ -564,9 +676,7 @@ bool bwd_mask_supported(const Geo& g) {
 
 template <typename T, int VEC>
 static cudaError_t bwd_mask_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
-                                   const MaskGeo& mg, cudaStream_t s) {
-    const int HW = g.H * g.W;
-    const size_t smem = (((size_t)mg.TD * HW) + 15) / 16 * 16;
+                                   const MaskGeo& mg, size_t smem, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_overlap_mask<T, VEC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -582,8 +692,8 @@ static cudaError_t bwd_mask_t(const void* go, const int64_t* idx, void* gi, cons
     const bool a = g.adaptive != 0;
     const int HW = g.H * g.W;
     MaskGeo mg;
-    mg.Ch = max_cover(g.H, g.OH, g.kh, g.sh, a);
-    mg.Cw = max_cover(g.W, g.OW, g.kw, g.sw, a);
+    mg.lch = log2_exact(pow2_at_least(max_cover(g.H, g.OH, g.kh, g.sh, a)));
+    mg.lcw = log2_exact(pow2_at_least(max_cover(g.W, g.OW, g.kw, g.sw, a)));
     mg.ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
     mg.ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
     mg.aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
@@ -591,21 +701,23 @@ static cudaError_t bwd_mask_t(const void* go, const int64_t* idx, void* gi, cons
     mg.fW = FastDiv((uint32_t)g.W);
     mg.fOW = FastDiv((uint32_t)g.OW);
     mg.fOHOW = FastDiv((uint32_t)(g.OH * g.OW));
-    int td = kMaskBytes / HW;
-    if (td > g.D) td = g.D;
-    if (td < 1) td = 1;
+    // Deepest tile whose masks and staged gradients fit the shared budget.
+    int td = g.D;
+    while (td > 1 && mask_smem_bytes(g, td, sizeof(T)) > (size_t)kMaskBytes) --td;
     // 16-byte stores need every tile (and plane) to start on a 16-byte boundary.
     bool vec = (uintptr_t)gi % 16 == 0 && ((long long)g.vol * sizeof(T)) % 16 == 0;
-    if (vec) {
+    if (vec && td < g.D) {
         int t = td;
         while (t > 0 && ((long long)t * HW * sizeof(T)) % 16 != 0) --t;
-        if (t > 0 || td == g.D) td = t > 0 ? t : td;
-        vec = ((long long)td * HW * sizeof(T)) % 16 == 0 || td == g.D;
+        if (t > 0) td = t;
+        else vec = false;
     }
     mg.TD = td;
     mg.ntiles = (g.D + td - 1) / td;
-    if (vec) return bwd_mask_launch<T, VEC>(go, idx, gi, g, mg, s);
-    return bwd_mask_launch<T, 1>(go, idx, gi, g, mg, s);
+    mg.grows = max_window_rows(g, td);
+    const size_t smem = mask_smem_bytes(g, td, sizeof(T));
+    if (vec) return bwd_mask_launch<T, VEC>(go, idx, gi, g, mg, smem, s);
+    return bwd_mask_launch<T, 1>(go, idx, gi, g, mg, smem, s);
 }
 
 cudaError_t launch_bwd_overlap_mask(const void* go, const int64_t* idx, void* gi, const Geo& g,

@@ -237,117 +237,224 @@ __device__ __noinline__ void exact_window(const T* __restrict__ xp, int ds, int 
 
 constexpr uint32_t kLanes = 0x00010001u;   // a constant in both 16-bit lanes
 
-template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH>
-__global__ void __launch_bounds__(128)
-k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
-         int nq, int nt, int nc, long long nthreads) {
-    constexpr int NR = (TOH - 1) * SH + KH;          // rows of a full oh-tile
-    static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
-    const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (tid >= nthreads) return;
-    const int c = (int)(tid % nc);
-    long long t2 = tid / nc;
-    const int t = (int)(t2 % nt);
-    t2 /= nt;
-    const int q = (int)(t2 % nq);
-    const long long p = t2 / nq;
+// ---- bulk-copy pipeline helpers (mbarrier + cp.async.bulk, sm_90+) ----
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+// Bounded wait: gives up after `limit` polls (each poll may itself suspend
+// for a short, hardware-defined time) and reports failure.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit) {
+    for (int i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Set when a pipeline wait gave up (never expected); read and cleared by
+// mp3d_device_error_flags().
+__device__ unsigned int g_mp3d_device_error = 0;
+constexpr unsigned int kErrPipelineTimeout = 1u;
+constexpr int kWaitLimit = 1 << 22;
+
+// One CTA = (plane p, output-depth group, band of G oh-tiles of TOH rows).
+// Threads = nc chunks x G tiles. Each depth slice's band of input rows is
+// one contiguous span of memory; thread 0 streams slice after slice into a
+// ring of NS shared-memory stages with cp.async.bulk, completion counted by
+// an mbarrier per stage; every thread reduces its chunk's rows from shared
+// memory. Outputs of one output depth are staged in shared memory and
+// written with coalesced stores.
+template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS>
+__global__ void __launch_bounds__(256)
+k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
+         int nq, int G, int nbands, int nc) {
+    static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int band = (int)(blockIdx.x % nbands);
+    long long rest = blockIdx.x / nbands;
+    const int q = (int)(rest % nq);
+    const long long p = rest / nq;
+
+    const int tid = threadIdx.x;
+    const int c = tid % nc;
+    const int tl = tid / nc;                       // tile inside the band
     const int ow0 = 4 * c, w0 = 8 * c;
-    const int oh0 = t * TOH;
-    const int nh = min(TOH, g.OH - oh0);
+    const int oh_band = band * G * TOH;            // first output row of the band
+    const int oh_band_end = min(g.OH, oh_band + G * TOH);
+    const int oh0 = oh_band + tl * TOH;
+    const int nh = max(0, min(TOH, oh_band_end - oh0));
     const int od0 = q * odg;
     const int nd = min(odg, g.OD - od0);
     const int HW = g.H * g.W;
-    const T* xp = x + p * g.vol;
     const bool has_extra = (KW > 2) && (w0 + 8 < g.W);
-    const int hbeg = oh0 * SH;
-    const int nrows = (nh - 1) * SH + KH;
+    const int band_rows = (oh_band_end - oh_band - 1) * SH + KH;
+    const uint32_t span_bytes = (uint32_t)band_rows * g.W * sizeof(T);
+    const uint32_t stage_stride = (span_bytes + 127) / 128 * 128;
+    const int out_rows = oh_band_end - oh_band;
+    // shared layout: [NS stages][staged y][staged idx][NS mbarriers]
+    unsigned char* stages = smem;
+    uint16_t* ys = reinterpret_cast<uint16_t*>(smem + NS * stage_stride);
+    const int nout = out_rows * g.OW;
+    int64_t* is = reinterpret_cast<int64_t*>(smem + NS * stage_stride + ((nout * 2 + 15) / 16) * 16);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(is) + nout * 8);
+
+    const T* xp = x + p * g.vol;
+    const T* band_src = xp + (long long)oh_band * SH * g.W;
+    const int nslices = (KD >= SD) ? nd * SD + KD - SD : nd * KD;
+    auto slice_d = [&](int k) { return (KD >= SD) ? od0 * SD + k : (od0 + k / KD) * SD + k % KD; };
+
+    if (tid == 0) {
+        for (int st = 0; st < NS; ++st) mbar_init(smem_addr(&bars[st]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int k = 0; k < NS && k < nslices; ++k) {
+            const uint32_t bar = smem_addr(&bars[k]);
+            mbar_expect_tx(bar, span_bytes);
+            bulk_g2s(smem_addr(stages + k * stage_stride), band_src + (long long)slice_d(k) * HW,
+                     span_bytes, bar);
+        }
+    }
 
     uint32_t poison = 0;
+    bool failed = false;
     uint32_t cv[TOH][2], cc[TOH][2], pv[TOH][2], pc[TOH][2];
 #pragma unroll
     for (int j = 0; j < TOH; ++j)
 #pragma unroll
         for (int k = 0; k < 2; ++k) cv[j][k] = cc[j][k] = pv[j][k] = pc[j][k] = 0;
 
-    auto emit = [&](int od, uint32_t (&v)[TOH][2], uint32_t (&cd)[TOH][2]) {
+    // Stage this thread's outputs of depth od into shared memory.
+    auto stage_out = [&](int od, uint32_t (&v)[TOH][2], uint32_t (&cd)[TOH][2]) {
         const bool exact = Pair<T>::is_poisoned(poison);
 #pragma unroll
         for (int j = 0; j < TOH; ++j) {
             if (j >= nh) break;
             const int oh = oh0 + j;
-            const long long obase = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
 #pragma unroll
                 for (int lane = 0; lane < 2; ++lane) {
                     const int ow = ow0 + 2 * k + lane;
                     if (ow >= g.OW) continue;
+                    const int so = (oh - oh_band) * g.OW + ow;
                     if (exact) {
+                        T yv;
                         exact_window<T>(xp, od * SD, od * SD + KD, oh * SH, oh * SH + KH, ow * 2,
-                                        ow * 2 + KW, g.W, HW, y + obase + ow, idx + obase + ow);
+                                        ow * 2 + KW, g.W, HW, &yv, &is[so]);
+                        ys[so] = *reinterpret_cast<uint16_t*>(&yv);
                         continue;
                     }
                     const uint32_t code = (cd[j][k] >> (16 * lane)) & 0xFFFFu;
                     const int wl = code & 3, hl = (code >> 2) & 3, dl = (code >> 4) & 3;
-                    const uint16_t bitsv = (uint16_t)((v[j][k] >> (16 * lane)) & 0xFFFFu);
-                    reinterpret_cast<uint16_t*>(y)[obase + ow] = bitsv;
-                    idx[obase + ow] = (int64_t)(od * SD + dl) * HW + (oh * SH + hl) * g.W + ow * 2 + wl;
+                    ys[so] = (uint16_t)((v[j][k] >> (16 * lane)) & 0xFFFFu);
+                    is[so] = (int64_t)(od * SD + dl) * HW + (oh * SH + hl) * g.W + ow * 2 + wl;
                 }
         }
     };
+    // Write the staged outputs of depth od with coalesced stores.
+    auto flush_out = [&](int od) {
+        __syncthreads();
+        const long long obase = ((p * g.OD + od) * g.OH + oh_band) * (long long)g.OW;
+        uint16_t* yd = reinterpret_cast<uint16_t*>(y) + obase;
+        int64_t* id = idx + obase;
+        for (int k = tid; k < nout; k += blockDim.x) {
+            yd[k] = ys[k];
+            id[k] = is[k];
+        }
+        __syncthreads();
+    };
 
+    int sl = 0;   // slices consumed so far
     for (int od = od0; od <= od0 + nd; ++od) {
 #pragma unroll
         for (int i = 0; i < SD; ++i) {
             const bool role_cur = (od < od0 + nd) && (i < KD);
             const bool role_prev = (od > od0) && (SD + i < KD);
             if (!role_cur && !role_prev) continue;
-            const int d = od * SD + i;
+            const int stage = sl % NS;
+            const uint32_t parity = (uint32_t)((sl / NS) & 1);
+            if (!failed && !mbar_wait(smem_addr(&bars[stage]), parity, kWaitLimit)) {
+                failed = true;
+                atomicOr(&g_mp3d_device_error, kErrPipelineTimeout);
+            }
+            const unsigned char* buf = stages + stage * stage_stride;
             uint32_t hv[TOH][2], hc[TOH][2];
 #pragma unroll
             for (int j = 0; j < TOH; ++j) hv[j][0] = hv[j][1] = hc[j][0] = hc[j][1] = 0;
+            if (nh > 0) {
+                const int nrows = (nh - 1) * SH + KH;
+                const int rbase = tl * TOH * SH;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                if (r >= nrows) break;
-                const T* row = xp + (long long)d * HW + (long long)(hbeg + r) * g.W + w0;
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row));
-                uint32_t e8 = 0;
-                if (KW > 2 && has_extra) e8 = __ldg(reinterpret_cast<const unsigned short*>(row + 8));
-                poison = Pair<T>::poison(poison, raw.x);
-                poison = Pair<T>::poison(poison, raw.y);
-                poison = Pair<T>::poison(poison, raw.z);
-                poison = Pair<T>::poison(poison, raw.w);
-                if (KW > 2) poison = Pair<T>::poison(poison, e8);
-                // W: outputs (0,1) from words x,y (+z), outputs (2,3) from z,w (+e8)
-                uint32_t wv[2], wc[2];
-                wv[0] = __byte_perm(raw.x, raw.y, 0x5410);
-                wc[0] = 0;
-                merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 1u * kLanes);
-                wv[1] = __byte_perm(raw.z, raw.w, 0x5410);
-                wc[1] = 0;
-                merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 1u * kLanes);
-                if (KW > 2) {
-                    merge2<T>(wv[0], wc[0], __byte_perm(raw.y, raw.z, 0x5410), 2u * kLanes);
-                    merge2<T>(wv[1], wc[1], __byte_perm(raw.w, e8, 0x5410), 2u * kLanes);
-                }
-                // H: row r is row hl = r - j*SH of output row j
+                for (int r = 0; r < (TOH - 1) * SH + KH; ++r) {
+                    if (r >= nrows) break;
+                    const unsigned char* row = buf + ((rbase + r) * g.W + w0) * sizeof(T);
+                    const uint4 raw = *reinterpret_cast<const uint4*>(row);
+                    uint32_t e8 = 0;
+                    if (KW > 2 && has_extra) e8 = *reinterpret_cast<const unsigned short*>(row + 16);
+                    poison = Pair<T>::poison(poison, raw.x);
+                    poison = Pair<T>::poison(poison, raw.y);
+                    poison = Pair<T>::poison(poison, raw.z);
+                    poison = Pair<T>::poison(poison, raw.w);
+                    if (KW > 2) poison = Pair<T>::poison(poison, e8);
+                    uint32_t wv[2], wc[2];
+                    wv[0] = __byte_perm(raw.x, raw.y, 0x5410);
+                    wc[0] = 0;
+                    merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 1u * kLanes);
+                    wv[1] = __byte_perm(raw.z, raw.w, 0x5410);
+                    wc[1] = 0;
+                    merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 1u * kLanes);
+                    if (KW > 2) {
+                        merge2<T>(wv[0], wc[0], __byte_perm(raw.y, raw.z, 0x5410), 2u * kLanes);
+                        merge2<T>(wv[1], wc[1], __byte_perm(raw.w, e8, 0x5410), 2u * kLanes);
+                    }
 #pragma unroll
-                for (int j = 0; j < TOH; ++j) {
-                    const int hl = r - j * SH;
-                    if (hl < 0 || hl >= KH) continue;
+                    for (int j = 0; j < TOH; ++j) {
+                        const int hl = r - j * SH;
+                        if (hl < 0 || hl >= KH) continue;
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        if (hl == 0) {
-                            hv[j][k] = wv[k];
-                            hc[j][k] = wc[k];
-                        } else {
-                            merge2<T>(hv[j][k], hc[j][k], wv[k], wc[k] | ((uint32_t)hl << 2) * kLanes);
+                        for (int k = 0; k < 2; ++k) {
+                            if (hl == 0) {
+                                hv[j][k] = wv[k];
+                                hc[j][k] = wc[k];
+                            } else {
+                                merge2<T>(hv[j][k], hc[j][k], wv[k], wc[k] | ((uint32_t)hl << 2) * kLanes);
+                            }
                         }
                     }
                 }
             }
-            // D: slice d is depth dl = i of od, and dl = SD + i of od - 1
+            // Every thread is done reading this stage: refill it.
+            __syncthreads();
+            if (tid == 0 && sl + NS < nslices && !failed) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bar = smem_addr(&bars[stage]);
+                mbar_expect_tx(bar, span_bytes);
+                bulk_g2s(smem_addr(stages + stage * stage_stride),
+                         band_src + (long long)slice_d(sl + NS) * HW, span_bytes, bar);
+            }
+            ++sl;
 #pragma unroll
             for (int j = 0; j < TOH; ++j)
 #pragma unroll
@@ -363,8 +470,14 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                         }
                     }
                 }
-            if (role_prev && SD + i == KD - 1) emit(od - 1, pv, pc);
-            if (role_cur && i == KD - 1) emit(od, cv, cc);
+            if (role_prev && SD + i == KD - 1) {
+                if (!failed) stage_out(od - 1, pv, pc);
+                flush_out(od - 1);
+            }
+            if (role_cur && i == KD - 1) {
+                if (!failed) stage_out(od, cv, cc);
+                flush_out(od);
+            }
         }
 #pragma unroll
         for (int j = 0; j < TOH; ++j)
@@ -373,6 +486,11 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                 pv[j][k] = cv[j][k];
                 pc[j][k] = cc[j][k];
             }
+    }
+    // After a timeout, let copies still in flight land before the CTA exits.
+    if (failed && tid == 0) {
+        for (int k = (sl > NS ? sl - NS : 0); k < sl && k < nslices; ++k)
+            mbar_wait(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1), kWaitLimit);
     }
 }
 
@@ -391,22 +509,31 @@ bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
 template <typename T, int KD, int SD, int KH, int SH, int KW>
 static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                             cudaStream_t s) {
-    constexpr int TOH = 4;
+    constexpr int TOH = 4, NS = 3;
     const int nc = g.W / 8;
     const int nt = (g.OH + TOH - 1) / TOH;
-    const long long base = g.P * nt * (long long)nc;
-    // Split the output depths across threads until there are enough threads
-    // to keep every SM busy (about 4096 per SM).
-    const long long target = (long long)sms * 4096;
+    // Band of G tiles: at most 256 threads and 16 KB of input rows per stage.
+    int G = 256 / nc;
+    if (G > nt) G = nt;
+    while (G > 1 && ((long long)((G * TOH - 1) * SH + KH) * g.W * sizeof(T)) > 16384) --G;
+    const int nbands = (nt + G - 1) / G;
+    // Split output depths into groups until there are about 8 CTAs per SM.
+    const long long base = g.P * nbands;
+    const long long target = (long long)sms * 8;
     long long want = (target + base - 1) / base;
     if (want < 1) want = 1;
     if (want > g.OD) want = g.OD;
     const int odg = (int)((g.OD + want - 1) / want);
     const int nq = (g.OD + odg - 1) / odg;
-    const long long n = base * nq;
-    const long long blocks = (n + 127) / 128;
-    k_fwd_s2<T, KD, SD, KH, SH, KW, TOH><<<(unsigned)blocks, 128, 0, s>>>(
-        (const T*)x, (T*)y, idx, g, odg, nq, nt, nc, n);
+    const int band_rows = (G * TOH - 1) * SH + KH;
+    const size_t stage = ((size_t)band_rows * g.W * sizeof(T) + 127) / 128 * 128;
+    const int nout = G * TOH * g.OW;
+    const size_t smem = NS * stage + ((size_t)nout * 2 + 15) / 16 * 16 + (size_t)nout * 8 + NS * 8;
+    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long blocks = g.P * nq * nbands;
+    kern<<<(unsigned)blocks, nc * G, smem, s>>>((const T*)x, (T*)y, idx, g, odg, nq, G, nbands, nc);
     return cudaGetLastError();
 }
 
@@ -425,6 +552,17 @@ cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g, in
     if (dtype == F16) return fwd_s2_dispatch<__half>(x, y, idx, g, sms, s);
     if (dtype == BF16) return fwd_s2_dispatch<__nv_bfloat16>(x, y, idx, g, sms, s);
     return cudaErrorNotSupported;
+}
+
+}  // namespace mp3d
+
+namespace mp3d {
+
+cudaError_t read_device_error(unsigned int* flags, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_mp3d_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_mp3d_device_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace mp3d

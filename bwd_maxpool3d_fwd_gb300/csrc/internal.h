@@ -21,6 +21,9 @@ cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g,
 // input on a 16-byte boundary; plan queries assume an aligned buffer).
 bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16);
 
+// Error flags set by kernels whose bounded waits gave up (fwd.cu).
+cudaError_t read_device_error(unsigned int* flags, bool clear);
+
 // Backward paths (bwd.cu). For the disjoint gather, g.kd..g.sw hold the
 // fixed window (adaptive divisible shapes are passed as kernel = stride =
 // input / output).

@@ -188,6 +188,15 @@ int maxpool3d_bwd_noalloc(const void* grad_out, const int64_t* idx, void* grad_i
                           int kd, int kh, int kw, int sd, int sh, int sw,
                           int dtype, cudaStream_t stream);
 
+/* Error flags raised on the device by a kernel whose bounded wait for an
+ * asynchronous copy gave up (bit 0: the forward's copy pipeline timed out;
+ * the kernel then leaves its outputs unwritten and exits). Not expected in
+ * normal operation. Reads the current device's flags into *flags (clearing
+ * them if clear != 0); this call waits for the device to finish prior work.
+ * No counterpart on the pages: it exists because the library's kernels
+ * never trap or spin without limit. */
+int mp3d_device_error_flags(unsigned int* flags, int clear);
+
 /* Static description of a status code (never NULL). */
 const char* mp3d_status_string(int status);
 

@@ -280,3 +280,8 @@ def test_disjoint_backward_row_chunks(case, dtype):
     g = torch.randn(i_ref.shape, generator=gen).to(dtype)
     assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
                       "grad_in")
+
+
+def test_no_device_error_flags_after_suite():
+    # The forward's copy pipeline never timed out during these tests.
+    assert mp.mp3d_device_error_flags(clear=True) == 0
