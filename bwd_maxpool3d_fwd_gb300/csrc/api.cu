@@ -41,7 +41,7 @@ const char* path_name(int path) {
     case MP3D_PATH_FWD_S2: return "fwd_s2";
     case MP3D_PATH_FWD_GLOBAL: return "fwd_global";
     case MP3D_PATH_BWD_DISJOINT: return "bwd_disjoint";
-    case MP3D_PATH_BWD_OVERLAP_MASK: return "bwd_overlap_mask";
+    case MP3D_PATH_BWD_OVERLAP_TILE: return "bwd_overlap_tile";
     case MP3D_PATH_BWD_OVERLAP_DIRECT: return "bwd_overlap_direct";
     case MP3D_PATH_BWD_ATOMIC: return "bwd_atomic";
     default: return "?";
@@ -158,7 +158,7 @@ int bwd_path(const Geo& g, int algo) {
     if (g.P == 0) return MP3D_PATH_NOOP;
     if (algo == MP3D_BWD_ATOMIC) return MP3D_PATH_BWD_ATOMIC;
     if (is_disjoint(g)) return MP3D_PATH_BWD_DISJOINT;
-    if (bwd_mask_supported(g)) return MP3D_PATH_BWD_OVERLAP_MASK;
+    if (bwd_tile_supported(g)) return MP3D_PATH_BWD_OVERLAP_TILE;
     return MP3D_PATH_BWD_OVERLAP_DIRECT;
 }
 
@@ -316,8 +316,8 @@ int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64
     case MP3D_PATH_BWD_DISJOINT:
         e = launch_bwd_disjoint(grad_out, idx, grad_in, gk, dtype, sms, stream);
         break;
-    case MP3D_PATH_BWD_OVERLAP_MASK:
-        e = launch_bwd_overlap_mask(grad_out, idx, grad_in, gk, dtype, sms, stream);
+    case MP3D_PATH_BWD_OVERLAP_TILE:
+        e = launch_bwd_overlap_tile(grad_out, idx, grad_in, gk, dtype, sms, stream);
         break;
     default:
         e = launch_bwd_overlap_direct(grad_out, idx, grad_in, gk, dtype, sms, stream);

@@ -319,28 +319,33 @@ k_bwd_disjoint_rows(const T* __restrict__ go, const int64_t* __restrict__ idx,
         }
     }
 }
-// ------------------------------------------------------------------ overlap, shared masks
-// Overlapping windows, deterministic gather in two phases per tile of TD
-// depth slices of one plane:
-//  1. Every window that can cover the tile reads its stored index; if the
-//     index falls in the tile, the window sets one bit in a per-input byte
-//     in shared memory. The bit (slot) is the window's rank among the
-//     input's covering windows in ascending (od, oh, ow) order:
-//     slot = (jd*Ch + jh)*Cw + jw with jd = od - (first window covering d)
-//     and likewise for h, w. Setting bits with atomicOr is order-free.
-//  2. Every input reads its byte: zero means no window picked it (+0); else
-//     it walks the set bits in ascending order, which is ascending
-//     (od, oh, ow), and sums the matching gradients in binary32, starting
-//     from the first, then rounds once.
-// The result equals enumerating the covering windows in order and checking
-// each stored index, with one index read per window instead of one per
-// (input, covering window) pair.
+// ------------------------------------------------------------------ overlap, tiles
+// Overlapping windows, deterministic gather. One CTA owns a tile of TD
+// depth slices of one plane and every input in it:
+//  1. It zero-fills the tile with 16-byte stores. Each window that can
+//     cover the tile reads its stored index j; if j lies in the tile and in
+//     the window, the window sets one bit in a per-input byte in shared
+//     memory: its slot, the rank of the window among the windows covering
+//     j in ascending (od, oh, ow) order, packed as (jd, jh, jw) with
+//     power-of-two radices. It records (j, slot) and stages its gradient.
+//  2. After a barrier (which also orders the zero stores before what
+//     follows) each window checks whether its slot is the lowest bit set on
+//     its j. That owner sums, in ascending bit order (= ascending
+//     (od, oh, ow)), its own gradient and those of the windows whose bits
+//     follow (found by slot offsets), in binary32, rounds once and stores.
+// Per input the work is a share of one vector store; per window, a few
+// integer operations, one shared atomic and, for owners, the sum.
 struct AxisMap {
     int I, O, K, S;
     int adaptive;
     FastDiv fS;   // fixed: divide by S
     FastDiv fI;   // adaptive: divide by I
     FastDiv fO;   // adaptive: divide by O
+    // Window o along this axis: [start(o), end(o)).
+    __device__ __forceinline__ int start(int o) const { return adaptive ? fO.div(o * I) : o * S; }
+    __device__ __forceinline__ int len(int o) const {
+        return adaptive ? fO.div((o + 1) * I + O - 1) - fO.div(o * I) : K;
+    }
     __device__ __forceinline__ int lo(int x) const {
         if (adaptive) return fI.div(x * O);
         return x < K ? 0 : fS.div(x - K) + 1;
@@ -350,87 +355,57 @@ struct AxisMap {
         const int h = fS.div(x);
         return h < O - 1 ? h : O - 1;
     }
-    __device__ __forceinline__ bool covers(int o, int x) const {
-        if (adaptive) return fO.div(o * I) <= x && x < fO.div((o + 1) * I + O - 1);
-        return o * S <= x && x < o * S + K;
+    // Windows before o that also cover position start(o) + rel.
+    __device__ __forceinline__ int earlier(int o, int rel) const {
+        if (adaptive) return o - lo(start(o) + rel);
+        const int e = fS.div(K - 1 - rel);
+        return e < o ? e : o;
     }
 };
 
-// Raw bits of an element in a 32-bit word, and back.
-template <typename T> struct Elem16 {
-    static __device__ __forceinline__ uint32_t bits(T v) {
-        if (sizeof(T) == 4) return __float_as_uint(*reinterpret_cast<float*>(&v));
-        return (uint32_t)*reinterpret_cast<unsigned short*>(&v);
-    }
-    static __device__ __forceinline__ T from_bits(uint32_t b) {
-        T v;
-        if (sizeof(T) == 4) {
-            float f = __uint_as_float(b);
-            v = *reinterpret_cast<T*>(&f);
-        } else {
-            unsigned short h = (unsigned short)b;
-            v = *reinterpret_cast<T*>(&h);
-        }
-        return v;
-    }
-};
-
-struct MaskGeo {
+struct TileGeo {
     int TD, ntiles;
-    int lch, lcw;        // log2 of the slot radix along h and w (powers of two)
-    int grows;           // window rows (od values) staged per tile, at most
+    int rows;             // window rows (od values) staged per tile, at most
+    int lch, lcw;         // log2 of the slot radix along h and w
     AxisMap ad, ah, aw;
     FastDiv fHW, fW, fOW, fOHOW;
 };
 
-// Sum of the gradients of the windows whose bits are set, in ascending bit
-// order (ascending (od, oh, ow)), from the tile's staged gradients.
-template <typename T>
-__device__ __forceinline__ T gather_bits(const T* __restrict__ gtile, int od_lo, const Geo& g,
-                                         const MaskGeo& mg, int d, int local_hw, uint32_t bits) {
-    const int h = mg.fW.div(local_hw);
-    const int w = local_hw - h * g.W;
-    const int ld = mg.ad.lo(d) - od_lo, lh = mg.ah.lo(h), lw = mg.aw.lo(w);
-    float acc = 0.0f;
-    bool any = false;
-    while (bits) {
-        const int slot = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int jd = slot >> (mg.lch + mg.lcw);
-        const int jh = (slot >> mg.lcw) & ((1 << mg.lch) - 1);
-        const int jw = slot & ((1 << mg.lcw) - 1);
-        const float v = Elem<T>::to_f(gtile[((ld + jd) * g.OH + (lh + jh)) * g.OW + (lw + jw)]);
-        acc = any ? acc + v : v;
-        any = true;
-    }
-    return Elem<T>::from_f(acc);
-}
-
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256)
-k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
-                   Geo g, MaskGeo mg) {
+k_bwd_overlap_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
+                   Geo g, TileGeo tg) {
     constexpr int UNR = 8;                       // window loads in flight per thread
     extern __shared__ __align__(16) unsigned char smem[];
     const int HW = g.H * g.W;
-    const int d0 = blockIdx.x * mg.TD;
-    const int d1 = min(d0 + mg.TD, g.D);
+    const int d0 = blockIdx.x * tg.TD;
+    const int d1 = min(d0 + tg.TD, g.D);
     const int n = (d1 - d0) * HW;
-    const int mask_bytes = (mg.TD * HW + 15) / 16 * 16;
-    const int gtile_bytes = (mg.grows * g.OH * g.OW * (int)sizeof(T) + 15) / 16 * 16;
-    uint32_t* mask32 = reinterpret_cast<uint32_t*>(smem);
-    T* gtile = reinterpret_cast<T*>(smem + mask_bytes);
-    const T zero = Elem<T>::from_f(0.0f);
-    const int od_lo = mg.ad.lo(d0), od_hi = mg.ad.hi(d1 - 1);
     const int ohow = g.OH * g.OW;
+    const int od_lo = tg.ad.lo(d0), od_hi = tg.ad.hi(d1 - 1);
     const int wbeg = od_lo * ohow;
     const int wend = (od_hi + 1) * ohow;          // empty when od_lo > od_hi
+    const int mask_bytes = (tg.TD * HW + 15) / 16 * 16;
+    uint32_t* mask32 = reinterpret_cast<uint32_t*>(smem);
+    int* wrec = reinterpret_cast<int*>(smem + mask_bytes);
+    T* gt = reinterpret_cast<T*>(smem + mask_bytes + (size_t)tg.rows * ohow * sizeof(int));
+    const T zero = Elem<T>::from_f(0.0f);
+    const int lo_j = d0 * HW, hi_j = d1 * HW;     // the tile's in-plane offsets
+    const int lhw = tg.lch + tg.lcw;
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
-        uint4* m16 = reinterpret_cast<uint4*>(smem);
-        for (int i = threadIdx.x; i < (n + 15) / 16; i += blockDim.x) m16[i] = make_uint4(0, 0, 0, 0);
-        __syncthreads();
-        // Phase 1: stage the gradients, mark each window's winner.
+        T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
         const long long obase = p * (long long)g.ovol;
+        uint4* m16 = reinterpret_cast<uint4*>(smem);
+        for (int i = threadIdx.x; i < mask_bytes / 16; i += blockDim.x) m16[i] = make_uint4(0, 0, 0, 0);
+        if (VEC > 1) {
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+            for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) o4[c] = make_uint4(0, 0, 0, 0);
+            for (int e = (n / VEC) * VEC + threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
+        } else {
+            for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
+        }
+        __syncthreads();
+        // 1. claims
         for (int wb = wbeg; wb < wend; wb += UNR * blockDim.x) {
             int64_t j[UNR];
             T gv[UNR];
@@ -445,99 +420,55 @@ k_bwd_overlap_mask(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
             for (int u = 0; u < UNR; ++u) {
                 const int wi = wb + u * blockDim.x + threadIdx.x;
                 if (wi >= wend) continue;
-                gtile[wi - wbeg] = gv[u];
-                const long long local64 = j[u] - (long long)d0 * HW;
-                if (local64 < 0 || local64 >= n) continue;
-                const int local = (int)local64;
-                const int od = mg.fOHOW.div(wi);
-                const int rem = wi - od * ohow;
-                const int oh = mg.fOW.div(rem);
-                const int ow = rem - oh * g.OW;
-                const int dd = mg.fHW.div(local);
-                const int r = local - dd * HW;
-                const int h = mg.fW.div(r);
-                const int w = r - h * g.W;
-                const int d = d0 + dd;
-                if (!mg.ad.covers(od, d) || !mg.ah.covers(oh, h) || !mg.aw.covers(ow, w)) continue;
-                const int slot = (((od - mg.ad.lo(d)) << mg.lch | (oh - mg.ah.lo(h))) << mg.lcw) |
-                                 (ow - mg.aw.lo(w));
-                atomicOr(&mask32[local >> 2], 1u << ((local & 3) * 8 + slot));
+                const int me = wi - wbeg;
+                gt[me] = gv[u];
+                int rec = -1;
+                if (j[u] >= lo_j && j[u] < hi_j) {
+                    const int jj = (int)j[u];
+                    const int od = tg.fOHOW.div(wi);
+                    const int rem = wi - od * ohow;
+                    const int oh = tg.fOW.div(rem);
+                    const int ow = rem - oh * g.OW;
+                    const int ds = tg.ad.start(od), hs = tg.ah.start(oh), ws = tg.aw.start(ow);
+                    const int rel = jj - (ds * HW + hs * g.W + ws);
+                    if (rel >= 0) {
+                        const int dl = tg.fHW.div(rel);
+                        const int r2 = rel - dl * HW;
+                        const int hl = tg.fW.div(r2);
+                        const int wl = r2 - hl * g.W;
+                        if (dl < tg.ad.len(od) && hl < tg.ah.len(oh) && wl < tg.aw.len(ow)) {
+                            const int slot = (tg.ad.earlier(od, dl) << lhw) |
+                                             (tg.ah.earlier(oh, hl) << tg.lcw) | tg.aw.earlier(ow, wl);
+                            const int local = jj - lo_j;
+                            atomicOr(&mask32[local >> 2], 1u << ((local & 3) * 8 + slot));
+                            rec = local << 3 | slot;
+                        }
+                    }
+                }
+                wrec[me] = rec;
             }
         }
         __syncthreads();
-        // Phase 2: every input of the tile, from its mask byte. A warp takes
-        // 32 chunks at a time; lanes publish the elements that have bits set
-        // to a per-warp list (in lane, then element order), the 32 lanes sum
-        // the list entries in parallel, and each lane then assembles its
-        // chunk from zeros and its entries and stores it with one 16-byte
-        // store. This keeps the (rare, uneven) sums from serialising a warp.
-        T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
-        const int nchunks = (VEC > 1) ? n / VEC : 0;
-        const int lane = threadIdx.x & 31;
-        uint32_t* list = reinterpret_cast<uint32_t*>(smem + mask_bytes + gtile_bytes) +
-                         (threadIdx.x >> 5) * (32 * VEC);
-        for (int cb = threadIdx.x - lane; cb < nchunks; cb += blockDim.x) {
-            const int c = cb + lane;
-            const bool live = c < nchunks;
-            const int r0 = c * VEC;
-            uint32_t mw[VEC / 4 > 0 ? VEC / 4 : 1];
-#pragma unroll
-            for (int k = 0; k < VEC / 4; ++k) mw[k] = live ? mask32[(r0 >> 2) + k] : 0u;
-            uint32_t nz = 0;
-#pragma unroll
-            for (int i = 0; i < VEC; ++i)
-                nz |= (((mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu) != 0 ? 1u : 0u) << i;
-            const int cnt = __popc(nz);
-            int incl = cnt;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
+        // 2. owners
+        for (int me = threadIdx.x; me < wend - wbeg; me += blockDim.x) {
+            const int rec = wrec[me];
+            if (rec < 0) continue;
+            const int local = rec >> 3, slot = rec & 7;
+            uint32_t m = (mask32[local >> 2] >> ((local & 3) * 8)) & 0xFFu;
+            if (__ffs(m) - 1 != slot) continue;
+            float acc = Elem<T>::to_f(gt[me]);
+            m &= m - 1;
+            const int sd = slot >> lhw, sh = (slot >> tg.lcw) & ((1 << tg.lch) - 1),
+                      sw = slot & ((1 << tg.lcw) - 1);
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                const int bd = b >> lhw, bh = (b >> tg.lcw) & ((1 << tg.lch) - 1),
+                          bw = b & ((1 << tg.lcw) - 1);
+                const int k = me + (bd - sd) * ohow + (bh - sh) * g.OW + (bw - sw);
+                acc += Elem<T>::to_f(gt[k]);
             }
-            const int total = __shfl_sync(0xffffffffu, incl, 31);
-            const int first = incl - cnt;
-            if (total == 0) {
-                if (live) {
-                    Vec16<T> o;
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) o.e[i] = zero;
-                    *reinterpret_cast<uint4*>(out + r0) = o.u;
-                }
-                continue;
-            }
-            {
-                int k = first;
-#pragma unroll
-                for (int i = 0; i < VEC; ++i)
-                    if (nz >> i & 1u)
-                        list[k++] = (uint32_t)(r0 + i) << 8 | ((mw[i >> 2] >> ((i & 3) * 8)) & 0xFFu);
-            }
-            __syncwarp();
-            for (int e = lane; e < total; e += 32) {
-                const uint32_t ent = list[e];
-                const int local = (int)(ent >> 8);
-                const int dd = mg.fHW.div(local);
-                const T v = gather_bits<T>(gtile, od_lo, g, mg, d0 + dd, local - dd * HW, ent & 0xFFu);
-                list[e] = (uint32_t)Elem16<T>::bits(v);
-            }
-            __syncwarp();
-            if (live) {
-                Vec16<T> o;
-                int k = first;
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) o.e[i] = (nz >> i & 1u) ? Elem16<T>::from_bits(list[k++]) : zero;
-                *reinterpret_cast<uint4*>(out + r0) = o.u;
-            }
-            __syncwarp();
-        }
-        for (int e = nchunks * VEC + threadIdx.x; e < n; e += blockDim.x) {
-            const uint32_t b = (mask32[e >> 2] >> ((e & 3) * 8)) & 0xFFu;
-            if (b == 0) {
-                out[e] = zero;
-            } else {
-                const int dd = mg.fHW.div(e);
-                out[e] = gather_bits<T>(gtile, od_lo, g, mg, d0 + dd, e - dd * HW, b);
-            }
+            out[local] = Elem<T>::from_f(acc);
         }
         __syncthreads();
     }
@@ -600,9 +531,9 @@ cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi, co
     }
 }
 
-// ------------------------------------------------------------------ launch: masks
+// ------------------------------------------------------------------ launch: tiles
 
-static constexpr int kMaskBytes = 72 * 1024;   // shared bytes per tile: masks + gradients
+static constexpr int kTileBytes = 110 * 1024;   // shared bytes per tile (two CTAs per SM)
 
 // Most windows that can cover one position along an axis.
 static int max_cover(int I, int O, int K, int S, bool adaptive) {
@@ -610,15 +541,6 @@ static int max_cover(int I, int O, int K, int S, bool adaptive) {
     if (adaptive) c = (O + I - 1) / I + 1;
     else c = K <= S ? 1 : (K + S - 1) / S;
     return c < O ? c : O;
-}
-
-static AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
-    AxisMap a;
-    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
-    a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
-    a.fI = FastDiv((uint32_t)I);
-    a.fO = FastDiv((uint32_t)O);
-    return a;
 }
 
 static int pow2_at_least(int c) {
@@ -631,6 +553,15 @@ static int log2_exact(int p) {
     int l = 0;
     while ((1 << l) < p) ++l;
     return l;
+}
+
+static AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
+    AxisMap a;
+    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
+    a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
+    a.fI = FastDiv((uint32_t)I);
+    a.fO = FastDiv((uint32_t)O);
+    return a;
 }
 
 // Window rows (od values) that can cover one tile of td slices, at most.
@@ -651,20 +582,21 @@ static int max_window_rows(const Geo& g, int td) {
     return best;
 }
 
-static size_t mask_smem_bytes(const Geo& g, int td, int es) {
+static size_t tile_smem_bytes(const Geo& g, int td, int es) {
     const size_t masks = ((size_t)td * g.H * g.W + 15) / 16 * 16;
-    const size_t gt = ((size_t)max_window_rows(g, td) * g.OH * g.OW * es + 15) / 16 * 16;
-    const size_t lists = 8 * 32 * (16 / es) * 4;     // per-warp entry lists (256 threads)
-    return masks + gt + lists;
+    const size_t wins = (size_t)max_window_rows(g, td) * g.OH * g.OW;
+    return masks + wins * sizeof(int) + (wins * es + 15) / 16 * 16;
 }
 
-bool bwd_mask_supported(const Geo& g) {
+bool bwd_tile_supported(const Geo& g) {
     const bool a = g.adaptive != 0;
     const long long slots = (long long)pow2_at_least(max_cover(g.D, g.OD, g.kd, g.sd, a)) *
                             pow2_at_least(max_cover(g.H, g.OH, g.kh, g.sh, a)) *
                             pow2_at_least(max_cover(g.W, g.OW, g.kw, g.sw, a));
     if (slots > 8) return false;
-    if (mask_smem_bytes(g, 1, 4) > (size_t)kMaskBytes) return false;
+    if (tile_smem_bytes(g, 1, 4) > (size_t)kTileBytes) return false;
+    // local offsets in a tile are packed with a 3-bit slot into an int
+    if ((long long)g.H * g.W * g.D >= (1LL << 28)) return false;
     if (a) {   // products used by the adaptive window arithmetic stay below 2^31
         const long long lim = (1LL << 31) - 1;
         if ((long long)g.D * g.OD + g.OD > lim || (long long)g.H * g.OH + g.OH > lim ||
@@ -675,36 +607,36 @@ bool bwd_mask_supported(const Geo& g) {
 }
 
 template <typename T, int VEC>
-static cudaError_t bwd_mask_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
-                                   const MaskGeo& mg, size_t smem, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_overlap_mask<T, VEC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+static cudaError_t bwd_tile_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                   const TileGeo& tg, size_t smem, cudaStream_t s) {
+    auto kern = k_bwd_overlap_tile<T, VEC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)mg.ntiles, (unsigned)(g.P < 65535 ? g.P : 65535));
-    k_bwd_overlap_mask<T, VEC><<<grid, 256, smem, s>>>((const T*)go, idx, (T*)gi, g, mg);
+    dim3 grid((unsigned)tg.ntiles, (unsigned)(g.P < 65535 ? g.P : 65535));
+    kern<<<grid, 256, smem, s>>>((const T*)go, idx, (T*)gi, g, tg);
     return cudaGetLastError();
 }
 
 template <typename T>
-static cudaError_t bwd_mask_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
+static cudaError_t bwd_tile_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
                               cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     const bool a = g.adaptive != 0;
     const int HW = g.H * g.W;
-    MaskGeo mg;
-    mg.lch = log2_exact(pow2_at_least(max_cover(g.H, g.OH, g.kh, g.sh, a)));
-    mg.lcw = log2_exact(pow2_at_least(max_cover(g.W, g.OW, g.kw, g.sw, a)));
-    mg.ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
-    mg.ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
-    mg.aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
-    mg.fHW = FastDiv((uint32_t)HW);
-    mg.fW = FastDiv((uint32_t)g.W);
-    mg.fOW = FastDiv((uint32_t)g.OW);
-    mg.fOHOW = FastDiv((uint32_t)(g.OH * g.OW));
-    // Deepest tile whose masks and staged gradients fit the shared budget.
+    TileGeo tg;
+    tg.lch = log2_exact(pow2_at_least(max_cover(g.H, g.OH, g.kh, g.sh, a)));
+    tg.lcw = log2_exact(pow2_at_least(max_cover(g.W, g.OW, g.kw, g.sw, a)));
+    tg.ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
+    tg.ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
+    tg.aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
+    tg.fHW = FastDiv((uint32_t)HW);
+    tg.fW = FastDiv((uint32_t)g.W);
+    tg.fOW = FastDiv((uint32_t)g.OW);
+    tg.fOHOW = FastDiv((uint32_t)(g.OH * g.OW));
+    // Deepest tile whose masks and staged windows fit the shared budget.
     int td = g.D;
-    while (td > 1 && mask_smem_bytes(g, td, sizeof(T)) > (size_t)kMaskBytes) --td;
-    // 16-byte stores need every tile (and plane) to start on a 16-byte boundary.
+    while (td > 1 && tile_smem_bytes(g, td, sizeof(T)) > (size_t)kTileBytes) --td;
+    // 16-byte fill stores need every tile (and plane) on a 16-byte boundary.
     bool vec = (uintptr_t)gi % 16 == 0 && ((long long)g.vol * sizeof(T)) % 16 == 0;
     if (vec && td < g.D) {
         int t = td;
@@ -712,20 +644,20 @@ static cudaError_t bwd_mask_t(const void* go, const int64_t* idx, void* gi, cons
         if (t > 0) td = t;
         else vec = false;
     }
-    mg.TD = td;
-    mg.ntiles = (g.D + td - 1) / td;
-    mg.grows = max_window_rows(g, td);
-    const size_t smem = mask_smem_bytes(g, td, sizeof(T));
-    if (vec) return bwd_mask_launch<T, VEC>(go, idx, gi, g, mg, smem, s);
-    return bwd_mask_launch<T, 1>(go, idx, gi, g, mg, smem, s);
+    tg.TD = td;
+    tg.ntiles = (g.D + td - 1) / td;
+    tg.rows = max_window_rows(g, td);
+    const size_t smem = tile_smem_bytes(g, td, sizeof(T));
+    if (vec) return bwd_tile_launch<T, VEC>(go, idx, gi, g, tg, smem, s);
+    return bwd_tile_launch<T, 1>(go, idx, gi, g, tg, smem, s);
 }
 
-cudaError_t launch_bwd_overlap_mask(const void* go, const int64_t* idx, void* gi, const Geo& g,
+cudaError_t launch_bwd_overlap_tile(const void* go, const int64_t* idx, void* gi, const Geo& g,
                                     int dtype, int, cudaStream_t s) {
     switch (dtype) {
-    case F32: return bwd_mask_t<float>(go, idx, gi, g, s);
-    case F16: return bwd_mask_t<__half>(go, idx, gi, g, s);
-    default: return bwd_mask_t<__nv_bfloat16>(go, idx, gi, g, s);
+    case F32: return bwd_tile_t<float>(go, idx, gi, g, s);
+    case F16: return bwd_tile_t<__half>(go, idx, gi, g, s);
+    default: return bwd_tile_t<__nv_bfloat16>(go, idx, gi, g, s);
     }
 }
 

@@ -31,10 +31,11 @@ cudaError_t launch_bwd_disjoint(const void* go, const int64_t* idx, void* gi,
                                 const Geo& g, int dtype, int sms, cudaStream_t s);
 cudaError_t launch_bwd_overlap_direct(const void* go, const int64_t* idx, void* gi,
                                       const Geo& g, int dtype, int sms, cudaStream_t s);
-cudaError_t launch_bwd_overlap_mask(const void* go, const int64_t* idx, void* gi,
+cudaError_t launch_bwd_overlap_tile(const void* go, const int64_t* idx, void* gi,
                                     const Geo& g, int dtype, int sms, cudaStream_t s);
-// Whether the shared-mask gather handles this geometry.
-bool bwd_mask_supported(const Geo& g);
+// Whether the tiled owner gather handles this geometry (its staged windows fit
+// in shared memory).
+bool bwd_tile_supported(const Geo& g);
 cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, float* ws,
                               const Geo& g, int dtype, int sms, cudaStream_t s);
 

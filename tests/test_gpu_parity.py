@@ -285,3 +285,25 @@ def test_disjoint_backward_row_chunks(case, dtype):
 def test_no_device_error_flags_after_suite():
     # The forward's copy pipeline never timed out during these tests.
     assert mp.mp3d_device_error_flags(clear=True) == 0
+
+
+# Overlapping shapes for the tiled owner gather: several tiles per plane,
+# inputs claimed by up to eight windows, ties (many shared winners).
+TILE_CASES = [((3, 3, 3), (2, 2, 2), (2, 3, 40, 30, 24)), ((2, 2, 2), (1, 1, 1), (1, 2, 20, 33, 17)),
+              ((3, 2, 3), (2, 1, 2), (2, 2, 13, 9, 40)), ((4, 4, 4), (3, 3, 3), (1, 2, 22, 19, 31)),
+              # large output planes: several depth tiles per plane, odd H*W
+              ((3, 3, 3), (2, 2, 2), (1, 2, 24, 112, 112)), ((3, 3, 3), (2, 2, 2), (1, 2, 20, 113, 114))]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(TILE_CASES)))
+def test_overlap_tile_backward(case, dtype):
+    k, s, shape = TILE_CASES[case]
+    out = mp.pool_out_size(shape[2:], k, s)
+    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_tile"
+    gen = torch.Generator().manual_seed(8000 + case)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
+                      "grad_in")
