@@ -474,6 +474,126 @@ k_bwd_overlap_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
     }
 }
 
+// ------------------------------------------------------------------ overlap, fixed windows
+// Overlapping fixed windows with kernel <= 2 * stride on every axis, window
+// shape known at compile time. Along each axis an input is then covered by
+// its window and at most one neighbour: the previous one when it sits in
+// the window's first K - S positions, the next one when it sits in the last
+// K - S positions. One CTA owns a tile of TD depth slices of one plane:
+//  1. stage, for every window that can cover the tile, its gradient and its
+//     winner as a tile-local int32 (-1 when outside the tile), and zero a
+//     dense shared-memory copy of the output tile;
+//  2. each window decodes its winner relative to its own window (compare
+//     chains), finds the windows that also cover it (itself plus at most
+//     one neighbour per axis, so at most eight) and walks them in ascending
+//     (od, oh, ow) order: if an earlier one chose the same input it stops,
+//     otherwise it is the owner and sums its gradient and those of the later
+//     ones that chose the same input, in binary32, rounds once, and writes
+//     the value into the shared tile;
+//  3. the tile leaves with 16-byte coalesced stores.
+// The ascending walk visits the eight sign patterns (sd, sh, sw) in {0,1}^3
+// as i ^ neg, where neg has a bit set for each axis whose neighbour is the
+// previous window: that order is ascending window order, and i == neg is
+// the window itself.
+template <typename T, int VEC, int KD, int SD, int KH, int SH, int KW, int SW>
+__global__ void __launch_bounds__(512)
+k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
+                    T* __restrict__ gi, Geo g, int TD, int rows_max, FastDiv fOH, FastDiv fOW) {
+    static_assert(KD <= 2 * SD && KH <= 2 * SH && KW <= 2 * SW && KD <= 4 && KH <= 4 && KW <= 4,
+                  "at most two covering windows per axis");
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int HW = g.H * g.W;
+    const int d0 = blockIdx.x * TD;
+    const int d1 = min(d0 + TD, g.D);
+    const int n = (d1 - d0) * HW;
+    const int od_lo = d0 < KD ? 0 : (d0 - KD) / SD + 1;
+    const int od_hi = min((d1 - 1) / SD, g.OD - 1);
+    const int ohow = g.OH * g.OW;
+    const int nwin = (od_hi >= od_lo) ? (od_hi - od_lo + 1) * ohow : 0;
+    int* jt = reinterpret_cast<int*>(smem);
+    T* gt = reinterpret_cast<T*>(smem + (size_t)rows_max * ohow * sizeof(int));
+    const long long lo_j = (long long)d0 * HW, hi_j = (long long)d1 * HW;
+    const T zero = Elem<T>::from_f(0.0f);
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        const long long obase = p * (long long)g.ovol + (long long)od_lo * ohow;
+        // 1. zero-fill the output tile and stage the windows
+        T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
+        if (VEC > 1) {
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+            for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) o4[c] = make_uint4(0, 0, 0, 0);
+            for (int e = (n / VEC) * VEC + threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
+        } else {
+            for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
+        }
+        constexpr int UNR = 4;
+        for (int wb = 0; wb < nwin; wb += UNR * blockDim.x) {
+            int64_t j[UNR];
+            T gv[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int me = wb + u * blockDim.x + threadIdx.x;
+                const bool ok = me < nwin;
+                j[u] = ok ? __ldg(idx + obase + me) : -1;
+                gv[u] = ok ? go[obase + me] : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int me = wb + u * blockDim.x + threadIdx.x;
+                if (me >= nwin) continue;
+                jt[me] = (j[u] >= lo_j && j[u] < hi_j) ? (int)(j[u] - lo_j) : -1;
+                gt[me] = gv[u];
+            }
+        }
+        __syncthreads();
+        // 2. owners: one window row (od, oh) per warp, lanes along ow; every
+        // lane runs the same predicated sequence (no early exits).
+        const int nrows = nwin / g.OW;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+        for (int rr = warp; rr < nrows; rr += nwarps) {
+            const int odr = fOH.div(rr);
+            const int oh = rr - odr * g.OH;
+            const int od = od_lo + odr;
+            const int rowstart = (od * SD) * HW + (oh * SH) * g.W - (int)lo_j;
+            for (int ow = lane; ow - lane < g.OW; ow += 32) {
+                const int me = rr * g.OW + ow;
+                const bool live = ow < g.OW;
+                const int jj = live ? jt[me] : -1;
+                const int rel = jj - (rowstart + ow * SW);
+                int dl = 0;
+#pragma unroll
+                for (int k = 1; k < KD; ++k) dl += (rel >= k * HW) ? 1 : 0;
+                const int r2 = rel - dl * HW;
+                int hl = 0;
+#pragma unroll
+                for (int k = 1; k < KH; ++k) hl += (r2 >= k * g.W) ? 1 : 0;
+                const int wl = r2 - hl * g.W;
+                const bool valid = jj >= 0 && rel >= 0 && rel < KD * HW && r2 < KH * g.W && wl < KW;
+                // neighbour per axis: -1 (previous window), +1 (next window) or none
+                const int ed = (dl < KD - SD && od > 0) ? -1 : ((dl >= SD && od + 1 < g.OD) ? 1 : 0);
+                const int eh = (hl < KH - SH && oh > 0) ? -1 : ((hl >= SH && oh + 1 < g.OH) ? 1 : 0);
+                const int ew = (wl < KW - SW && ow > 0) ? -1 : ((wl >= SW && ow + 1 < g.OW) ? 1 : 0);
+                const int neg = (ed < 0 ? 4 : 0) | (eh < 0 ? 2 : 0) | (ew < 0 ? 1 : 0);
+                const int have = (ed != 0 ? 4 : 0) | (eh != 0 ? 2 : 0) | (ew != 0 ? 1 : 0);
+                const int step_d = ed * ohow, step_h = eh * g.OW;
+                bool earlier = false;
+                float acc = valid ? Elem<T>::to_f(gt[me]) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int sel = i ^ neg;
+                    const bool use = valid && sel != 0 && (sel & ~have) == 0;
+                    const int k = me + ((sel & 4) ? step_d : 0) + ((sel & 2) ? step_h : 0) + ((sel & 1) ? ew : 0);
+                    const bool hit = use && jt[use ? k : 0] == jj;
+                    earlier |= hit && i < neg;
+                    if (hit && i > neg) acc += Elem<T>::to_f(gt[k]);
+                }
+                if (valid && !earlier) out[jj] = Elem<T>::from_f(acc);
+            }
+        }
+        __syncthreads();
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------------ launch: disjoint
 
 template <typename T, int SW>
@@ -617,10 +737,61 @@ static cudaError_t bwd_tile_launch(const void* go, const int64_t* idx, void* gi,
     return cudaGetLastError();
 }
 
+// Window shapes with a compiled fixed-window overlap kernel.
+static int fixed_variant(const Geo& g) {
+    if (g.adaptive) return -1;
+    if (g.kd == 3 && g.sd == 2 && g.kh == 3 && g.sh == 2 && g.kw == 3 && g.sw == 2) return 0;
+    if (g.kd == 2 && g.sd == 1 && g.kh == 2 && g.sh == 1 && g.kw == 2 && g.sw == 1) return 1;
+    return -1;
+}
+
+static constexpr int kFixedTileBytes = 72 * 1024;    // shared bytes per tile (three CTAs per SM)
+
+static size_t fixed_smem_bytes(const Geo& g, int td, int es) {
+    return (size_t)max_window_rows(g, td) * g.OH * g.OW * (sizeof(int) + es);
+}
+
+template <typename T, int KD, int SD, int KH, int SH, int KW, int SW>
+static cudaError_t bwd_fixed_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                    int td, cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
+    const size_t smem = fixed_smem_bytes(g, td, sizeof(T));
+    auto kern = k_bwd_overlap_fixed<T, VEC, KD, SD, KH, SH, KW, SW>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((g.D + td - 1) / td), (unsigned)(g.P < 65535 ? g.P : 65535));
+    kern<<<grid, 512, smem, s>>>((const T*)go, idx, (T*)gi, g, td, max_window_rows(g, td),
+                                 FastDiv((uint32_t)g.OH), FastDiv((uint32_t)g.OW));
+    return cudaGetLastError();
+}
+
+// The fixed-window kernel when the shape has a variant, the tile fits and
+// tiles start on 16-byte boundaries; cudaErrorNotSupported otherwise.
+template <typename T>
+static cudaError_t bwd_fixed_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                               cudaStream_t s) {
+    const int v = fixed_variant(g);
+    if (v < 0) return cudaErrorNotSupported;
+    const int HW = g.H * g.W;
+    if ((uintptr_t)gi % 16 != 0 || ((long long)g.vol * sizeof(T)) % 16 != 0) return cudaErrorNotSupported;
+    int td = g.D;
+    while (td > 1 && fixed_smem_bytes(g, td, sizeof(T)) > (size_t)kFixedTileBytes) --td;
+    while (td > 1 && td < g.D && ((long long)td * HW * sizeof(T)) % 16 != 0) --td;
+    if (fixed_smem_bytes(g, td, sizeof(T)) > (size_t)kFixedTileBytes) return cudaErrorNotSupported;
+    if (td < g.D && ((long long)td * HW * sizeof(T)) % 16 != 0) return cudaErrorNotSupported;
+    if ((long long)td * HW >= (1LL << 28)) return cudaErrorNotSupported;
+    if (v == 0) return bwd_fixed_launch<T, 3, 2, 3, 2, 3, 2>(go, idx, gi, g, td, s);
+    return bwd_fixed_launch<T, 2, 1, 2, 1, 2, 1>(go, idx, gi, g, td, s);
+}
+
 template <typename T>
 static cudaError_t bwd_tile_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
                               cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
+    {
+        const cudaError_t ef = bwd_fixed_t<T>(go, idx, gi, g, s);
+        if (ef != cudaErrorNotSupported) return ef;
+    }
     const bool a = g.adaptive != 0;
     const int HW = g.H * g.W;
     TileGeo tg;

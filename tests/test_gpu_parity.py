@@ -292,7 +292,9 @@ def test_no_device_error_flags_after_suite():
 TILE_CASES = [((3, 3, 3), (2, 2, 2), (2, 3, 40, 30, 24)), ((2, 2, 2), (1, 1, 1), (1, 2, 20, 33, 17)),
               ((3, 2, 3), (2, 1, 2), (2, 2, 13, 9, 40)), ((4, 4, 4), (3, 3, 3), (1, 2, 22, 19, 31)),
               # large output planes: several depth tiles per plane, odd H*W
-              ((3, 3, 3), (2, 2, 2), (1, 2, 24, 112, 112)), ((3, 3, 3), (2, 2, 2), (1, 2, 20, 113, 114))]
+              ((3, 3, 3), (2, 2, 2), (1, 2, 24, 112, 112)), ((3, 3, 3), (2, 2, 2), (1, 2, 20, 113, 114)),
+              # compiled fixed-window variants on aligned planes
+              ((2, 2, 2), (1, 1, 1), (1, 2, 12, 20, 16)), ((3, 3, 3), (2, 2, 2), (2, 2, 17, 31, 40))]
 
 
 @pytest.mark.parametrize("dtype", DTYPES, ids=str)
