@@ -283,42 +283,61 @@ __global__ void __launch_bounds__(256)
 k_bwd_disjoint_rows(const T* __restrict__ go, const int64_t* __restrict__ idx,
                     T* __restrict__ gi, Geo g, FastDiv fHW, FastDiv fW, FastDiv fSD, FastDiv fSH) {
     constexpr int NWIN = VEC / SW;
+    constexpr int UNR = 4;                       // chunks per thread, loads issued together
     const int nchunks = g.vol / VEC;
     const T zero = Elem<T>::from_f(0.0f);
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += gridDim.x * blockDim.x) {
-            const int r0 = c * VEC;
-            const int d = fHW.div(r0);
-            const int rr = r0 - d * g.H * g.W;
-            const int h = fW.div(rr);
-            const int w0 = rr - h * g.W;
-            const int od = fSD.div(d), dr = d - od * g.sd;
-            const int oh = fSH.div(h), hr = h - oh * g.sh;
-            Vec16<T> out;
-            if (od < g.OD && dr < g.kd && oh < g.OH && hr < g.kh) {
-                const int ow0 = w0 / SW;
-                const long long rowo = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW;
-                int64_t li[NWIN];
-                T lg[NWIN];
+        for (int cb = blockIdx.x * blockDim.x * UNR + threadIdx.x; cb < nchunks;
+             cb += gridDim.x * blockDim.x * UNR) {
+            int64_t li[UNR][NWIN];
+            T lg[UNR][NWIN];
+            bool cov[UNR];
+            int r0[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int c = cb + u * blockDim.x;
+                r0[u] = c * VEC;
+                cov[u] = false;
 #pragma unroll
                 for (int j = 0; j < NWIN; ++j) {
-                    const bool ok = ow0 + j < g.OW;
-                    li[j] = ok ? __ldg(idx + rowo + ow0 + j) : -1;
-                    lg[j] = ok ? go[rowo + ow0 + j] : zero;
+                    li[u][j] = -1;
+                    lg[u][j] = zero;
                 }
+                if (c >= nchunks) continue;
+                const int d = fHW.div(r0[u]);
+                const int rr = r0[u] - d * g.H * g.W;
+                const int h = fW.div(rr);
+                const int w0 = rr - h * g.W;
+                const int od = fSD.div(d), dr = d - od * g.sd;
+                const int oh = fSH.div(h), hr = h - oh * g.sh;
+                cov[u] = od < g.OD && dr < g.kd && oh < g.OH && hr < g.kh;
+                if (!cov[u]) continue;
+                const int ow0 = w0 / SW;
+                const long long rowo = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW;
+#pragma unroll
+                for (int j = 0; j < NWIN; ++j) {
+                    if (ow0 + j < g.OW) {
+                        li[u][j] = __ldg(idx + rowo + ow0 + j);
+                        lg[u][j] = go[rowo + ow0 + j];
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int c = cb + u * blockDim.x;
+                if (c >= nchunks) continue;
+                Vec16<T> out;
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
-                    const bool hit = (i % SW) < g.kw && li[i / SW] == (int64_t)(r0 + i);
-                    out.e[i] = hit ? lg[i / SW] : zero;
+                    const bool hit = cov[u] && (i % SW) < g.kw && li[u][i / SW] == (int64_t)(r0[u] + i);
+                    out.e[i] = hit ? lg[u][i / SW] : zero;
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) out.e[i] = zero;
+                *reinterpret_cast<uint4*>(gi + p * g.vol + r0[u]) = out.u;
             }
-            *reinterpret_cast<uint4*>(gi + p * g.vol + r0) = out.u;
         }
     }
 }
+
 // ------------------------------------------------------------------ overlap, tiles
 // Overlapping windows, deterministic gather. One CTA owns a tile of TD
 // depth slices of one plane and every input in it:
@@ -601,7 +620,7 @@ static cudaError_t bwd_rows_t(const void* go, const int64_t* idx, void* gi, cons
                               cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     const int nchunks = g.vol / VEC;
-    dim3 grid((unsigned)((nchunks + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
+    dim3 grid((unsigned)((nchunks + 1023) / 1024), (unsigned)(g.P < 65535 ? g.P : 65535));
     k_bwd_disjoint_rows<T, VEC, SW><<<grid, 256, 0, s>>>(
         (const T*)go, idx, (T*)gi, g, FastDiv((uint32_t)(g.H * g.W)), FastDiv((uint32_t)g.W),
         FastDiv((uint32_t)g.sd), FastDiv((uint32_t)g.sh));
