@@ -500,16 +500,16 @@ k_bwd_overlap_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
 // the window's first K - S positions, the next one when it sits in the last
 // K - S positions. One CTA owns a tile of TD depth slices of one plane:
 //  1. stage, for every window that can cover the tile, its gradient and its
-//     winner as a tile-local int32 (-1 when outside the tile), and zero a
-//     dense shared-memory copy of the output tile;
+//     winner as a tile-local int32 (-1 when outside the tile), then zero the
+//     tile in global memory with 16-byte stores (after the staging, so that
+//     the zeroed sectors are still in L2 when the owners' stores arrive);
 //  2. each window decodes its winner relative to its own window (compare
 //     chains), finds the windows that also cover it (itself plus at most
 //     one neighbour per axis, so at most eight) and walks them in ascending
 //     (od, oh, ow) order: if an earlier one chose the same input it stops,
 //     otherwise it is the owner and sums its gradient and those of the later
-//     ones that chose the same input, in binary32, rounds once, and writes
-//     the value into the shared tile;
-//  3. the tile leaves with 16-byte coalesced stores.
+//     ones that chose the same input, in binary32, rounds once, and stores
+//     the value at the winner's place in the tile.
 // The ascending walk visits the eight sign patterns (sd, sh, sw) in {0,1}^3
 // as i ^ neg, where neg has a bit set for each axis whose neighbour is the
 // previous window: that order is ascending window order, and i == neg is
@@ -535,15 +535,8 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
     const T zero = Elem<T>::from_f(0.0f);
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
         const long long obase = p * (long long)g.ovol + (long long)od_lo * ohow;
-        // 1. zero-fill the output tile and stage the windows
+        // 1. stage the windows
         T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
-        if (VEC > 1) {
-            uint4* o4 = reinterpret_cast<uint4*>(out);
-            for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) o4[c] = make_uint4(0, 0, 0, 0);
-            for (int e = (n / VEC) * VEC + threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
-        } else {
-            for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
-        }
         constexpr int UNR = 4;
         for (int wb = 0; wb < nwin; wb += UNR * blockDim.x) {
             int64_t j[UNR];
@@ -562,6 +555,15 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
                 jt[me] = (j[u] >= lo_j && j[u] < hi_j) ? (int)(j[u] - lo_j) : -1;
                 gt[me] = gv[u];
             }
+        }
+        // zero-fill the output tile only now, so that the owners' stores below
+        // find its sectors still in L2
+        if (VEC > 1) {
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+            for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) o4[c] = make_uint4(0, 0, 0, 0);
+            for (int e = (n / VEC) * VEC + threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
+        } else {
+            for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
         }
         __syncthreads();
         // 2. owners: one window row (od, oh) per warp, lanes along ow; every
@@ -608,7 +610,6 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
                 if (valid && !earlier) out[jj] = Elem<T>::from_f(acc);
             }
         }
-        __syncthreads();
         __syncthreads();
     }
 }

@@ -102,6 +102,108 @@ k_fwd_global(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ i
     }
 }
 
+// ------------------------------------------------------------------ slab
+// Any window shape (fixed or adaptive) whose depth slab fits in shared
+// memory. One CTA per (plane, output depth od): the slices [ds, de) of the
+// window depth are one contiguous span of the plane; the CTA copies it into
+// shared memory with 16-byte loads (the span is placed at the same offset
+// modulo 16 bytes, so both sides stay aligned; the ragged ends are copied
+// element by element), then each thread scans whole windows of that depth
+// from shared memory, d then h then w ascending, with the exact rule
+// (strict "beats", NaN beats numbers, first occurrence kept).
+template <typename T, bool ADAPTIVE>
+__global__ void __launch_bounds__(256)
+k_fwd_slab(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int VEC = 16 / sizeof(T);
+    const int od = blockIdx.x;
+    const int HW = g.H * g.W;
+    const int ds = win_start(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int de = win_end(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int n = (de - ds) * HW;
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        const T* src = x + p * g.vol + (long long)ds * HW;
+        const int mis = (int)(((uintptr_t)src % 16) / sizeof(T));   // elements before a 16-byte boundary
+        T* sl = reinterpret_cast<T*>(smem) + mis;                    // sl[i] = src[i]
+        const int head = mis ? min(VEC - mis, n) : 0;
+        const int nvec = (n - head) / VEC;
+        const uint4* gv = reinterpret_cast<const uint4*>(src + head);
+        uint4* sv = reinterpret_cast<uint4*>(sl + head);
+        for (int c = threadIdx.x; c < nvec; c += blockDim.x) sv[c] = __ldg(gv + c);
+        for (int e = threadIdx.x; e < head; e += blockDim.x) sl[e] = src[e];
+        for (int e = head + nvec * VEC + threadIdx.x; e < n; e += blockDim.x) sl[e] = src[e];
+        __syncthreads();
+        const long long obase = ((p * g.OD + od) * (long long)g.OH) * g.OW;
+        for (int t = threadIdx.x; t < g.OH * g.OW; t += blockDim.x) {
+            const int oh = t / g.OW, ow = t - (t / g.OW) * g.OW;
+            const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+            const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+            const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+            const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+            int best = hs * g.W + ws;
+            float m = Elem<T>::to_f(sl[best]);
+            for (int d = 0; d < de - ds; ++d)
+                for (int h = hs; h < he; ++h) {
+                    const int row = d * HW + h * g.W;
+                    for (int w = ws; w < we; ++w) {
+                        const float v = Elem<T>::to_f(sl[row + w]);
+                        if (beats(v, m)) {
+                            m = v;
+                            best = row + w;
+                        }
+                    }
+                }
+            y[obase + t] = sl[best];
+            idx[obase + t] = (int64_t)ds * HW + best;
+        }
+        __syncthreads();
+    }
+}
+
+static constexpr int kSlabBytes = 96 * 1024;
+
+// Deepest window along D (slices the slab must hold).
+static int max_depth(const Geo& g) {
+    if (!g.adaptive) return g.kd;
+    int best = 0;
+    for (int i = 0; i < g.OD; ++i) {
+        const int s = (int)(((long long)i * g.D) / g.OD);
+        const int e = (int)(((long long)(i + 1) * g.D + g.OD - 1) / g.OD);
+        if (e - s > best) best = e - s;
+    }
+    return best;
+}
+
+bool fwd_slab_supported(const Geo& g, int dtype) {
+    const int es = dtype == F32 ? 4 : 2;
+    return (long long)max_depth(g) * g.H * g.W * es + 16 <= kSlabBytes;
+}
+
+template <typename T>
+static cudaError_t fwd_slab_t(const void* x, void* y, int64_t* idx, const Geo& g, cudaStream_t s) {
+    const size_t smem = (size_t)max_depth(g) * g.H * g.W * sizeof(T) + 16;
+    dim3 grid((unsigned)g.OD, (unsigned)(g.P < 65535 ? g.P : 65535));
+    if (g.adaptive) {
+        cudaError_t e = cudaFuncSetAttribute(k_fwd_slab<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_fwd_slab<T, true><<<grid, 256, smem, s>>>((const T*)x, (T*)y, idx, g);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(k_fwd_slab<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_fwd_slab<T, false><<<grid, 256, smem, s>>>((const T*)x, (T*)y, idx, g);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_slab(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int,
+                            cudaStream_t s) {
+    switch (dtype) {
+    case F32: return fwd_slab_t<float>(x, y, idx, g, s);
+    case F16: return fwd_slab_t<__half>(x, y, idx, g, s);
+    default: return fwd_slab_t<__nv_bfloat16>(x, y, idx, g, s);
+    }
+}
+
 // ------------------------------------------------------------------ launch
 
 static int grid_for(long long work, int per_block, int sms, int blocks_per_sm) {

@@ -17,6 +17,10 @@ cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g
                               int dtype, int sms, cudaStream_t s);
 cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g,
                           int dtype, int sms, cudaStream_t s);
+cudaError_t launch_fwd_slab(const void* x, void* y, int64_t* idx, const Geo& g,
+                            int dtype, int sms, cudaStream_t s);
+// Whether a window-depth slab of this geometry fits the slab kernel's shared memory.
+bool fwd_slab_supported(const Geo& g, int dtype);
 // Whether the stride-2 kernel handles this geometry and type (it needs the
 // input on a 16-byte boundary; plan queries assume an aligned buffer).
 bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16);

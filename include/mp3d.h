@@ -82,6 +82,7 @@ typedef enum {
     MP3D_PATH_FWD_GENERIC = 1,       /* one thread per output, any window     */
     MP3D_PATH_FWD_S2 = 2,            /* stride-2 register-column kernel       */
     MP3D_PATH_FWD_GLOBAL = 3,        /* one window per plane (global pool)    */
+    MP3D_PATH_FWD_SLAB = 4,          /* window-depth slab staged in shared memory */
     MP3D_PATH_BWD_DISJOINT = 10,     /* single-pass gather, disjoint windows  */
     MP3D_PATH_BWD_OVERLAP_TILE = 11, /* overlapping gather, staged tile + owner sums */
     MP3D_PATH_BWD_OVERLAP_DIRECT = 12, /* overlapping gather, direct reads    */
