@@ -576,8 +576,8 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
             const int od = od_lo + odr;
             const int rowstart = (od * SD) * HW + (oh * SH) * g.W - (int)lo_j;
             for (int ow = lane; ow - lane < g.OW; ow += 32) {
-                const int me = rr * g.OW + ow;
                 const bool live = ow < g.OW;
+                const int me = live ? rr * g.OW + ow : 0;
                 const int jj = live ? jt[me] : -1;
                 const int rel = jj - (rowstart + ow * SW);
                 int dl = 0;
@@ -589,23 +589,28 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
                 for (int k = 1; k < KH; ++k) hl += (r2 >= k * g.W) ? 1 : 0;
                 const int wl = r2 - hl * g.W;
                 const bool valid = jj >= 0 && rel >= 0 && rel < KD * HW && r2 < KH * g.W && wl < KW;
-                // neighbour per axis: -1 (previous window), +1 (next window) or none
-                const int ed = (dl < KD - SD && od > 0) ? -1 : ((dl >= SD && od + 1 < g.OD) ? 1 : 0);
-                const int eh = (hl < KH - SH && oh > 0) ? -1 : ((hl >= SH && oh + 1 < g.OH) ? 1 : 0);
-                const int ew = (wl < KW - SW && ow > 0) ? -1 : ((wl >= SW && ow + 1 < g.OW) ? 1 : 0);
-                const int neg = (ed < 0 ? 4 : 0) | (eh < 0 ? 2 : 0) | (ew < 0 ? 1 : 0);
-                const int have = (ed != 0 ? 4 : 0) | (eh != 0 ? 2 : 0) | (ew != 0 ? 1 : 0);
-                const int step_d = ed * ohow, step_h = eh * g.OW;
+                // neighbour per axis, as an offset in tile window indices:
+                // -step (previous window), +step (next window) or 0 (none)
+                const int nd = !valid ? 0 : (dl < KD - SD && od > 0) ? -ohow : ((dl >= SD && od + 1 < g.OD) ? ohow : 0);
+                const int nh = !valid ? 0 : (hl < KH - SH && oh > 0) ? -g.OW : ((hl >= SH && oh + 1 < g.OH) ? g.OW : 0);
+                const int nw = !valid ? 0 : (wl < KW - SW && ow > 0) ? -1 : ((wl >= SW && ow + 1 < g.OW) ? 1 : 0);
+                // Combination i takes, per axis, the lower (bit clear) or the
+                // upper (bit set) of {window, neighbour}; over the combinations
+                // that exist, the window index k(i) rises with i, so a
+                // combination precedes this window exactly when k(i) < me.
+                const int dlo = min(nd, 0), dhi = max(nd, 0);
+                const int hlo = min(nh, 0), hhi = max(nh, 0);
+                const int wlo = min(nw, 0), whi = max(nw, 0);
                 bool earlier = false;
                 float acc = valid ? Elem<T>::to_f(gt[me]) : 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int sel = i ^ neg;
-                    const bool use = valid && sel != 0 && (sel & ~have) == 0;
-                    const int k = me + ((sel & 4) ? step_d : 0) + ((sel & 2) ? step_h : 0) + ((sel & 1) ? ew : 0);
-                    const bool hit = use && jt[use ? k : 0] == jj;
-                    earlier |= hit && i < neg;
-                    if (hit && i > neg) acc += Elem<T>::to_f(gt[k]);
+                    const bool use = ((i & 4) == 0 || nd != 0) && ((i & 2) == 0 || nh != 0) &&
+                                     ((i & 1) == 0 || nw != 0);
+                    const int k = me + ((i & 4) ? dhi : dlo) + ((i & 2) ? hhi : hlo) + ((i & 1) ? whi : wlo);
+                    const bool hit = use && jt[k] == jj;
+                    earlier |= hit && k < me;
+                    if (hit && k > me) acc += Elem<T>::to_f(gt[k]);
                 }
                 if (valid && !earlier) out[jj] = Elem<T>::from_f(acc);
             }
