@@ -499,8 +499,9 @@ k_bwd_overlap_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
 // its window and at most one neighbour: the previous one when it sits in
 // the window's first K - S positions, the next one when it sits in the last
 // K - S positions. One CTA owns a tile of TD depth slices of one plane:
-//  1. stage, for every window that can cover the tile, its gradient and its
-//     winner as a tile-local int32 (-1 when outside the tile), then zero the
+//  1. stage, for every window that can cover the tile, one 8-byte word: its
+//     winner as a tile-local int32 (-1 when outside the tile) and its
+//     gradient widened to binary32 (exact), then zero the
 //     tile in global memory with 16-byte stores (after the staging, so that
 //     the zeroed sectors are still in L2 when the owners' stores arrive);
 //  2. each window decodes its winner relative to its own window (compare
@@ -529,8 +530,8 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
     const int od_hi = min((d1 - 1) / SD, g.OD - 1);
     const int ohow = g.OH * g.OW;
     const int nwin = (od_hi >= od_lo) ? (od_hi - od_lo + 1) * ohow : 0;
-    int* jt = reinterpret_cast<int*>(smem);
-    T* gt = reinterpret_cast<T*>(smem + (size_t)rows_max * ohow * sizeof(int));
+    // per staged window: {tile-local winner or -1, gradient as binary32 bits}
+    int2* wt = reinterpret_cast<int2*>(smem);
     const long long lo_j = (long long)d0 * HW, hi_j = (long long)d1 * HW;
     const T zero = Elem<T>::from_f(0.0f);
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
@@ -552,8 +553,8 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
             for (int u = 0; u < UNR; ++u) {
                 const int me = wb + u * blockDim.x + threadIdx.x;
                 if (me >= nwin) continue;
-                jt[me] = (j[u] >= lo_j && j[u] < hi_j) ? (int)(j[u] - lo_j) : -1;
-                gt[me] = gv[u];
+                wt[me] = make_int2((j[u] >= lo_j && j[u] < hi_j) ? (int)(j[u] - lo_j) : -1,
+                                   __float_as_int(Elem<T>::to_f(gv[u])));
             }
         }
         // zero-fill the output tile only now, so that the owners' stores below
@@ -578,7 +579,8 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
             for (int ow = lane; ow - lane < g.OW; ow += 32) {
                 const bool live = ow < g.OW;
                 const int me = live ? rr * g.OW + ow : 0;
-                const int jj = live ? jt[me] : -1;
+                const int2 self = wt[me];
+                const int jj = live ? self.x : -1;
                 const int rel = jj - (rowstart + ow * SW);
                 int dl = 0;
 #pragma unroll
@@ -602,15 +604,16 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
                 const int hlo = min(nh, 0), hhi = max(nh, 0);
                 const int wlo = min(nw, 0), whi = max(nw, 0);
                 bool earlier = false;
-                float acc = valid ? Elem<T>::to_f(gt[me]) : 0.0f;
+                float acc = valid ? __int_as_float(self.y) : 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const bool use = ((i & 4) == 0 || nd != 0) && ((i & 2) == 0 || nh != 0) &&
                                      ((i & 1) == 0 || nw != 0);
                     const int k = me + ((i & 4) ? dhi : dlo) + ((i & 2) ? hhi : hlo) + ((i & 1) ? whi : wlo);
-                    const bool hit = use && jt[k] == jj;
+                    const int2 e = use ? wt[k] : make_int2(-1, 0);
+                    const bool hit = use && e.x == jj;
                     earlier |= hit && k < me;
-                    if (hit && k > me) acc += Elem<T>::to_f(gt[k]);
+                    if (hit && k > me) acc += __int_as_float(e.y);
                 }
                 if (valid && !earlier) out[jj] = Elem<T>::from_f(acc);
             }
@@ -770,10 +773,10 @@ static int fixed_variant(const Geo& g) {
     return -1;
 }
 
-static constexpr int kFixedTileBytes = 72 * 1024;    // shared bytes per tile (three CTAs per SM)
+static constexpr int kFixedTileBytes = 100 * 1024;   // shared bytes per tile (two CTAs per SM)
 
-static size_t fixed_smem_bytes(const Geo& g, int td, int es) {
-    return (size_t)max_window_rows(g, td) * g.OH * g.OW * (sizeof(int) + es);
+static size_t fixed_smem_bytes(const Geo& g, int td, int) {
+    return (size_t)max_window_rows(g, td) * g.OH * g.OW * sizeof(int2);
 }
 
 template <typename T, int KD, int SD, int KH, int SH, int KW, int SW>
