@@ -493,52 +493,157 @@ k_bwd_overlap_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T*
     }
 }
 
-// ------------------------------------------------------------------ overlap, fixed windows
-// Overlapping fixed windows with kernel <= 2 * stride on every axis, window
-// shape known at compile time. Along each axis an input is then covered by
-// its window and at most one neighbour: the previous one when it sits in
-// the window's first K - S positions, the next one when it sits in the last
-// K - S positions. One CTA owns a tile of TD depth slices of one plane:
+// ------------------------------------------------------------------ overlap, chunk gather
+// Overlapping fixed windows with kernel <= 2 * stride on every axis (so at
+// most two windows cover an input along each axis), window shape known at
+// compile time. One CTA owns a tile of TD depth slices of one plane:
 //  1. stage, for every window that can cover the tile, one 8-byte word: its
-//     winner as a tile-local int32 (-1 when outside the tile) and its
-//     gradient widened to binary32 (exact), then zero the
-//     tile in global memory with 16-byte stores (after the staging, so that
-//     the zeroed sectors are still in L2 when the owners' stores arrive);
-//  2. each window decodes its winner relative to its own window (compare
-//     chains), finds the windows that also cover it (itself plus at most
-//     one neighbour per axis, so at most eight) and walks them in ascending
-//     (od, oh, ow) order: if an earlier one chose the same input it stops,
-//     otherwise it is the owner and sums its gradient and those of the later
-//     ones that chose the same input, in binary32, rounds once, and stores
-//     the value at the winner's place in the tile.
-// The ascending walk visits the eight sign patterns (sd, sh, sw) in {0,1}^3
-// as i ^ neg, where neg has a bit set for each axis whose neighbour is the
-// previous window: that order is ascending window order, and i == neg is
-// the window itself.
+//     winner as a tile-local index held in a float (exact below 2^24; a
+//     large negative value when outside the tile) and its gradient widened
+//     to binary32 (exact);
+//  2. each thread computes VEC consecutive inputs of one row (d, h), a
+//     chunk starting on a window boundary along w: it walks the at most
+//     2 x 2 window rows (od, oh) that cover the row, in ascending order, and
+//     in each the windows ow that overlap the chunk, in ascending order; a
+//     window can only have chosen one of the at most KW inputs it covers, so
+//     its winner is compared against those fixed chunk positions and, on a
+//     match, its gradient is added to that input's binary32 sum. Every
+//     input therefore sums the windows that chose it in ascending (od, oh,
+//     ow) order and is rounded once;
+//  3. the chunk leaves as one coalesced 16-byte store (element stores when
+//     rows are not 16-byte multiples); inputs no window chose get +0.
+// Two forms of step 2, chosen per tile:
+//  - when every staged gradient is finite and none is -0, a match is taken
+//    arithmetically: with x = winner - position (an integer held exactly),
+//    h = sat(1 - x*x) is 1 for x == 0 and 0 otherwise, and acc = fma(g, h,
+//    acc) equals acc + g or acc exactly (a sum that starts from +0 and has
+//    no -0 term is never -0, so adding a signed zero leaves it unchanged);
+//    this keeps the selection on the floating-point pipe;
+//  - otherwise sums start from -0, matches are taken by comparison and
+//    per-input "touched" bits turn inputs no window chose into +0.
+// Staged window rows are interleaved: window ow of a row sits at
+// ((ow + R) % R) * Q + (ow + R) / R with R = VEC / SW and Q = chunks + 1, so
+// the lanes of a warp, whose chunks start R windows apart, read consecutive
+// words; the places of the missing windows ow = -1 and ow >= OW hold a
+// sentinel that matches nothing. Rows of a tile are visited with all even h
+// before all odd h when the stride along h is 2, so the lanes of a warp
+// mostly have the same number of covering window rows.
+static constexpr float kNoWinner = -16777216.0f;   // never within 2^24 of a chunk
+
+// 1 when the integer x (held exactly in a float) is 0, else 0: the
+// saturated 1 - x*x, as one fused multiply-add with saturation.
+__device__ __forceinline__ float hit_weight(float x) {
+    float h;
+    asm("fma.rn.sat.f32 %0, %1, %2, 0f3F800000;" : "=f"(h) : "f"(-x), "f"(x));
+    return h;
+}
+
+// Sums, rounds and stores one chunk of VEC inputs (see the kernel below).
+// row0 points at the first covering window row; off[i] is the place of the
+// chunk's window ow = c * R + DMIN + i within a staged window row.
+template <typename T, int VEC, int KW, int SW, bool EXACT>
+__device__ __forceinline__ void gather_chunk(const float2* __restrict__ row0, const int (&off)[(VEC - 1) / SW + (KW - 1) / SW + 1],
+                                             int nod, int noh, int rowsp, int RQ, float basef,
+                                             T* __restrict__ dst, bool vstore, int nt) {
+    constexpr int DMIN = -((KW - 1) / SW), DMAX = (VEC - 1) / SW;
+    float acc[VEC];
+    unsigned touched = 0;
+#pragma unroll
+    for (int t = 0; t < VEC; ++t) acc[t] = EXACT ? -0.0f : 0.0f;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        if (a >= nod) break;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            if (b >= noh) break;
+            const float2* row = row0 + (a * rowsp + b * RQ);
+#pragma unroll
+            for (int dl = DMIN; dl <= DMAX; ++dl) {
+                const float2 e = row[off[dl - DMIN]];
+                const float u = e.x - basef;     // winner relative to the chunk start
+#pragma unroll
+                for (int q = 0; q < KW; ++q) {
+                    const int t = SW * dl + q;
+                    if (t < 0 || t >= VEC) continue;
+                    if (EXACT) {
+                        if (u == (float)t) {
+                            acc[t] += e.y;
+                            touched |= 1u << t;
+                        }
+                    } else {
+                        acc[t] = fmaf(e.y, hit_weight(u - (float)t), acc[t]);
+                    }
+                }
+            }
+        }
+    }
+    Vec16<T> v;
+#pragma unroll
+    for (int t = 0; t < VEC; ++t)
+        v.e[t] = Elem<T>::from_f((EXACT && !((touched >> t) & 1u)) ? 0.0f : acc[t]);
+    if (vstore) {
+        *reinterpret_cast<uint4*>(dst) = v.u;
+    } else {
+        for (int t = 0; t < nt; ++t) dst[t] = v.e[t];
+    }
+}
+
 template <typename T, int VEC, int KD, int SD, int KH, int SH, int KW, int SW>
 __global__ void __launch_bounds__(512)
-k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
-                    T* __restrict__ gi, Geo g, int TD, int rows_max, FastDiv fOH, FastDiv fOW) {
-    static_assert(KD <= 2 * SD && KH <= 2 * SH && KW <= 2 * SW && KD <= 4 && KH <= 4 && KW <= 4,
-                  "at most two covering windows per axis");
+k_bwd_overlap_gather(const T* __restrict__ go, const int64_t* __restrict__ idx,
+                     T* __restrict__ gi, Geo g, int TD, int rows_max, int nchunk, bool vstore,
+                     FastDiv fOW) {
+    static_assert(KD <= 2 * SD && KH <= 2 * SH && KW <= 2 * SW, "at most two covering windows per axis");
+    static_assert(VEC % SW == 0, "chunks start on a window boundary along w");
+    static_assert(SH == 1 || SH == 2, "row order handles strides 1 and 2 along h");
+    static_assert((KW - 1) / SW <= VEC / SW, "one sentinel column before the first chunk suffices");
+    constexpr int R = VEC / SW;
+    constexpr int DMIN = -((KW - 1) / SW), DMAX = (VEC - 1) / SW, NDL = DMAX - DMIN + 1;
     extern __shared__ __align__(16) unsigned char smem[];
     const int HW = g.H * g.W;
     const int d0 = blockIdx.x * TD;
     const int d1 = min(d0 + TD, g.D);
-    const int n = (d1 - d0) * HW;
     const int od_lo = d0 < KD ? 0 : (d0 - KD) / SD + 1;
     const int od_hi = min((d1 - 1) / SD, g.OD - 1);
     const int ohow = g.OH * g.OW;
     const int nwin = (od_hi >= od_lo) ? (od_hi - od_lo + 1) * ohow : 0;
-    // per staged window: {tile-local winner or -1, gradient as binary32 bits}
-    int2* wt = reinterpret_cast<int2*>(smem);
     const long long lo_j = (long long)d0 * HW, hi_j = (long long)d1 * HW;
-    const T zero = Elem<T>::from_f(0.0f);
+    const int Q = nchunk + 1, RQ = R * Q, rowsp = g.OH * RQ;
+    float2* wt = reinterpret_cast<float2*>(smem);
+    int2* rinfo = reinterpret_cast<int2*>(smem + (size_t)rows_max * rowsp * sizeof(float2));
+    const int nrows_t = (d1 - d0) * g.H;
+    const int h_even = (g.H + 1) / 2;
+    // sentinels everywhere once (the staging below overwrites the places of
+    // real windows only) and, per input row of the tile, {row offset in the
+    // tile, first covering window row | #covering along d << 28 | along h << 30}
+    for (int e = threadIdx.x; e < rows_max * rowsp; e += blockDim.x) wt[e] = make_float2(kNoWinner, 0.0f);
+    for (int ri = threadIdx.x; ri < nrows_t; ri += blockDim.x) {
+        const int dr = ri / g.H, r = ri - dr * g.H;
+        const int h = (SH == 2) ? (r < h_even ? 2 * r : 2 * (r - h_even) + 1) : r;
+        const int d = d0 + dr;
+        const int odl = d < KD ? 0 : (d - KD) / SD + 1, odh = min(d / SD, g.OD - 1);
+        const int ohl = h < KH ? 0 : (h - KH) / SH + 1, ohh = min(h / SH, g.OH - 1);
+        const int nod = max(0, odh - odl + 1), noh = max(0, ohh - ohl + 1);
+        const int wrow = (nod > 0 && noh > 0) ? (odl - od_lo) * rowsp + ohl * RQ : 0;
+        rinfo[ri] = make_int2(dr * HW + h * g.W,
+                              (int)((unsigned)wrow | ((unsigned)nod << 28) | ((unsigned)noh << 30)));
+    }
+    // this thread's chunk column and the places of its windows in a row
+    const int rstep = blockDim.x / nchunk;
+    const int c = threadIdx.x % nchunk, r0 = threadIdx.x / nchunk;
+    int off[NDL];
+#pragma unroll
+    for (int dl = DMIN; dl <= DMAX; ++dl) {
+        const int slot = ((dl % R) + R) % R, cadd = (dl - slot) / R;
+        off[dl - DMIN] = slot * Q + c + 1 + cadd;
+    }
+    const int nt = min(VEC, g.W - c * VEC);
+    __syncthreads();
     for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
         const long long obase = p * (long long)g.ovol + (long long)od_lo * ohow;
         // 1. stage the windows
-        T* out = gi + p * (long long)g.vol + (long long)d0 * HW;
         constexpr int UNR = 4;
+        bool special = false;
         for (int wb = 0; wb < nwin; wb += UNR * blockDim.x) {
             int64_t j[UNR];
             T gv[UNR];
@@ -547,75 +652,37 @@ k_bwd_overlap_fixed(const T* __restrict__ go, const int64_t* __restrict__ idx,
                 const int me = wb + u * blockDim.x + threadIdx.x;
                 const bool ok = me < nwin;
                 j[u] = ok ? __ldg(idx + obase + me) : -1;
-                gv[u] = ok ? go[obase + me] : zero;
+                gv[u] = ok ? go[obase + me] : Elem<T>::from_f(0.0f);
             }
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
                 const int me = wb + u * blockDim.x + threadIdx.x;
                 if (me >= nwin) continue;
-                wt[me] = make_int2((j[u] >= lo_j && j[u] < hi_j) ? (int)(j[u] - lo_j) : -1,
-                                   __float_as_int(Elem<T>::to_f(gv[u])));
+                const float gf = Elem<T>::to_f(gv[u]);
+                const unsigned gb = __float_as_uint(gf);
+                special |= gb == 0x80000000u || (gb & 0x7f800000u) == 0x7f800000u;
+                const int row = fOW.div(me);
+                const int ow = me - row * g.OW + R;
+                const bool in = j[u] >= lo_j && j[u] < hi_j;
+                wt[row * RQ + (ow % R) * Q + ow / R] =
+                    make_float2(in ? (float)(int)(j[u] - lo_j) : kNoWinner, gf);
             }
         }
-        // zero-fill the output tile only now, so that the owners' stores below
-        // find its sectors still in L2
-        if (VEC > 1) {
-            uint4* o4 = reinterpret_cast<uint4*>(out);
-            for (int c = threadIdx.x; c < n / VEC; c += blockDim.x) o4[c] = make_uint4(0, 0, 0, 0);
-            for (int e = (n / VEC) * VEC + threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
-        } else {
-            for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = zero;
-        }
-        __syncthreads();
-        // 2. owners: one window row (od, oh) per warp, lanes along ow; every
-        // lane runs the same predicated sequence (no early exits).
-        const int nrows = nwin / g.OW;
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-        for (int rr = warp; rr < nrows; rr += nwarps) {
-            const int odr = fOH.div(rr);
-            const int oh = rr - odr * g.OH;
-            const int od = od_lo + odr;
-            const int rowstart = (od * SD) * HW + (oh * SH) * g.W - (int)lo_j;
-            for (int ow = lane; ow - lane < g.OW; ow += 32) {
-                const bool live = ow < g.OW;
-                const int me = live ? rr * g.OW + ow : 0;
-                const int2 self = wt[me];
-                const int jj = live ? self.x : -1;
-                const int rel = jj - (rowstart + ow * SW);
-                int dl = 0;
-#pragma unroll
-                for (int k = 1; k < KD; ++k) dl += (rel >= k * HW) ? 1 : 0;
-                const int r2 = rel - dl * HW;
-                int hl = 0;
-#pragma unroll
-                for (int k = 1; k < KH; ++k) hl += (r2 >= k * g.W) ? 1 : 0;
-                const int wl = r2 - hl * g.W;
-                const bool valid = jj >= 0 && rel >= 0 && rel < KD * HW && r2 < KH * g.W && wl < KW;
-                // neighbour per axis, as an offset in tile window indices:
-                // -step (previous window), +step (next window) or 0 (none)
-                const int nd = !valid ? 0 : (dl < KD - SD && od > 0) ? -ohow : ((dl >= SD && od + 1 < g.OD) ? ohow : 0);
-                const int nh = !valid ? 0 : (hl < KH - SH && oh > 0) ? -g.OW : ((hl >= SH && oh + 1 < g.OH) ? g.OW : 0);
-                const int nw = !valid ? 0 : (wl < KW - SW && ow > 0) ? -1 : ((wl >= SW && ow + 1 < g.OW) ? 1 : 0);
-                // Combination i takes, per axis, the lower (bit clear) or the
-                // upper (bit set) of {window, neighbour}; over the combinations
-                // that exist, the window index k(i) rises with i, so a
-                // combination precedes this window exactly when k(i) < me.
-                const int dlo = min(nd, 0), dhi = max(nd, 0);
-                const int hlo = min(nh, 0), hhi = max(nh, 0);
-                const int wlo = min(nw, 0), whi = max(nw, 0);
-                bool earlier = false;
-                float acc = valid ? __int_as_float(self.y) : 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const bool use = ((i & 4) == 0 || nd != 0) && ((i & 2) == 0 || nh != 0) &&
-                                     ((i & 1) == 0 || nw != 0);
-                    const int k = me + ((i & 4) ? dhi : dlo) + ((i & 2) ? hhi : hlo) + ((i & 1) ? whi : wlo);
-                    const int2 e = use ? wt[k] : make_int2(-1, 0);
-                    const bool hit = use && e.x == jj;
-                    earlier |= hit && k < me;
-                    if (hit && k > me) acc += __int_as_float(e.y);
-                }
-                if (valid && !earlier) out[jj] = Elem<T>::from_f(acc);
+        const bool exact = __syncthreads_or(special) != 0;
+        // 2. this thread's chunk in rows r0, r0 + rstep, ...
+        T* out = gi + p * (long long)g.vol + lo_j + c * VEC;
+        if (r0 < rstep) {
+            for (int ri = r0; ri < nrows_t; ri += rstep) {
+                const int2 info = rinfo[ri];
+                const int base = info.x + c * VEC;
+                const float2* row0 = wt + (info.y & 0x0FFFFFFF);
+                const int nod = (info.y >> 28) & 3, noh = (int)((unsigned)info.y >> 30);
+                if (!exact)
+                    gather_chunk<T, VEC, KW, SW, false>(row0, off, nod, noh, rowsp, RQ, (float)base,
+                                                        out + info.x, vstore, nt);
+                else
+                    gather_chunk<T, VEC, KW, SW, true>(row0, off, nod, noh, rowsp, RQ, (float)base,
+                                                       out + info.x, vstore, nt);
             }
         }
         __syncthreads();
@@ -773,10 +840,19 @@ static int fixed_variant(const Geo& g) {
     return -1;
 }
 
-static constexpr int kFixedTileBytes = 100 * 1024;   // shared bytes per tile (two CTAs per SM)
+static constexpr int kFixedTileBytes = 113 * 1024;   // shared bytes per tile (two CTAs per SM)
 
-static size_t fixed_smem_bytes(const Geo& g, int td, int) {
-    return (size_t)max_window_rows(g, td) * g.OH * g.OW * sizeof(int2);
+// Staged window rows: R = (16 / element size) / stride_w slots of
+// (chunks per row + 1) columns each.
+static int fixed_row_words(const Geo& g, int es) {
+    const int vec = 16 / es;
+    return (vec / g.sw) * ((g.W + vec - 1) / vec + 1);
+}
+
+// Staged window rows plus one int2 per input row of the tile.
+static size_t fixed_smem_bytes(const Geo& g, int td, int es) {
+    return (size_t)max_window_rows(g, td) * g.OH * fixed_row_words(g, es) * sizeof(float2) +
+           (size_t)td * g.H * sizeof(int2);
 }
 
 template <typename T, int KD, int SD, int KH, int SH, int KW, int SW>
@@ -784,30 +860,30 @@ static cudaError_t bwd_fixed_launch(const void* go, const int64_t* idx, void* gi
                                     int td, cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     const size_t smem = fixed_smem_bytes(g, td, sizeof(T));
-    auto kern = k_bwd_overlap_fixed<T, VEC, KD, SD, KH, SH, KW, SW>;
+    auto kern = k_bwd_overlap_gather<T, VEC, KD, SD, KH, SH, KW, SW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    const int nchunk = (g.W + VEC - 1) / VEC;
+    const bool vstore = g.W % VEC == 0 && (uintptr_t)gi % 16 == 0;
     dim3 grid((unsigned)((g.D + td - 1) / td), (unsigned)(g.P < 65535 ? g.P : 65535));
-    kern<<<grid, 512, smem, s>>>((const T*)go, idx, (T*)gi, g, td, max_window_rows(g, td),
-                                 FastDiv((uint32_t)g.OH), FastDiv((uint32_t)g.OW));
+    kern<<<grid, 512, smem, s>>>((const T*)go, idx, (T*)gi, g, td, max_window_rows(g, td), nchunk,
+                                 vstore, FastDiv((uint32_t)g.OW));
     return cudaGetLastError();
 }
 
-// The fixed-window kernel when the shape has a variant, the tile fits and
-// tiles start on 16-byte boundaries; cudaErrorNotSupported otherwise.
+// The fixed-window kernel when the shape has a variant and the tile fits;
+// cudaErrorNotSupported otherwise.
 template <typename T>
 static cudaError_t bwd_fixed_t(const void* go, const int64_t* idx, void* gi, const Geo& g,
                                cudaStream_t s) {
     const int v = fixed_variant(g);
     if (v < 0) return cudaErrorNotSupported;
     const int HW = g.H * g.W;
-    if ((uintptr_t)gi % 16 != 0 || ((long long)g.vol * sizeof(T)) % 16 != 0) return cudaErrorNotSupported;
     int td = g.D;
     while (td > 1 && fixed_smem_bytes(g, td, sizeof(T)) > (size_t)kFixedTileBytes) --td;
-    while (td > 1 && td < g.D && ((long long)td * HW * sizeof(T)) % 16 != 0) --td;
     if (fixed_smem_bytes(g, td, sizeof(T)) > (size_t)kFixedTileBytes) return cudaErrorNotSupported;
-    if (td < g.D && ((long long)td * HW * sizeof(T)) % 16 != 0) return cudaErrorNotSupported;
-    if ((long long)td * HW >= (1LL << 28)) return cudaErrorNotSupported;
+    if ((long long)td * HW >= (1LL << 24)) return cudaErrorNotSupported;   // exact in a float
+    if ((g.W + 16 / (int)sizeof(T) - 1) / (16 / (int)sizeof(T)) > 512) return cudaErrorNotSupported;
     if (v == 0) return bwd_fixed_launch<T, 3, 2, 3, 2, 3, 2>(go, idx, gi, g, td, s);
     return bwd_fixed_launch<T, 2, 1, 2, 1, 2, 1>(go, idx, gi, g, td, s);
 }

@@ -309,3 +309,41 @@ def test_overlap_tile_backward(case, dtype):
     g = torch.randn(i_ref.shape, generator=gen).to(dtype)
     assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
                       "grad_in")
+
+
+# Gradients holding -0 and +0 on inputs claimed by several windows: a sum
+# whose terms are all -0 is -0, any other all-zero sum is +0, and inputs no
+# window chose are +0. Also infinite and NaN gradients.
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("window", [((3, 3, 3), (2, 2, 2)), ((2, 2, 2), (1, 1, 1))], ids=["k3s2", "k2s1"])
+@pytest.mark.parametrize("grad", ["mixed_zeros", "all_negative_zero", "non_finite"])
+def test_overlap_backward_signed_zero_gradients(window, dtype, grad):
+    k, s = window
+    shape = (2, 2, 11, 14, 24)
+    out = mp.pool_out_size(shape[2:], k, s)
+    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_tile"
+    gen = torch.Generator().manual_seed(8100)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    if grad == "all_negative_zero":
+        g = torch.full(i_ref.shape, -0.0).to(dtype)
+    elif grad == "non_finite":
+        # +-inf and NaN gradients (plus one -0): sums through them follow
+        # IEEE rules in the same order as the oracle
+        r = torch.rand(i_ref.shape, generator=gen)
+        g = torch.randint(-2, 3, i_ref.shape, generator=gen).float()
+        g = torch.where(r < 0.02, torch.tensor(float("inf")), g)
+        g = torch.where((r >= 0.02) & (r < 0.04), torch.tensor(float("-inf")), g)
+        g = torch.where((r >= 0.04) & (r < 0.05), torch.tensor(float("nan")), g)
+        g.view(-1)[0] = -0.0
+        g = g.to(dtype)
+    else:
+        r = torch.rand(i_ref.shape, generator=gen)
+        g = torch.where(r < 0.4, torch.tensor(-0.0), torch.where(r < 0.7, torch.tensor(0.0),
+                                                                 torch.randint(-2, 3, i_ref.shape,
+                                                                               generator=gen).float()))
+        g = g.to(dtype)
+    ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    if grad != "non_finite":
+        assert bool((bits(ref) == bits(torch.tensor(-0.0).to(dtype))).any())
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), ref, "grad_in")
