@@ -23,7 +23,7 @@ BWD_AUTO, BWD_GATHER, BWD_ATOMIC = 0, 1, 2
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 10: "bwd_disjoint",
-         11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic"}
+         11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll"}
 
 _lib = None
 

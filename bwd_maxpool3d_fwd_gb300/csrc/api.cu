@@ -45,6 +45,7 @@ const char* path_name(int path) {
     case MP3D_PATH_BWD_OVERLAP_TILE: return "bwd_overlap_tile";
     case MP3D_PATH_BWD_OVERLAP_DIRECT: return "bwd_overlap_direct";
     case MP3D_PATH_BWD_ATOMIC: return "bwd_atomic";
+    case MP3D_PATH_BWD_OVERLAP_ROLL: return "bwd_overlap_roll";
     default: return "?";
     }
 }
@@ -156,10 +157,11 @@ int fwd_path(const Geo& g, int dtype, bool aligned16 = true) {
     return MP3D_PATH_FWD_GENERIC;
 }
 
-int bwd_path(const Geo& g, int algo) {
+int bwd_path(const Geo& g, int dtype, int algo, bool aligned16 = true) {
     if (g.P == 0) return MP3D_PATH_NOOP;
     if (algo == MP3D_BWD_ATOMIC) return MP3D_PATH_BWD_ATOMIC;
     if (is_disjoint(g)) return MP3D_PATH_BWD_DISJOINT;
+    if (bwd_roll_supported(g, dtype, aligned16)) return MP3D_PATH_BWD_OVERLAP_ROLL;
     if (bwd_tile_supported(g)) return MP3D_PATH_BWD_OVERLAP_TILE;
     return MP3D_PATH_BWD_OVERLAP_DIRECT;
 }
@@ -246,7 +248,7 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, in
                        int algo, int* path) {
     Geo g;
     int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, algo);
-    if (!st && path) *path = bwd_path(g, algo);
+    if (!st && path) *path = bwd_path(g, dtype, algo);
     return st;
 }
 
@@ -305,7 +307,7 @@ int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64
                 return MP3D_ERR_ALIAS;
         }
     }
-    const int path = bwd_path(g, algo);
+    const int path = bwd_path(g, dtype, algo, (uintptr_t)grad_in % 16 == 0);
     const Geo gk = (path == MP3D_PATH_BWD_DISJOINT) ? as_fixed(g) : g;
     log_path("bwd", path, gk, dtype);
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
@@ -318,6 +320,9 @@ int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64
         break;
     case MP3D_PATH_BWD_DISJOINT:
         e = launch_bwd_disjoint(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_OVERLAP_ROLL:
+        e = launch_bwd_roll(grad_out, idx, grad_in, gk, dtype, sms, stream);
         break;
     case MP3D_PATH_BWD_OVERLAP_TILE:
         e = launch_bwd_overlap_tile(grad_out, idx, grad_in, gk, dtype, sms, stream);

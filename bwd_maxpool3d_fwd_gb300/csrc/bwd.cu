@@ -354,34 +354,6 @@ k_bwd_disjoint_rows(const T* __restrict__ go, const int64_t* __restrict__ idx,
 //     follow (found by slot offsets), in binary32, rounds once and stores.
 // Per input the work is a share of one vector store; per window, a few
 // integer operations, one shared atomic and, for owners, the sum.
-struct AxisMap {
-    int I, O, K, S;
-    int adaptive;
-    FastDiv fS;   // fixed: divide by S
-    FastDiv fI;   // adaptive: divide by I
-    FastDiv fO;   // adaptive: divide by O
-    // Window o along this axis: [start(o), end(o)).
-    __device__ __forceinline__ int start(int o) const { return adaptive ? fO.div(o * I) : o * S; }
-    __device__ __forceinline__ int len(int o) const {
-        return adaptive ? fO.div((o + 1) * I + O - 1) - fO.div(o * I) : K;
-    }
-    __device__ __forceinline__ int lo(int x) const {
-        if (adaptive) return fI.div(x * O);
-        return x < K ? 0 : fS.div(x - K) + 1;
-    }
-    __device__ __forceinline__ int hi(int x) const {
-        if (adaptive) return fI.div((x + 1) * O - 1);
-        const int h = fS.div(x);
-        return h < O - 1 ? h : O - 1;
-    }
-    // Windows before o that also cover position start(o) + rel.
-    __device__ __forceinline__ int earlier(int o, int rel) const {
-        if (adaptive) return o - lo(start(o) + rel);
-        const int e = fS.div(K - 1 - rel);
-        return e < o ? e : o;
-    }
-};
-
 struct TileGeo {
     int TD, ntiles;
     int rows;             // window rows (od values) staged per tile, at most
@@ -770,14 +742,6 @@ static int log2_exact(int p) {
     return l;
 }
 
-static AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
-    AxisMap a;
-    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
-    a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
-    a.fI = FastDiv((uint32_t)I);
-    a.fO = FastDiv((uint32_t)O);
-    return a;
-}
 
 // Window rows (od values) that can cover one tile of td slices, at most.
 static int max_window_rows(const Geo& g, int td) {

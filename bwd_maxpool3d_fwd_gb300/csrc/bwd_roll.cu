@@ -1,0 +1,493 @@
+// Overlapping backward as an ordered scatter into a rolling ring of depth
+// slices held in shared memory (FlagGems-Experimental PR #308, "Add
+// adaptive_max_pool3d_backward Moore Threads specialized operator",
+// Summary: when the axes do not divide evenly, windows overlap and the
+// gradients of the windows that chose one input are summed).
+//
+// grad_in[p, j] is the binary32 sum of the gradients of the windows whose
+// stored index is j, taken in ascending (od, oh, ow) order and starting from
+// the first term, rounded once to the type; +0 where no window chose j.
+//
+// Scope: at most two windows cover any position along each axis (fixed
+// windows with kernel <= 2 * stride; adaptive windows with
+// end(i) <= start(i + 2)). One CTA owns the inputs of one plane in the rows
+// [h0, h1) (an h-tile) and walks the window rows od = 0 .. OD-1 in order.
+// For each row:
+//  1. Every thread decodes its windows of the row (the (oh, ow) whose rows
+//     meet [h0, h1)). The stored index must name an input inside the window
+//     and inside the h-tile, else the window adds nothing here (as in every
+//     gather path). The input's binary32 accumulator lives in a ring of RS
+//     depth slices in shared memory, slot jd mod RS, RS being the longest
+//     window along d; the slices one row reaches never share a slot.
+//  2. Four passes, separated by barriers, add the gradients. Pass (rh, rw)
+//     takes the windows whose input is also covered by the next window
+//     along h (rh = 0) or not (rh = 1), and likewise along w. Two windows
+//     of one row that choose the same input differ in oh or ow; on such an
+//     axis the lower window has role 0 and the upper role 1, so they fall in
+//     different passes with the lower first, and no pass has two windows on
+//     one accumulator (plain shared loads and stores, no atomics). Earlier
+//     rows were added in earlier iterations, so every input receives its
+//     terms in ascending (od, oh, ow) order.
+//  3. The slices no later row reaches, [start(od), start(od + 1)) (up to D
+//     after the last row), are rounded and written with coalesced 16-byte
+//     stores, and their accumulators are reset.
+// Accumulators start at +0. Adding the first term t to +0 gives t, except
+// that +0 + (-0) is +0, so the sum differs from the first-term sum only when
+// every term is -0 (the first-term sum is then -0); and an accumulator never
+// holds -0. Windows with a -0 gradient therefore set a bit for their input;
+// before the store, an input whose accumulator is +0 and whose bit is set
+// re-reads its covering windows in global memory, and its accumulator is set
+// to -0 when every window that chose it has a -0 gradient. Inputs no window
+// chose leave as +0.
+#include <climits>
+
+#include "internal.h"
+
+namespace mp3d {
+
+struct RollGeo {
+    int TH, nht;        // input rows per h-tile, h-tiles per plane
+    int RS;             // ring slots (depth slices)
+    int SSTR;           // floats per slot: a multiple of 32 holding TH*W + alignment
+    AxisMap ad, ah, aw;
+    FastDiv fHW, fW, fOW;
+};
+
+// Window arithmetic along one axis with the window kind known at compile
+// time (fixed: [o*S, o*S + K); adaptive: [floor(o*I/O), ceil((o+1)*I/O))).
+template <bool AD>
+__device__ __forceinline__ int ax_start(const AxisMap& a, int o) {
+    if constexpr (AD) return a.fO.div(o * a.I);
+    else return o * a.S;
+}
+template <bool AD>
+__device__ __forceinline__ int ax_end(const AxisMap& a, int o) {
+    if constexpr (AD) return a.fO.div((o + 1) * a.I + a.O - 1);
+    else return o * a.S + a.K;
+}
+template <bool AD>
+__device__ __forceinline__ int ax_lo(const AxisMap& a, int x) {
+    if constexpr (AD) return a.fI.div(x * a.O);
+    else return x < a.K ? 0 : a.fS.div(x - a.K) + 1;
+}
+template <bool AD>
+__device__ __forceinline__ int ax_hi(const AxisMap& a, int x) {
+    if constexpr (AD) return a.fI.div((x + 1) * a.O - 1);
+    else return min(a.fS.div(x), a.O - 1);
+}
+
+// Whether every window that chose input j of plane p has a -0 gradient
+// (the input is known to be chosen by at least one). Windows are visited
+// through their stored indices in global memory.
+template <typename T, bool AD>
+__device__ __forceinline__ bool roll_all_negzero(const T* __restrict__ go,
+                                                 const int64_t* __restrict__ idx, long long p, int j,
+                                                 const Geo& g, const RollGeo& rg) {
+    const int HW = g.H * g.W;
+    const int jd = rg.fHW.div(j);
+    const int rem = j - jd * HW;
+    const int jh = rg.fW.div(rem);
+    const int jw = rem - jh * g.W;
+    const long long ob = p * (long long)g.ovol;
+    for (int od = ax_lo<AD>(rg.ad, jd); od <= ax_hi<AD>(rg.ad, jd); ++od)
+        for (int oh = ax_lo<AD>(rg.ah, jh); oh <= ax_hi<AD>(rg.ah, jh); ++oh)
+            for (int ow = ax_lo<AD>(rg.aw, jw); ow <= ax_hi<AD>(rg.aw, jw); ++ow) {
+                const long long o = ob + ((long long)od * g.OH + oh) * g.OW + ow;
+                if (idx[o] == j && __float_as_uint(Elem<T>::to_f(go[o])) != 0x80000000u) return false;
+            }
+    return true;
+}
+
+// Two binary32 values rounded to T and packed into 32 bits (low = first).
+template <typename T> __device__ __forceinline__ unsigned pack2(float a, float b);
+template <> __device__ __forceinline__ unsigned pack2<__half>(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const unsigned*>(&h);
+}
+template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const unsigned*>(&h);
+}
+
+// One 16-byte output chunk from the accumulators at src (reset to +0).
+template <typename T>
+__device__ __forceinline__ uint4 roll_take(float* src) {
+    float4* s4 = reinterpret_cast<float4*>(src);
+    uint4 out;
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = s4[0];
+        s4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        out = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z),
+                         __float_as_uint(a.w));
+    } else {
+        const float4 a = s4[0], b = s4[1];
+        s4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        s4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        out = make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y),
+                         pack2<T>(b.z, b.w));
+    }
+    return out;
+}
+
+template <typename T, bool AD, int NT, int WPT, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
+           RollGeo rg) {
+    constexpr int VEC = 16 / sizeof(T);
+    extern __shared__ __align__(16) float ring[];
+    const int RS = rg.RS, SSTR = rg.SSTR;
+    const int nacc = RS * SSTR;
+    unsigned* negbits = reinterpret_cast<unsigned*>(ring + nacc);   // one bit per accumulator
+    int* slotmask = reinterpret_cast<int*>(negbits + nacc / 32);    // slots holding a set bit
+    const int tid = threadIdx.x;
+    const int W = g.W, HW = g.H * g.W, OW = g.OW, OD = g.OD;
+    {
+        float4* r4 = reinterpret_cast<float4*>(ring);
+        for (int i = tid; i < nacc / 4; i += NT) r4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = tid; i < nacc / 32; i += NT) negbits[i] = 0u;
+        if (tid == 0) *slotmask = 0;
+    }
+    const long long units = g.P * rg.nht;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const long long p = u / rg.nht;
+        const int h0 = (int)(u - p * rg.nht) * rg.TH;
+        const int h1 = min(h0 + rg.TH, g.H);
+        const int h0W = h0 * W;
+        const int L = (h1 - h0) * W;
+        const int ohl = ax_lo<AD>(rg.ah, h0), ohh = ax_hi<AD>(rg.ah, h1 - 1);
+        const int nw = ohh >= ohl ? (ohh - ohl + 1) * OW : 0;
+        const long long pbase = p * (long long)g.vol;
+        const int pv = (int)(pbase & (VEC - 1));
+        T* gplane = gi + pbase;
+        // this thread's windows me = tid + k * NT: first (h, w) offset of each,
+        // and (adaptive) its lengths and the distances to the next windows
+        int wo[WPT];
+        int wsh[WPT];    // adaptive: kh | kw << 8 | sh << 16 | sw << 24 (each < 256)
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) {
+            const int me = tid + k * NT;
+            const int row = rg.fOW.div(me);
+            const int oh = min(ohl + row, g.OH - 1), ow = me - row * OW;   // slots past nw stay idle
+            const int hs = ax_start<AD>(rg.ah, oh), ws = ax_start<AD>(rg.aw, ow);
+            wo[k] = hs * W + ws;
+            if constexpr (AD) {
+                const int kh = ax_end<AD>(rg.ah, oh) - hs, kw = ax_end<AD>(rg.aw, ow) - ws;
+                const int sh = oh + 1 < g.OH ? ax_start<AD>(rg.ah, oh + 1) - hs : 255;
+                const int sw = ow + 1 < OW ? ax_start<AD>(rg.aw, ow + 1) - ws : 255;
+                wsh[k] = kh | kw << 8 | sh << 16 | sw << 24;
+            } else {
+                wsh[k] = 0;
+            }
+        }
+        const long long rstride = (long long)g.OH * OW;
+        const int64_t* ip = idx + p * (long long)g.ovol + (long long)ohl * OW + tid;
+        const T* gp = go + p * (long long)g.ovol + (long long)ohl * OW + tid;
+        int64_t rj[WPT];
+        T rgd[WPT];
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) {
+            const bool in = tid + k * NT < nw;
+            rj[k] = in ? __ldg(ip + k * NT) : -1;
+            rgd[k] = in ? gp[k * NT] : Elem<T>::from_f(0.0f);
+        }
+        int ds = 0, sbase = 0;          // first slice of the row and its ring slot
+        __syncthreads();   // the ring is clear (first unit: initialised) before any pass
+        for (int od = 0; od < OD; ++od) {
+            const int de = ax_end<AD>(rg.ad, od);      // slices at or beyond de are in no window
+            const int kd = de - ds;
+            const int dsHW = ds * HW;
+            const int pvt = pv + dsHW + h0W;
+            // 1. decode this row (key 4: the window adds nothing here);
+            //    mark inputs reached by -0 gradients
+            int key[WPT], off[WPT];
+            float gv[WPT];
+#pragma unroll
+            for (int k = 0; k < WPT; ++k) {
+                const int64_t j = rj[k];
+                gv[k] = Elem<T>::to_f(rgd[k]);
+                const int rel = (int)j - dsHW - wo[k];
+                const int offd = rg.fHW.div(rel);
+                const int rem = rel - offd * HW;
+                const int offh = rg.fW.div(rem);
+                const int offw = rem - offh * W;
+                int kh, kw, sh, sw;
+                if constexpr (AD) {
+                    kh = wsh[k] & 255; kw = (wsh[k] >> 8) & 255;
+                    sh = (wsh[k] >> 16) & 255; sw = (unsigned)wsh[k] >> 24;
+                } else {
+                    kh = g.kh; kw = g.kw; sh = g.sh; sw = g.sw;
+                }
+                const int loc = wo[k] - h0W + rem;      // place inside the h-tile's rows
+                const bool ok = (uint64_t)j < (uint64_t)g.vol && rel >= 0 && offd < kd && offh < kh &&
+                                offw < kw && (unsigned)loc < (unsigned)L;
+                int slot = sbase + offd;
+                slot -= slot >= RS ? RS : 0;
+                const int ph = (pvt + offd * HW) & (VEC - 1);
+                off[k] = (slot * SSTR + ph + loc) * (int)sizeof(float);
+                key[k] = ok ? ((offh >= sh ? 0 : 2) | (offw >= sw ? 0 : 1)) : 4;
+                if (ok && __float_as_uint(gv[k]) == 0x80000000u) {
+                    const int a = off[k] >> 2;
+                    atomicOr(&negbits[a >> 5], 1u << (a & 31));
+                    atomicOr(slotmask, 1 << slot);
+                }
+            }
+            // the next row's loads are in flight during the passes and the store
+            if (od + 1 < OD) {
+                ip += rstride;
+                gp += rstride;
+#pragma unroll
+                for (int k = 0; k < WPT; ++k) {
+                    if (tid + k * NT < nw) {
+                        rj[k] = __ldg(ip + k * NT);
+                        rgd[k] = gp[k * NT];
+                    }
+                }
+            }
+            // 2. four ordered passes
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int k = 0; k < WPT; ++k)
+                    if (key[k] == q) {
+                        float* a = reinterpret_cast<float*>(reinterpret_cast<char*>(ring) + off[k]);
+                        *a += gv[k];
+                    }
+                __syncthreads();
+            }
+            // 3. round and store the completed slices [ds, dn), clear their accumulators
+            const int dn = od + 1 < OD ? ax_start<AD>(rg.ad, od + 1) : g.D;
+            const int nring = min(dn, de) - ds;        // completed slices held in the ring
+            const int stored = ((1 << nring) - 1) << sbase | ((1 << nring) - 1) >> (RS - sbase);
+            const int marked = *slotmask & stored;
+            if (marked) {
+                // inputs chosen only by -0 gradients: accumulator +0 -> -0
+                for (int s = 0; s < nring; ++s) {
+                    int slot = sbase + s;
+                    slot -= slot >= RS ? RS : 0;
+                    if (!((marked >> slot) & 1)) continue;
+                    const int off0 = (ds + s) * HW + h0W;
+                    const int ph = (pv + off0) & (VEC - 1);
+                    for (int i = tid; i < SSTR / 32; i += NT) {
+                        unsigned m = negbits[slot * (SSTR / 32) + i];
+                        negbits[slot * (SSTR / 32) + i] = 0u;
+                        while (m) {
+                            const int b = __ffs(m) - 1;
+                            m &= m - 1;
+                            float* acc = ring + slot * SSTR + i * 32 + b;
+                            if (__float_as_uint(*acc) == 0u &&
+                                roll_all_negzero<T, AD>(go, idx, p, off0 + i * 32 + b - ph, g, rg))
+                                *acc = -0.0f;
+                        }
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) *slotmask &= ~stored;
+            }
+            for (int s = 0; s < dn - ds; ++s) {
+                const int off0 = (ds + s) * HW + h0W;
+                const int ph = (pv + off0) & (VEC - 1);
+                T* dst = gplane + (off0 - ph);          // on a 16-byte boundary
+                const int nch = (ph + L + VEC - 1) / VEC;
+                const bool cov = s < nring;
+                int slot = sbase + s;
+                slot -= slot >= RS ? RS : 0;
+                float* src = ring + slot * SSTR;
+                for (int c = tid; c < nch; c += NT) {
+                    const int e0 = c * VEC - ph;
+                    Vec16<T> out;
+                    if (cov) out.u = roll_take<T>(src + c * VEC);
+                    else out.u = make_uint4(0u, 0u, 0u, 0u);
+                    if (e0 >= 0 && e0 + VEC <= L) {
+                        *reinterpret_cast<uint4*>(dst + c * VEC) = out.u;
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < VEC; ++t)
+                            if (e0 + t >= 0 && e0 + t < L) dst[c * VEC + t] = out.e[t];
+                    }
+                }
+            }
+            // the next row starts at dn; its slot follows
+            sbase += dn - ds;
+            while (sbase >= RS) sbase -= RS;
+            ds = dn;
+            __syncthreads();
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+// Windows along one axis as the host sees them.
+struct HostAxis {
+    int I, O, K, S;
+    bool adaptive;
+    long long start(int o) const { return adaptive ? (long long)o * I / O : (long long)o * S; }
+    long long end(int o) const {
+        return adaptive ? ((long long)(o + 1) * I + O - 1) / O : (long long)o * S + K;
+    }
+    int lo(int x) const {
+        if (adaptive) return (int)((long long)x * O / I);
+        return x < K ? 0 : (x - K) / S + 1;
+    }
+    int hi(int x) const {
+        if (adaptive) return (int)(((long long)(x + 1) * O - 1) / I);
+        const int h = x / S;
+        return h < O - 1 ? h : O - 1;
+    }
+    // At most two windows cover any position.
+    bool two_cover() const {
+        if (!adaptive) return K <= 2 * S;
+        for (int i = 0; i + 2 < O; ++i)
+            if (end(i) > start(i + 2)) return false;
+        return true;
+    }
+    int longest() const {
+        if (!adaptive) return K;
+        long long m = 0;
+        for (int i = 0; i < O; ++i) m = end(i) - start(i) > m ? end(i) - start(i) : m;
+        return (int)m;
+    }
+};
+
+HostAxis host_axis(int I, int O, int K, int S, bool adaptive) {
+    HostAxis a;
+    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive;
+    return a;
+}
+
+struct RollCfg {
+    int nt, wpt;     // threads, and windows per thread at most (1, 2 or 4)
+    int minb;        // CTAs per SM the registers are sized for
+    size_t budget;   // shared bytes per CTA
+};
+
+// 256 threads holding up to 4 windows each (64 registers), at most 54 KB of
+// shared memory, so that four CTAs fit on an SM. A launch compiles for the
+// fewest windows per thread that its h-tiles need.
+constexpr RollCfg kRollCfg = {256, 4, 4, 54 * 1024};
+
+size_t roll_smem(int RS, int SSTR) {
+    const size_t nacc = (size_t)RS * SSTR;
+    return nacc * sizeof(float) + nacc / 8 + sizeof(int);
+}
+
+// Fills rg (h-tiling, ring size), the shared bytes and the windows per
+// thread for geometry g, or returns false when the kernel does not apply.
+// The planes are split into the fewest h-tiles that fit, and into more when
+// that gives fewer than min_units CTAs (rows of at least 8 per h-tile).
+bool roll_plan(const Geo& g, int es, long long min_units, RollGeo* rg, size_t* smem, int* wpt) {
+    const bool a = g.adaptive != 0;
+    if (g.P == 0) return false;
+    if (a) {   // products used by the adaptive window arithmetic stay below 2^31
+        const long long lim = (1LL << 31) - 1;
+        if ((long long)g.D * g.OD + g.OD > lim || (long long)g.H * g.OH + g.OH > lim ||
+            (long long)g.W * g.OW + g.OW > lim)
+            return false;
+        if (g.OD > (1 << 20) || g.OH > (1 << 20) || g.OW > (1 << 20)) return false;
+    }
+    const HostAxis ad = host_axis(g.D, g.OD, g.kd, g.sd, a);
+    const HostAxis ah = host_axis(g.H, g.OH, g.kh, g.sh, a);
+    const HostAxis aw = host_axis(g.W, g.OW, g.kw, g.sw, a);
+    if (!ad.two_cover() || !ah.two_cover() || !aw.two_cover()) return false;
+    const int vec = 16 / es;
+    const int RS = ad.longest();
+    if (RS > 30) return false;                                  // slots fit a bit mask
+    if (a && (ah.longest() > 254 || aw.longest() > 254)) return false;   // packed in bytes
+    const RollCfg cfg = kRollCfg;
+    for (int nht = 1; nht <= g.H; ++nht) {
+        const int TH = (g.H + nht - 1) / nht;
+        if ((g.H + TH - 1) / TH != nht) continue;
+        const long long span = (long long)TH * g.W + vec - 1;
+        const long long SSTR = (span + 31) / 32 * 32;
+        if (SSTR * RS > (1LL << 24)) continue;
+        if (roll_smem(RS, (int)SSTR) > cfg.budget) continue;
+        long long most = 0;
+        for (int h0 = 0; h0 < g.H; h0 += TH) {
+            const int h1 = h0 + TH < g.H ? h0 + TH : g.H;
+            const int lo = ah.lo(h0), hi = ah.hi(h1 - 1);
+            const long long n = hi >= lo ? (long long)(hi - lo + 1) * g.OW : 0;
+            most = n > most ? n : most;
+        }
+        if (most > (long long)cfg.nt * cfg.wpt) continue;
+        if (g.P * nht < min_units && TH > 8) {
+            // more h-tiles for more CTAs, as long as each keeps 8 rows
+            long long want = (min_units + g.P - 1) / g.P;
+            long long cap = (g.H + 7) / 8;
+            const int n2 = (int)(want < cap ? want : cap);
+            if (n2 > nht) {
+                nht = n2 - 1;   // the loop's increment tries n2 next
+                continue;
+            }
+        }
+        *wpt = most <= cfg.nt ? 1 : most <= 2 * cfg.nt ? 2 : 4;
+        rg->TH = TH;
+        rg->nht = nht;
+        rg->RS = RS;
+        rg->SSTR = (int)SSTR;
+        rg->ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
+        rg->ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
+        rg->aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
+        rg->fHW = FastDiv((uint32_t)(g.H * g.W));
+        rg->fW = FastDiv((uint32_t)g.W);
+        rg->fOW = FastDiv((uint32_t)g.OW);
+        *smem = roll_smem(RS, (int)SSTR);
+        return true;
+    }
+    return false;
+}
+
+template <typename T, bool AD, int WPT>
+cudaError_t roll_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                        const RollGeo& rg, size_t smem, cudaStream_t s) {
+    constexpr int NT = kRollCfg.nt, MINB = kRollCfg.minb;
+    auto kern = k_bwd_roll<T, AD, NT, WPT, MINB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long units = g.P * rg.nht;
+    const unsigned grid = (unsigned)(units < INT_MAX ? units : INT_MAX);
+    kern<<<grid, NT, smem, s>>>((const T*)go, idx, (T*)gi, g, rg);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, int sms,
+                   cudaStream_t s) {
+    RollGeo rg;
+    size_t smem = 0;
+    int wpt = 0;
+    // one wave of CTAs at kRollCfg.minb per SM
+    const long long min_units = 1LL * sms * kRollCfg.minb;
+    if (!roll_plan(g, sizeof(T), min_units, &rg, &smem, &wpt)) return cudaErrorNotSupported;
+    if (g.adaptive) {
+        if (wpt == 1) return roll_launch<T, true, 1>(go, idx, gi, g, rg, smem, s);
+        if (wpt == 2) return roll_launch<T, true, 2>(go, idx, gi, g, rg, smem, s);
+        return roll_launch<T, true, 4>(go, idx, gi, g, rg, smem, s);
+    }
+    if (wpt == 1) return roll_launch<T, false, 1>(go, idx, gi, g, rg, smem, s);
+    if (wpt == 2) return roll_launch<T, false, 2>(go, idx, gi, g, rg, smem, s);
+    return roll_launch<T, false, 4>(go, idx, gi, g, rg, smem, s);
+}
+
+int elem_bytes(int dtype) { return dtype == F32 ? 4 : 2; }
+
+}  // namespace
+
+bool bwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
+    RollGeo rg;
+    size_t smem = 0;
+    int wpt = 0;
+    return aligned16 && roll_plan(g, elem_bytes(dtype), 0, &rg, &smem, &wpt);
+}
+
+cudaError_t launch_bwd_roll(const void* go, const int64_t* idx, void* gi, const Geo& g, int dtype,
+                            int sms, cudaStream_t s) {
+    switch (dtype) {
+    case F32: return roll_t<float>(go, idx, gi, g, sms, s);
+    case F16: return roll_t<__half>(go, idx, gi, g, sms, s);
+    default: return roll_t<__nv_bfloat16>(go, idx, gi, g, sms, s);
+    }
+}
+
+}  // namespace mp3d

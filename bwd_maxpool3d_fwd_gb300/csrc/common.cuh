@@ -95,6 +95,52 @@ struct FastDiv {
     __host__ __device__ __forceinline__ int mod(int n, int q) const { return n - q * (int)d; }
 };
 
+// ---------------------------------------------------------------- windows per axis
+// Windows along one axis, fixed (K, S) or adaptive (I -> O), with the
+// divisions done by multiply-shift. Adaptive products (o + 1) * I and
+// (x + 1) * O must stay below 2^31 (checked by the launchers).
+struct AxisMap {
+    int I, O, K, S;
+    int adaptive;
+    FastDiv fS;   // fixed: divide by S
+    FastDiv fI;   // adaptive: divide by I
+    FastDiv fO;   // adaptive: divide by O
+    // Window o along this axis: [start(o), end(o)).
+    __device__ __forceinline__ int start(int o) const { return adaptive ? fO.div(o * I) : o * S; }
+    __device__ __forceinline__ int end(int o) const {
+        return adaptive ? fO.div((o + 1) * I + O - 1) : o * S + K;
+    }
+    __device__ __forceinline__ int len(int o) const {
+        return adaptive ? fO.div((o + 1) * I + O - 1) - fO.div(o * I) : K;
+    }
+    __device__ __forceinline__ int lo(int x) const {
+        if (adaptive) return fI.div(x * O);
+        return x < K ? 0 : fS.div(x - K) + 1;
+    }
+    __device__ __forceinline__ int hi(int x) const {
+        if (adaptive) return fI.div((x + 1) * O - 1);
+        const int h = fS.div(x);
+        return h < O - 1 ? h : O - 1;
+    }
+    // Windows before o that also cover position start(o) + rel.
+    __device__ __forceinline__ int earlier(int o, int rel) const {
+        if (adaptive) return o - lo(start(o) + rel);
+        const int e = fS.div(K - 1 - rel);
+        return e < o ? e : o;
+    }
+};
+
+// Host-side construction of an AxisMap.
+inline AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
+    AxisMap a;
+    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
+    a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
+    a.fI = FastDiv((uint32_t)I);
+    a.fO = FastDiv((uint32_t)O);
+    return a;
+}
+
+
 // ---------------------------------------------------------------- vectors
 
 // Element-wise access to a 16-byte vector of T.

@@ -40,6 +40,12 @@ cudaError_t launch_bwd_overlap_tile(const void* go, const int64_t* idx, void* gi
 // Whether the tiled owner gather handles this geometry (its staged windows fit
 // in shared memory).
 bool bwd_tile_supported(const Geo& g);
+// Ordered scatter into a rolling ring of shared depth slices (bwd_roll.cu):
+// at most two windows cover any position along each axis, the ring fits in
+// shared memory, and grad_in starts on a 16-byte boundary.
+bool bwd_roll_supported(const Geo& g, int dtype, bool aligned16);
+cudaError_t launch_bwd_roll(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                            int dtype, int sms, cudaStream_t s);
 cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, float* ws,
                               const Geo& g, int dtype, int sms, cudaStream_t s);
 

@@ -86,7 +86,9 @@ typedef enum {
     MP3D_PATH_BWD_DISJOINT = 10,     /* single-pass gather, disjoint windows  */
     MP3D_PATH_BWD_OVERLAP_TILE = 11, /* overlapping gather, staged tile + owner sums */
     MP3D_PATH_BWD_OVERLAP_DIRECT = 12, /* overlapping gather, direct reads    */
-    MP3D_PATH_BWD_ATOMIC = 13        /* zero fill + atomic scatter ablation   */
+    MP3D_PATH_BWD_ATOMIC = 13,       /* zero fill + atomic scatter ablation   */
+    MP3D_PATH_BWD_OVERLAP_ROLL = 14  /* overlapping, ordered scatter into a
+                                        rolling ring of shared depth slices  */
 } mp3d_path;
 
 /*

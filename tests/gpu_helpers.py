@@ -32,10 +32,16 @@ def gpu_fwd(x_cpu, kernel=None, stride=None, out_size=None):
     return y.cpu(), idx.cpu()
 
 
-def gpu_bwd(g_cpu, idx_cpu, in_shape, kernel=None, stride=None, algo=mp.BWD_AUTO):
+def gpu_bwd(g_cpu, idx_cpu, in_shape, kernel=None, stride=None, algo=mp.BWD_AUTO, offset=0):
+    """Backward on the GPU; returns grad_in on the CPU. offset > 0 places
+    grad_in that many elements past a 16-byte boundary (paths that need
+    aligned 16-byte stores then give way to the others)."""
     g = g_cpu.to(DEV)
     idx = idx_cpu.to(DEV)
-    gin = torch.empty(in_shape, dtype=g.dtype, device=DEV)
+    n = 1
+    for v in in_shape:
+        n *= v
+    gin = torch.empty(n + offset, dtype=g.dtype, device=DEV)[offset:].view(in_shape)
     ws = None
     nbytes = mp.maxpool3d_bwd_workspace_bytes(in_shape, g.dtype, algo)
     if nbytes:

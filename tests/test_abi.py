@@ -122,9 +122,8 @@ def test_stated_output_sizes():
 def test_plans_per_workload(L):
     expect_fwd = {0: {"fwd_slab"}, 1: {"fwd_slab"}, 2: {"fwd_s2"}, 3: {"fwd_s2"},
                   4: {"fwd_global"}}
-    expect_bwd = {0: {"bwd_disjoint"}, 1: {"bwd_overlap_tile", "bwd_overlap_direct"},
-                  2: {"bwd_disjoint"}, 3: {"bwd_overlap_tile", "bwd_overlap_direct"},
-                  4: {"bwd_disjoint"}}
+    expect_bwd = {0: {"bwd_disjoint"}, 1: {"bwd_overlap_roll"}, 2: {"bwd_disjoint"},
+                  3: {"bwd_overlap_roll"}, 4: {"bwd_disjoint"}}
     for n, w in enumerate(workloads.WORKLOADS):
         if w.mode == "fixed":
             pf = mp.maxpool3d_fwd_plan(w.in_shape, w.kernel, w.stride, w.dtype)
@@ -150,6 +149,20 @@ def test_plan_rules(L):
     assert mp.maxpool3d_bwd_plan((1, 1, 3, 3, 3), (5, 5, 5), None, None,
                                  torch.float32) != "bwd_disjoint"
     assert mp.maxpool3d_fwd_plan((0, 4, 3, 3, 3), (2, 2, 2), (1, 1, 1), torch.float32) == "noop"
+    # at most two windows over any position on every axis: the rolling scatter
+    assert mp.maxpool3d_bwd_plan((1, 1, 9, 9, 9), (4, 4, 4), (3, 3, 3), (2, 2, 2),
+                                 torch.bfloat16) == "bwd_overlap_roll"
+    assert mp.maxpool3d_bwd_plan((1, 1, 9, 9, 9), (8, 8, 8), (2, 2, 2), (1, 1, 1),
+                                 torch.float32) == "bwd_overlap_roll"
+    # three windows over a position along d only: the tiled owner gather
+    assert mp.maxpool3d_bwd_plan((1, 1, 9, 8, 8), (7, 4, 4), (3, 2, 2), (1, 2, 2),
+                                 torch.float16) == "bwd_overlap_tile"
+    # three windows over a position on every axis (kernel 3, stride 1; adaptive
+    # 3 -> 5 has windows [0,1) [0,2) [1,2) [1,3) [2,3)): the direct gather
+    assert mp.maxpool3d_bwd_plan((1, 1, 9, 9, 9), (7, 7, 7), (3, 3, 3), (1, 1, 1),
+                                 torch.float16) == "bwd_overlap_direct"
+    assert mp.maxpool3d_bwd_plan((1, 1, 3, 3, 3), (5, 5, 5), None, None,
+                                 torch.float32) == "bwd_overlap_direct"
 
 
 def test_binding_rejects_cpu_tensors(L):

@@ -287,22 +287,33 @@ def test_no_device_error_flags_after_suite():
     assert mp.mp3d_device_error_flags(clear=True) == 0
 
 
-# Overlapping shapes for the tiled owner gather: several tiles per plane,
-# inputs claimed by up to eight windows, ties (many shared winners).
-TILE_CASES = [((3, 3, 3), (2, 2, 2), (2, 3, 40, 30, 24)), ((2, 2, 2), (1, 1, 1), (1, 2, 20, 33, 17)),
+# Overlapping shapes with at most two windows over any position on every
+# axis: the rolling ordered scatter. Several h-tiles per plane for the large
+# planes, ragged rows (H*W not a multiple of the vector width), inputs
+# claimed by up to eight windows, ties (many shared winners).
+ROLL_CASES = [((3, 3, 3), (2, 2, 2), (2, 3, 40, 30, 24)), ((2, 2, 2), (1, 1, 1), (1, 2, 20, 33, 17)),
               ((3, 2, 3), (2, 1, 2), (2, 2, 13, 9, 40)), ((4, 4, 4), (3, 3, 3), (1, 2, 22, 19, 31)),
-              # large output planes: several depth tiles per plane, odd H*W
               ((3, 3, 3), (2, 2, 2), (1, 2, 24, 112, 112)), ((3, 3, 3), (2, 2, 2), (1, 2, 20, 113, 114)),
-              # compiled fixed-window variants on aligned planes
-              ((2, 2, 2), (1, 1, 1), (1, 2, 12, 20, 16)), ((3, 3, 3), (2, 2, 2), (2, 2, 17, 31, 40))]
+              ((2, 2, 2), (1, 1, 1), (1, 2, 12, 20, 16)), ((3, 3, 3), (2, 2, 2), (2, 2, 17, 31, 40)),
+              # kernel < stride on d (uncovered slices), overlap on h and w
+              ((1, 3, 2), (3, 2, 1), (2, 2, 10, 21, 30)),
+              # a tall plane: many h-tiles
+              ((3, 3, 3), (2, 2, 2), (1, 2, 7, 301, 45)),
+              # wide rows: h-tiles of about 500 and 900 windows (two and four
+              # windows per thread)
+              ((3, 3, 3), (2, 2, 2), (1, 2, 9, 64, 200)), ((3, 3, 3), (2, 2, 2), (1, 2, 5, 20, 600))]
+# Adaptive shapes with at most two windows over any position.
+ROLL_ADAPTIVE = [((2, 3, 30, 50, 50), (8, 12, 12)), ((1, 2, 10, 12, 9), (4, 5, 4)),
+                 ((2, 2, 9, 7, 13), (5, 4, 8)), ((1, 3, 5, 6, 7), (3, 3, 3)),
+                 ((1, 2, 33, 250, 17), (10, 60, 5))]
 
 
 @pytest.mark.parametrize("dtype", DTYPES, ids=str)
-@pytest.mark.parametrize("case", range(len(TILE_CASES)))
-def test_overlap_tile_backward(case, dtype):
-    k, s, shape = TILE_CASES[case]
+@pytest.mark.parametrize("case", range(len(ROLL_CASES)))
+def test_overlap_roll_backward(case, dtype):
+    k, s, shape = ROLL_CASES[case]
     out = mp.pool_out_size(shape[2:], k, s)
-    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_tile"
+    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_roll"
     gen = torch.Generator().manual_seed(8000 + case)
     x = random_input(gen, shape, dtype, "ties")
     _, i_ref = oracle.maxpool3d_fwd(x, k, s)
@@ -311,17 +322,57 @@ def test_overlap_tile_backward(case, dtype):
                       "grad_in")
 
 
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(ROLL_ADAPTIVE)))
+def test_overlap_roll_backward_adaptive(case, dtype):
+    shape, out = ROLL_ADAPTIVE[case]
+    assert mp.maxpool3d_bwd_plan(shape, out, None, None, dtype) == "bwd_overlap_roll"
+    gen = torch.Generator().manual_seed(8050 + case)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    assert_bits_equal(gpu_bwd(g, i_ref, shape), oracle.maxpool3d_bwd(g, i_ref, shape[2:]),
+                      "grad_in")
+
+
+# The same overlapping shapes with grad_in one element past a 16-byte
+# boundary: the rolling scatter needs aligned rows, so the tiled owner gather
+# (and, for its compiled windows, the chunk gather) takes them. Plus shapes
+# with three windows over a position along one axis, which the tiled gather
+# takes at any alignment.
+TILE_ONLY = [((3, 2, 2), (1, 2, 2), (2, 2, 15, 18, 20)), ((2, 4, 3), (2, 1, 2), (1, 3, 9, 20, 33))]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(ROLL_CASES) + len(TILE_ONLY)))
+def test_overlap_tile_backward(case, dtype):
+    allc = ROLL_CASES + TILE_ONLY
+    k, s, shape = allc[case]
+    out = mp.pool_out_size(shape[2:], k, s)
+    offset = 1 if case < len(ROLL_CASES) else 0
+    if offset == 0:
+        assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_tile"
+    gen = torch.Generator().manual_seed(8200 + case)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s, offset=offset),
+                      oracle.maxpool3d_bwd(g, i_ref, shape[2:]), "grad_in")
+
+
 # Gradients holding -0 and +0 on inputs claimed by several windows: a sum
 # whose terms are all -0 is -0, any other all-zero sum is +0, and inputs no
-# window chose are +0. Also infinite and NaN gradients.
+# window chose are +0. Also infinite and NaN gradients. Run on the rolling
+# scatter (aligned grad_in) and on the gathers (offset grad_in).
 @pytest.mark.parametrize("dtype", DTYPES, ids=str)
 @pytest.mark.parametrize("window", [((3, 3, 3), (2, 2, 2)), ((2, 2, 2), (1, 1, 1))], ids=["k3s2", "k2s1"])
 @pytest.mark.parametrize("grad", ["mixed_zeros", "all_negative_zero", "non_finite"])
-def test_overlap_backward_signed_zero_gradients(window, dtype, grad):
+@pytest.mark.parametrize("offset", [0, 1], ids=["roll", "gather"])
+def test_overlap_backward_signed_zero_gradients(window, dtype, grad, offset):
     k, s = window
     shape = (2, 2, 11, 14, 24)
     out = mp.pool_out_size(shape[2:], k, s)
-    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_tile"
+    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_roll"
     gen = torch.Generator().manual_seed(8100)
     x = random_input(gen, shape, dtype, "ties")
     _, i_ref = oracle.maxpool3d_fwd(x, k, s)
@@ -346,4 +397,4 @@ def test_overlap_backward_signed_zero_gradients(window, dtype, grad):
     ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
     if grad != "non_finite":
         assert bool((bits(ref) == bits(torch.tensor(-0.0).to(dtype))).any())
-    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), ref, "grad_in")
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s, offset=offset), ref, "grad_in")
