@@ -338,6 +338,80 @@ k_bwd_disjoint_rows(const T* __restrict__ go, const int64_t* __restrict__ idx,
     }
 }
 
+// ------------------------------------------------------------------ disjoint, window blocks
+// Windows that tile the input exactly (kernel == stride on every axis, the
+// input a whole number of windows, rows that split into 16-byte chunks).
+// One thread owns NW = VEC / KW consecutive windows of one window row
+// (od, oh): it loads their indices and gradients once (vector loads) and
+// writes every input they cover, KD * KH output chunks of VEC elements, each
+// element the gradient of its window when the stored index names it and
+// zero otherwise.
+template <typename T, int KD, int KH, int KW>
+__global__ void __launch_bounds__(256)
+k_bwd_disjoint_blocks(const T* __restrict__ go, const int64_t* __restrict__ idx,
+                      T* __restrict__ gi, Geo g, FastDiv fSpr, FastDiv fOH) {
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int NW = VEC / KW;
+    static_assert(NW * KW == VEC, "windows fill a chunk");
+    const int HW = g.H * g.W;
+    const int spr = g.OW / NW;                      // segments per window row
+    const int nseg = g.ovol / NW;                   // segments per plane
+    const T zero = Elem<T>::from_f(0.0f);
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        for (int sg = blockIdx.x * blockDim.x + threadIdx.x; sg < nseg; sg += gridDim.x * blockDim.x) {
+            const int row = fSpr.div(sg);
+            const int ow0 = (sg - row * spr) * NW;
+            const int od = fOH.div(row);
+            const int oh = row - od * g.OH;
+            const long long o0 = p * (long long)g.ovol + (long long)sg * NW;
+            int64_t j[NW];
+            T gv[NW];
+            {
+                const uint4* ip = reinterpret_cast<const uint4*>(idx + o0);
+#pragma unroll
+                for (int v = 0; v < NW / 2; ++v) {
+                    const uint4 q = __ldg(ip + v);
+                    j[2 * v] = (int64_t)((uint64_t)q.y << 32 | q.x);
+                    j[2 * v + 1] = (int64_t)((uint64_t)q.w << 32 | q.z);
+                }
+                if (NW == 1) j[0] = __ldg(idx + o0);
+#pragma unroll
+                for (int k = 0; k < NW; ++k) gv[k] = go[o0 + k];
+            }
+            // place of each window's winner: row code dd * KH + hh (or -1), column ww
+            const int base = (od * KD) * HW + (oh * KH) * g.W + ow0 * KW;
+            int code[NW], ww[NW];
+#pragma unroll
+            for (int k = 0; k < NW; ++k) {
+                const int rel = (int)j[k] - (base + k * KW);
+                int dd = 0, hh = 0;
+#pragma unroll
+                for (int i = 1; i < KD; ++i) dd += rel >= i * HW;
+                const int r1 = rel - dd * HW;
+#pragma unroll
+                for (int i = 1; i < KH; ++i) hh += r1 >= i * g.W;
+                ww[k] = r1 - hh * g.W;
+                const bool ok = (uint64_t)j[k] < (uint64_t)g.vol && rel >= 0 && rel < KD * HW &&
+                                r1 < KH * g.W && ww[k] < KW;
+                code[k] = ok ? dd * KH + hh : -1;
+            }
+            T* out = gi + p * (long long)g.vol + base;
+#pragma unroll
+            for (int dd = 0; dd < KD; ++dd)
+#pragma unroll
+                for (int hh = 0; hh < KH; ++hh) {
+                    Vec16<T> c;
+#pragma unroll
+                    for (int k = 0; k < NW; ++k)
+#pragma unroll
+                        for (int t = 0; t < KW; ++t)
+                            c.e[k * KW + t] = (code[k] == dd * KH + hh && ww[k] == t) ? gv[k] : zero;
+                    *reinterpret_cast<uint4*>(out + dd * HW + hh * g.W) = c.u;
+                }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ overlap, tiles
 // Overlapping windows, deterministic gather. One CTA owns a tile of TD
 // depth slices of one plane and every input in it:
@@ -688,6 +762,17 @@ static cudaError_t bwd_disjoint_t(const void* go, const int64_t* idx, void* gi, 
             k_bwd_global<T, VEC><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g.P, g.vol);
         else
             k_bwd_global<T, 1><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g.P, g.vol);
+        return cudaGetLastError();
+    }
+    // exact tiling by 2x2x2 windows: one thread per run of windows
+    if (aligned && (uintptr_t)idx % 16 == 0 && g.kd == 2 && g.kh == 2 && g.kw == 2 && g.sd == 2 &&
+        g.sh == 2 && g.sw == 2 && g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW &&
+        g.W % VEC == 0) {
+        constexpr int NW = VEC / 2;
+        const int nseg = g.ovol / NW;
+        dim3 grid((unsigned)((nseg + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
+        k_bwd_disjoint_blocks<T, 2, 2, 2><<<grid, 256, 0, s>>>(
+            (const T*)go, idx, (T*)gi, g, FastDiv((uint32_t)(g.OW / NW)), FastDiv((uint32_t)g.OH));
         return cudaGetLastError();
     }
     if (aligned && g.W % VEC == 0) {
