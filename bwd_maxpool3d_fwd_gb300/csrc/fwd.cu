@@ -596,6 +596,106 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
     }
 }
 
+// ------------------------------------------------------------------ 2x2x2 tiling
+// Windows 2x2x2 with stride 2 that tile the input exactly, rows that split
+// into 16-byte chunks. One thread per run of four windows of one window row
+// (od, oh): four 16-byte loads (input rows (dd, hh) of the run, straight
+// from global memory), packed two-window compares (W, then H, then D; a
+// strictly greater value replaces, so the first occurrence wins), one 8-byte
+// store of the four maxima and two 16-byte stores of their indices. When a
+// NaN or an infinity was loaded, the four windows are rescanned exactly from
+// the loaded rows with the scalar rule.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_fwd_k2s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
+           FastDiv fSpr, FastDiv fOH) {
+    constexpr int NW = 4;
+    const int HW = g.H * g.W;
+    const int spr = g.OW / NW;
+    const int nseg = g.ovol / NW;
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        const T* xp = x + p * g.vol;
+        for (int sg = blockIdx.x * blockDim.x + threadIdx.x; sg < nseg; sg += gridDim.x * blockDim.x) {
+            const int row = fSpr.div(sg);
+            const int ow0 = (sg - row * spr) * NW;
+            const int od = fOH.div(row);
+            const int oh = row - od * g.OH;
+            const int base = 2 * od * HW + 2 * oh * g.W + 2 * ow0;
+            uint4 r[4];
+#pragma unroll
+            for (int dh = 0; dh < 4; ++dh)
+                r[dh] = __ldg(reinterpret_cast<const uint4*>(xp + base + (dh >> 1) * HW + (dh & 1) * g.W));
+            uint32_t poison = 0;
+#pragma unroll
+            for (int dh = 0; dh < 4; ++dh) {
+                poison = Pair<T>::poison(poison, r[dh].x);
+                poison = Pair<T>::poison(poison, r[dh].y);
+                poison = Pair<T>::poison(poison, r[dh].z);
+                poison = Pair<T>::poison(poison, r[dh].w);
+            }
+            // per row: lanes (window 2k, window 2k+1), code wl | hl << 1 | dl << 2
+            uint32_t mv[4][2], mc[4][2];
+#pragma unroll
+            for (int dh = 0; dh < 4; ++dh) {
+                const uint32_t cb = (uint32_t)(((dh >> 1) << 2) | ((dh & 1) << 1)) * kLanes;
+                mv[dh][0] = __byte_perm(r[dh].x, r[dh].y, 0x5410);
+                mc[dh][0] = cb;
+                merge2<T>(mv[dh][0], mc[dh][0], __byte_perm(r[dh].x, r[dh].y, 0x7632), cb | kLanes);
+                mv[dh][1] = __byte_perm(r[dh].z, r[dh].w, 0x5410);
+                mc[dh][1] = cb;
+                merge2<T>(mv[dh][1], mc[dh][1], __byte_perm(r[dh].z, r[dh].w, 0x7632), cb | kLanes);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                merge2<T>(mv[0][k], mc[0][k], mv[1][k], mc[1][k]);   // h within d = 0
+                merge2<T>(mv[2][k], mc[2][k], mv[3][k], mc[3][k]);   // h within d = 1
+                merge2<T>(mv[0][k], mc[0][k], mv[2][k], mc[2][k]);   // d
+            }
+            const long long o0 = p * (long long)g.ovol + (long long)sg * NW;
+            int64_t iv[NW];
+            uint2 yv = make_uint2(mv[0][0], mv[0][1]);
+            if (Pair<T>::is_poisoned(poison)) {
+                // exact scan of each window from the loaded rows (d, h, w order)
+                uint32_t yb[NW];
+#pragma unroll
+                for (int k = 0; k < NW; ++k) {
+                    uint32_t bb = 0, bc = 0;
+                    float m = 0.0f;
+#pragma unroll
+                    for (int dh = 0; dh < 4; ++dh) {
+                        const uint32_t wd = k == 0 ? r[dh].x : k == 1 ? r[dh].y : k == 2 ? r[dh].z : r[dh].w;
+#pragma unroll
+                        for (int ww = 0; ww < 2; ++ww) {
+                            const uint32_t b = (wd >> (16 * ww)) & 0xFFFFu;
+                            const uint16_t b16 = (uint16_t)b;
+                            const float v = Elem<T>::to_f(*reinterpret_cast<const T*>(&b16));
+                            if ((dh == 0 && ww == 0) || beats(v, m)) {
+                                m = v;
+                                bb = b;
+                                bc = (uint32_t)(((dh >> 1) << 2) | ((dh & 1) << 1) | ww);
+                            }
+                        }
+                    }
+                    yb[k] = bb;
+                    iv[k] = base + (int)(bc >> 2) * HW + (int)((bc >> 1) & 1) * g.W + 2 * k + (int)(bc & 1);
+                }
+                yv = make_uint2(yb[0] | yb[1] << 16, yb[2] | yb[3] << 16);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NW; ++k) {
+                    const uint32_t code = (mc[0][k >> 1] >> (16 * (k & 1))) & 7u;
+                    iv[k] = base + (int)(code >> 2) * HW + (int)((code >> 1) & 1) * g.W + 2 * k +
+                            (int)(code & 1);
+                }
+            }
+            *reinterpret_cast<uint2*>(y + o0) = yv;
+            int4* id = reinterpret_cast<int4*>(idx + o0);
+            id[0] = make_int4((int)iv[0], (int)(iv[0] >> 32), (int)iv[1], (int)(iv[1] >> 32));
+            id[1] = make_int4((int)iv[2], (int)(iv[2] >> 32), (int)iv[3], (int)(iv[3] >> 32));
+        }
+    }
+}
+
 // Window shapes with a compiled stride-2 kernel: (kd, sd, kh, sh, kw), sw = 2.
 static int s2_variant(const Geo& g) {
     if (g.adaptive || g.sw != 2) return -1;
@@ -642,6 +742,15 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
 template <typename T>
 static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                                    cudaStream_t s) {
+    // 2x2x2 windows tiling the input: direct loads, one thread per four windows
+    if (s2_variant(g) == 0 && g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW &&
+        g.OW % 4 == 0 && (uintptr_t)y % 8 == 0 && (uintptr_t)idx % 16 == 0) {
+        const int nseg = g.ovol / 4;
+        dim3 grid((unsigned)((nseg + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
+        k_fwd_k2s2<T><<<grid, 256, 0, s>>>((const T*)x, (T*)y, idx, g, FastDiv((uint32_t)(g.OW / 4)),
+                                           FastDiv((uint32_t)g.OH));
+        return cudaGetLastError();
+    }
     switch (s2_variant(g)) {
     case 0: return fwd_s2_t<T, 2, 2, 2, 2, 2>(x, y, idx, g, sms, s);
     case 1: return fwd_s2_t<T, 3, 2, 3, 2, 3>(x, y, idx, g, sms, s);
