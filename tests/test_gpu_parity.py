@@ -181,6 +181,26 @@ def test_unaligned_pointers_take_scalar_paths():
         assert_bits_equal(gind.cpu(), gin_ref, "grad_in (unaligned)")
 
 
+@pytest.mark.parametrize("dtype", (torch.float16, torch.bfloat16), ids=str)
+@pytest.mark.parametrize("window", [((2, 2, 2), (2, 2, 2)), ((3, 3, 3), (2, 2, 2))], ids=["k2s2", "k3s2"])
+def test_stride2_forward_unaligned_outputs(window, dtype):
+    # Aligned input, y and idx one element past a 16-byte boundary: the
+    # stride-2 kernels copy their outputs element by element.
+    k, s = window
+    shape = (2, 3, 10, 22, 48)
+    gen = torch.Generator().manual_seed(32)
+    x = random_input(gen, shape, dtype, "ties")
+    y_ref, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    assert mp.maxpool3d_fwd_plan(shape, k, s, dtype) == "fwd_s2"
+    yb = torch.empty(y_ref.numel() + 1, dtype=dtype, device=DEV)
+    ib = torch.empty(y_ref.numel() + 1, dtype=torch.int64, device=DEV)
+    yd, idd = yb[1:].view(y_ref.shape), ib[1:].view(y_ref.shape)
+    mp.maxpool3d_fwd(x.to(DEV), yd, idd, k, s)
+    torch.cuda.synchronize()
+    assert torch.equal(idd.cpu(), i_ref)
+    assert_bits_equal(yd.cpu(), y_ref, "y (unaligned outputs)")
+
+
 @pytest.mark.parametrize("algo", [mp.BWD_AUTO, mp.BWD_ATOMIC])
 def test_guard_bands_untouched(algo):
     # Outputs live inside larger buffers filled with a sentinel; nothing
