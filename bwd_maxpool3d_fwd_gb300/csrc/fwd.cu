@@ -56,8 +56,10 @@ k_fwd_generic(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ 
 // ------------------------------------------------------------------ global
 // One window per plane (output 1x1x1). One warp per plane: each lane scans
 // a strided share of the plane with 16-byte loads when every plane starts
-// on a 16-byte boundary, then the warp combines (value, offset) pairs.
-// The combine takes the pair that beats, and among equal values (or two
+// on a 16-byte boundary, then the warp combines (value, offset) pairs. A
+// lane meets its elements in ascending offset order, so inside a lane an
+// element replaces the running best only when it beats it; the combine
+// across lanes takes the pair that beats, and among equal values (or two
 // NaNs) the smaller offset, so the result is the first occurrence.
 __device__ __forceinline__ void take_better(float v, int i, float& m, int& best) {
     if (beats(v, m) || (!beats(m, v) && i < best)) {
@@ -85,10 +87,22 @@ k_fwd_global(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ i
                 Vec16<T> c;
                 c.u = __ldg(xv + v);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) take_better(Elem<T>::to_f(c.e[j]), v * VEC + j, m, best);
+                for (int j = 0; j < VEC; ++j) {
+                    const float f = Elem<T>::to_f(c.e[j]);
+                    if (beats(f, m) || best == INT_MAX) {
+                        m = f;
+                        best = v * VEC + j;
+                    }
+                }
             }
         }
-        for (int e = nvec * VEC + lane; e < vol; e += 32) take_better(Elem<T>::to_f(xp[e]), e, m, best);
+        for (int e = nvec * VEC + lane; e < vol; e += 32) {
+            const float f = Elem<T>::to_f(xp[e]);
+            if (beats(f, m) || best == INT_MAX) {
+                m = f;
+                best = e;
+            }
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
