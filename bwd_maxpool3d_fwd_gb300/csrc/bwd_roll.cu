@@ -129,7 +129,11 @@ __device__ __forceinline__ uint4 roll_take(float* src) {
     return out;
 }
 
-template <typename T, bool AD, int NT, int WPT, int MINB>
+// K3 (a specialization): fixed 3x3x3 windows with stride 2, sizes known at
+// compile time. AL: every row span starts on a 16-byte boundary and holds a
+// whole number of 16-byte chunks (W and D*H*W multiples of the vector width),
+// so the store has no ragged ends.
+template <typename T, bool AD, int NT, int WPT, int MINB, bool K3 = false, bool AL = false>
 __global__ void __launch_bounds__(NT, MINB)
 k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
            RollGeo rg) {
@@ -214,6 +218,8 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 if constexpr (AD) {
                     kh = wsh[k] & 255; kw = (wsh[k] >> 8) & 255;
                     sh = (wsh[k] >> 16) & 255; sw = (unsigned)wsh[k] >> 24;
+                } else if constexpr (K3) {
+                    kh = 3; kw = 3; sh = 2; sw = 2;
                 } else {
                     kh = g.kh; kw = g.kw; sh = g.sh; sw = g.sw;
                 }
@@ -222,7 +228,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                                 offw < kw && (unsigned)loc < (unsigned)L;
                 int slot = sbase + offd;
                 slot -= slot >= RS ? RS : 0;
-                const int ph = (pvt + offd * HW) & (VEC - 1);
+                const int ph = AL ? 0 : (pvt + offd * HW) & (VEC - 1);
                 off[k] = (slot * SSTR + ph + loc) * (int)sizeof(float);
                 key[k] = ok ? ((offh >= sh ? 0 : 2) | (offw >= sw ? 0 : 1)) : 4;
                 if (ok && __float_as_uint(gv[k]) == 0x80000000u) {
@@ -266,7 +272,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     slot -= slot >= RS ? RS : 0;
                     if (!((marked >> slot) & 1)) continue;
                     const int off0 = (ds + s) * HW + h0W;
-                    const int ph = (pv + off0) & (VEC - 1);
+                    const int ph = AL ? 0 : (pv + off0) & (VEC - 1);
                     for (int i = tid; i < SSTR / 32; i += NT) {
                         unsigned m = negbits[slot * (SSTR / 32) + i];
                         negbits[slot * (SSTR / 32) + i] = 0u;
@@ -283,7 +289,21 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 __syncthreads();
                 if (tid == 0) *slotmask &= ~stored;
             }
-            for (int s = 0; s < dn - ds; ++s) {
+            if constexpr (AL) {
+                for (int s = 0; s < dn - ds; ++s) {
+                    T* dst = gplane + (ds + s) * HW + h0W;     // on a 16-byte boundary
+                    const bool cov = s < nring;
+                    int slot = sbase + s;
+                    slot -= slot >= RS ? RS : 0;
+                    float* src = ring + slot * SSTR;
+                    for (int c = tid; c < L / VEC; c += NT) {
+                        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+                        if (cov) out = roll_take<T>(src + c * VEC);
+                        *reinterpret_cast<uint4*>(dst + c * VEC) = out;
+                    }
+                }
+            }
+            for (int s = 0; !AL && s < dn - ds; ++s) {
                 const int off0 = (ds + s) * HW + h0W;
                 const int ph = (pv + off0) & (VEC - 1);
                 T* dst = gplane + (off0 - ph);          // on a 16-byte boundary
@@ -438,11 +458,11 @@ bool roll_plan(const Geo& g, int es, long long min_units, RollGeo* rg, size_t* s
     return false;
 }
 
-template <typename T, bool AD, int WPT>
+template <typename T, bool AD, int WPT, bool K3 = false, bool AL = false>
 cudaError_t roll_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
                         const RollGeo& rg, size_t smem, cudaStream_t s) {
     constexpr int NT = kRollCfg.nt, MINB = kRollCfg.minb;
-    auto kern = k_bwd_roll<T, AD, NT, WPT, MINB>;
+    auto kern = k_bwd_roll<T, AD, NT, WPT, MINB, K3, AL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = g.P * rg.nht;
@@ -465,6 +485,10 @@ cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, i
         if (wpt == 2) return roll_launch<T, true, 2>(go, idx, gi, g, rg, smem, s);
         return roll_launch<T, true, 4>(go, idx, gi, g, rg, smem, s);
     }
+    constexpr int VEC = 16 / sizeof(T);
+    const bool k3 = g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 && g.sw == 2;
+    if (k3 && wpt == 4 && g.W % VEC == 0 && g.vol % VEC == 0)
+        return roll_launch<T, false, 4, true, true>(go, idx, gi, g, rg, smem, s);
     if (wpt == 1) return roll_launch<T, false, 1>(go, idx, gi, g, rg, smem, s);
     if (wpt == 2) return roll_launch<T, false, 2>(go, idx, gi, g, rg, smem, s);
     return roll_launch<T, false, 4>(go, idx, gi, g, rg, smem, s);

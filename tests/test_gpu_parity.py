@@ -418,3 +418,28 @@ def test_overlap_backward_signed_zero_gradients(window, dtype, grad, offset):
     if grad != "non_finite":
         assert bool((bits(ref) == bits(torch.tensor(-0.0).to(dtype))).any())
     assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s, offset=offset), ref, "grad_in")
+
+
+# The same gradients on wide rows (about 900 windows per h-tile, the
+# specialised 3x3x3 stride-2 form with 16-byte aligned rows).
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("grad", ["mixed_zeros", "all_negative_zero"])
+def test_overlap_roll_signed_zero_gradients_wide_rows(dtype, grad):
+    k, s = (3, 3, 3), (2, 2, 2)
+    shape = (1, 2, 5, 20, 600)
+    out = mp.pool_out_size(shape[2:], k, s)
+    assert mp.maxpool3d_bwd_plan(shape, out, k, s, dtype) == "bwd_overlap_roll"
+    gen = torch.Generator().manual_seed(8101)
+    x = random_input(gen, shape, dtype, "ties")
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    if grad == "all_negative_zero":
+        g = torch.full(i_ref.shape, -0.0).to(dtype)
+    else:
+        r = torch.rand(i_ref.shape, generator=gen)
+        g = torch.where(r < 0.4, torch.tensor(-0.0), torch.where(r < 0.7, torch.tensor(0.0),
+                                                                 torch.randint(-2, 3, i_ref.shape,
+                                                                               generator=gen).float()))
+        g = g.to(dtype)
+    ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    assert bool((bits(ref) == bits(torch.tensor(-0.0).to(dtype))).any())
+    assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), ref, "grad_in")
