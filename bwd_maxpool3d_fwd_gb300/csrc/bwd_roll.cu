@@ -385,8 +385,13 @@ struct RollCfg {
 
 // 256 threads holding up to 4 windows each (64 registers), at most 54 KB of
 // shared memory, so that four CTAs fit on an SM. A launch compiles for the
-// fewest windows per thread that its h-tiles need.
+// fewest windows per thread that its h-tiles need. The compiled 3x3x3
+// stride-2 form runs 224 threads: h-tiles of up to 896 windows then fill
+// their 4-per-thread slots more closely (on 112x112 planes, 825 windows in
+// 896 slots rather than 1024; measured 631 us against 658 us on the
+// 32x128x16x112x112 fp16 backward).
 constexpr RollCfg kRollCfg = {256, 4, 4, 54 * 1024};
+constexpr RollCfg kRollCfgK3 = {224, 4, 4, 54 * 1024};
 
 size_t roll_smem(int RS, int SSTR) {
     const size_t nacc = (size_t)RS * SSTR;
@@ -397,7 +402,8 @@ size_t roll_smem(int RS, int SSTR) {
 // thread for geometry g, or returns false when the kernel does not apply.
 // The planes are split into the fewest h-tiles that fit, and into more when
 // that gives fewer than min_units CTAs (rows of at least 8 per h-tile).
-bool roll_plan(const Geo& g, int es, long long min_units, RollGeo* rg, size_t* smem, int* wpt) {
+bool roll_plan(const Geo& g, int es, long long min_units, const RollCfg& cfg, RollGeo* rg,
+               size_t* smem, int* wpt) {
     const bool a = g.adaptive != 0;
     if (g.P == 0) return false;
     if (a) {   // products used by the adaptive window arithmetic stay below 2^31
@@ -415,7 +421,6 @@ bool roll_plan(const Geo& g, int es, long long min_units, RollGeo* rg, size_t* s
     const int RS = ad.longest();
     if (RS > 30) return false;                                  // slots fit a bit mask
     if (a && (ah.longest() > 254 || aw.longest() > 254)) return false;   // packed in bytes
-    const RollCfg cfg = kRollCfg;
     for (int nht = 1; nht <= g.H; ++nht) {
         const int TH = (g.H + nht - 1) / nht;
         if ((g.H + TH - 1) / TH != nht) continue;
@@ -461,34 +466,36 @@ bool roll_plan(const Geo& g, int es, long long min_units, RollGeo* rg, size_t* s
 template <typename T, bool AD, int WPT, bool K3 = false, bool AL = false>
 cudaError_t roll_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
                         const RollGeo& rg, size_t smem, cudaStream_t s) {
-    constexpr int NT = kRollCfg.nt, MINB = kRollCfg.minb;
-    auto kern = k_bwd_roll<T, AD, NT, WPT, MINB, K3, AL>;
+    constexpr RollCfg cfg = K3 ? kRollCfgK3 : kRollCfg;
+    auto kern = k_bwd_roll<T, AD, cfg.nt, WPT, cfg.minb, K3, AL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = g.P * rg.nht;
     const unsigned grid = (unsigned)(units < INT_MAX ? units : INT_MAX);
-    kern<<<grid, NT, smem, s>>>((const T*)go, idx, (T*)gi, g, rg);
+    kern<<<grid, cfg.nt, smem, s>>>((const T*)go, idx, (T*)gi, g, rg);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, int sms,
                    cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
     RollGeo rg;
     size_t smem = 0;
     int wpt = 0;
-    // one wave of CTAs at kRollCfg.minb per SM
-    const long long min_units = 1LL * sms * kRollCfg.minb;
-    if (!roll_plan(g, sizeof(T), min_units, &rg, &smem, &wpt)) return cudaErrorNotSupported;
+    // one wave of CTAs at minb per SM
+    const bool k3 = !g.adaptive && g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 &&
+                    g.sw == 2 && g.W % VEC == 0 && g.vol % VEC == 0;
+    if (k3 && roll_plan(g, sizeof(T), 1LL * sms * kRollCfgK3.minb, kRollCfgK3, &rg, &smem, &wpt) &&
+        wpt == 4)
+        return roll_launch<T, false, 4, true, true>(go, idx, gi, g, rg, smem, s);
+    if (!roll_plan(g, sizeof(T), 1LL * sms * kRollCfg.minb, kRollCfg, &rg, &smem, &wpt))
+        return cudaErrorNotSupported;
     if (g.adaptive) {
         if (wpt == 1) return roll_launch<T, true, 1>(go, idx, gi, g, rg, smem, s);
         if (wpt == 2) return roll_launch<T, true, 2>(go, idx, gi, g, rg, smem, s);
         return roll_launch<T, true, 4>(go, idx, gi, g, rg, smem, s);
     }
-    constexpr int VEC = 16 / sizeof(T);
-    const bool k3 = g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 && g.sw == 2;
-    if (k3 && wpt == 4 && g.W % VEC == 0 && g.vol % VEC == 0)
-        return roll_launch<T, false, 4, true, true>(go, idx, gi, g, rg, smem, s);
     if (wpt == 1) return roll_launch<T, false, 1>(go, idx, gi, g, rg, smem, s);
     if (wpt == 2) return roll_launch<T, false, 2>(go, idx, gi, g, rg, smem, s);
     return roll_launch<T, false, 4>(go, idx, gi, g, rg, smem, s);
@@ -502,7 +509,7 @@ bool bwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
     RollGeo rg;
     size_t smem = 0;
     int wpt = 0;
-    return aligned16 && roll_plan(g, elem_bytes(dtype), 0, &rg, &smem, &wpt);
+    return aligned16 && roll_plan(g, elem_bytes(dtype), 0, kRollCfg, &rg, &smem, &wpt);
 }
 
 cudaError_t launch_bwd_roll(const void* go, const int64_t* idx, void* gi, const Geo& g, int dtype,
