@@ -725,7 +725,7 @@ bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
 template <typename T, int KD, int SD, int KH, int SH, int KW>
 static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                             cudaStream_t s) {
-    constexpr int TOH = 4, NS = 3;
+    constexpr int TOH = 4, NS = 2;
     const int nc = g.W / 8;
     const int nt = (g.OH + TOH - 1) / TOH;
     // Band of G tiles: at most 256 threads and 16 KB of input rows per stage.
