@@ -176,6 +176,13 @@ class Runner:
             nb = 1
         return nf, nb
 
+    def fwd_values(self):
+        """Values-only forward (no index buffer)."""
+        if self.w.mode == "fixed":
+            self.mp.maxpool3d_fwd(self.x, self.y, None, self.w.kernel, self.w.stride)
+        else:
+            self.mp.adaptive_maxpool3d_fwd(self.x, self.y, None, self.w.out)
+
     def fwd(self, x=None, y=None, idx=None):
         x = self.x if x is None else x
         y = self.y if y is None else y
@@ -217,6 +224,26 @@ def time_per_kernel(r, iters, warmup, flush):
             b.synchronize()
             out.append(a.elapsed_time(b))
     return statistics.median(tf), statistics.median(tb)
+
+
+def time_one(fn, dev, iters, flush):
+    """Median device time (ms) of fn, each launch preceded by an L2 flush."""
+    stream = torch.cuda.current_stream()
+    fb = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(iters):
+        if fb is not None:
+            l2_flush(fb)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
 
 
 def kernel_hash():
@@ -414,6 +441,10 @@ def per_config(dev, peak):
         fb, bb = algorithmic_bytes(w)
         pf, pb = r.paths()
         fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
+        # values-only forward: the same minus the int64 index writes
+        tv = time_one(r.fwd_values, dev, iters=20, flush=True)
+        vb = fb - w.planes * w.out[0] * w.out[1] * w.out[2] * 8
+        vg = vb / (tv * 1e-3) / 1e9
         out[w.name] = {
             "fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2),
             "fwd_bytes": fb, "bwd_bytes": bb,
@@ -421,7 +452,9 @@ def per_config(dev, peak):
             "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
             "fwd_frac_of_nominal_8000": round(fg / NOMINAL_HBM_GBS, 4),
             "bwd_frac_of_nominal_8000": round(bg / NOMINAL_HBM_GBS, 4),
-            "fwd_path": pf, "bwd_path": pb}
+            "fwd_path": pf, "bwd_path": pb,
+            "fwd_values_only_us": round(tv * 1e3, 2), "fwd_values_only_bytes": vb,
+            "fwd_values_only_gbs": round(vg, 1), "fwd_values_only_frac": round(vg / peak, 4)}
         del r
         torch.cuda.empty_cache()
     return out

@@ -93,6 +93,11 @@ def _cuda(*ts):
             raise ValueError("tensors must be contiguous (NCDHW)")
 
 
+def _ptr(t) -> int:
+    """Device address of a tensor, or 0 (NULL) for None."""
+    return 0 if t is None else t.data_ptr()
+
+
 def _stream(t: torch.Tensor, stream):
     if stream is None:
         return torch.cuda.current_stream(t.device).cuda_stream
@@ -112,21 +117,23 @@ def pool_out_size(size, kernel, stride):
 
 
 def maxpool3d_fwd(x, y, idx, kernel, stride, stream=None):
-    """Fixed-window forward into caller-allocated y (x's dtype) and idx (int64)."""
+    """Fixed-window forward into caller-allocated y (x's dtype) and idx
+    (int64); idx None: values only (no index is stored)."""
     _cuda(x, y, idx)
     N, C, D, H, W = x.shape
     with torch.cuda.device(x.device):
-        st = lib().maxpool3d_fwd(x.data_ptr(), y.data_ptr(), idx.data_ptr(), N, C, D, H, W,
+        st = lib().maxpool3d_fwd(x.data_ptr(), y.data_ptr(), _ptr(idx), N, C, D, H, W,
                                  *kernel, *stride, _code(x), _stream(x, stream))
     _check(st, "maxpool3d_fwd")
 
 
 def adaptive_maxpool3d_fwd(x, y, idx, out_size, stream=None):
-    """Adaptive-window forward into caller-allocated y and idx."""
+    """Adaptive-window forward into caller-allocated y and idx; idx None:
+    values only."""
     _cuda(x, y, idx)
     N, C, D, H, W = x.shape
     with torch.cuda.device(x.device):
-        st = lib().adaptive_maxpool3d_fwd(x.data_ptr(), y.data_ptr(), idx.data_ptr(), N, C, D, H,
+        st = lib().adaptive_maxpool3d_fwd(x.data_ptr(), y.data_ptr(), _ptr(idx), N, C, D, H,
                                           W, *out_size, _code(x), _stream(x, stream))
     _check(st, "adaptive_maxpool3d_fwd")
 

@@ -187,9 +187,9 @@ int check_fwd_buffers(const void* x, const void* y, const int64_t* idx, const Ge
     const int es = elem_size(dtype);
     if (es == 0) return MP3D_ERR_DTYPE;
     if (g.P == 0) return MP3D_OK;
-    if (!x || !y || !idx) return MP3D_ERR_NULLPTR;
-    if (misaligned(x, es) || misaligned(y, es) || misaligned(idx, 8)) return MP3D_ERR_ALIGN;
-    const long long nx = g.P * g.vol * es, ny = g.P * g.ovol * es, ni = g.P * g.ovol * 8;
+    if (!x || !y) return MP3D_ERR_NULLPTR;                 // idx NULL: values only
+    if (misaligned(x, es) || misaligned(y, es) || (idx && misaligned(idx, 8))) return MP3D_ERR_ALIGN;
+    const long long nx = g.P * g.vol * es, ny = g.P * g.ovol * es, ni = idx ? g.P * g.ovol * 8 : 0;
     if (overlaps(x, nx, y, ny) || overlaps(x, nx, idx, ni) || overlaps(y, ny, idx, ni))
         return MP3D_ERR_ALIAS;
     return MP3D_OK;

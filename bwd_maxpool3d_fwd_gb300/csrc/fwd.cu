@@ -49,7 +49,7 @@ k_fwd_generic(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ 
                 }
             }
         y[o] = xp[best];
-        idx[o] = best;
+        if (idx) idx[o] = best;
     }
 }
 
@@ -111,7 +111,7 @@ k_fwd_global(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ i
         }
         if (lane == 0) {
             y[p] = xp[best];
-            idx[p] = best;
+            if (idx) idx[p] = best;
         }
     }
 }
@@ -168,7 +168,7 @@ k_fwd_slab(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                     }
                 }
             y[obase + t] = sl[best];
-            idx[obase + t] = (int64_t)ds * HW + best;
+            if (idx) idx[obase + t] = (int64_t)ds * HW + best;
         }
         __syncthreads();
     }
@@ -494,10 +494,14 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
         __syncthreads();
         const long long obase = ((p * g.OD + od) * g.OH + oh_band) * (long long)g.OW;
         uint16_t* yd = reinterpret_cast<uint16_t*>(y) + obase;
-        int64_t* id = idx + obase;
-        for (int k = tid; k < nout; k += blockDim.x) {
-            yd[k] = ys[k];
-            id[k] = is[k];
+        if (idx) {
+            int64_t* id = idx + obase;
+            for (int k = tid; k < nout; k += blockDim.x) {
+                yd[k] = ys[k];
+                id[k] = is[k];
+            }
+        } else {
+            for (int k = tid; k < nout; k += blockDim.x) yd[k] = ys[k];
         }
         __syncthreads();
     };
@@ -703,9 +707,11 @@ k_fwd_k2s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 }
             }
             *reinterpret_cast<uint2*>(y + o0) = yv;
-            int4* id = reinterpret_cast<int4*>(idx + o0);
-            id[0] = make_int4((int)iv[0], (int)(iv[0] >> 32), (int)iv[1], (int)(iv[1] >> 32));
-            id[1] = make_int4((int)iv[2], (int)(iv[2] >> 32), (int)iv[3], (int)(iv[3] >> 32));
+            if (idx) {
+                int4* id = reinterpret_cast<int4*>(idx + o0);
+                id[0] = make_int4((int)iv[0], (int)(iv[0] >> 32), (int)iv[1], (int)(iv[1] >> 32));
+                id[1] = make_int4((int)iv[2], (int)(iv[2] >> 32), (int)iv[3], (int)(iv[3] >> 32));
+            }
         }
     }
 }

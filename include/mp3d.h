@@ -98,7 +98,10 @@ typedef enum {
  * (no padding). y[n,c,od,oh,ow] is the maximum of x over
  * d in [od*sd, od*sd + kd), h in [oh*sh, oh*sh + kh), w in [ow*sw, ow*sw + kw).
  * Requires 1 <= k <= input size and s >= 1 on every axis.
- * idx may be NULL only together with N*C == 0.
+ * idx may be NULL: the values-only forward ([MPF]'s launch tuple has an
+ * input and an output pointer and no index output). y is written exactly as
+ * with an index buffer and no index is stored, which saves the 8-byte
+ * index of every output (a backward then needs an index from another call).
  */
 int maxpool3d_fwd(const void* x, void* y, int64_t* idx,
                   int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
@@ -109,7 +112,8 @@ int maxpool3d_fwd(const void* x, void* y, int64_t* idx,
  * Adaptive-window forward (the forward of [AMPB]'s operator). Output size
  * (od, oh, ow) is given, each >= 1 (an output larger than the input is
  * accepted). Window i along an axis of input size I and output size O is
- * [floor(i*I/O), ceil((i+1)*I/O)). Buffers as for maxpool3d_fwd.
+ * [floor(i*I/O), ceil((i+1)*I/O)). Buffers as for maxpool3d_fwd (idx may
+ * be NULL: values only).
  */
 int adaptive_maxpool3d_fwd(const void* x, void* y, int64_t* idx,
                            int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,

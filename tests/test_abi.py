@@ -59,7 +59,12 @@ def test_fwd_argument_errors(L, bufs):
     x, y, i, _ = bufs
     assert fwd(L, None, y, i) == NULLPTR
     assert fwd(L, x, None, i) == NULLPTR
-    assert fwd(L, x, y, None) == NULLPTR
+    # idx NULL asks for the values-only forward: the other checks still apply
+    # (each case below fails before any CUDA call)
+    assert fwd(L, x, y, None, dt=3) == DTYPE
+    assert fwd(L, x + 1, y, None, dt=1) == ALIGN
+    assert fwd(L, x, x + 64, None) == ALIAS
+    assert fwd(L, x, None, None) == NULLPTR
     assert fwd(L, x, y, i, D=0) == SHAPE
     assert fwd(L, x, y, i, N=-1) == SHAPE
     assert fwd(L, x, y, i, k=(0, 2, 2)) == WINDOW

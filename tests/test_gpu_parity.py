@@ -443,3 +443,35 @@ def test_overlap_roll_signed_zero_gradients_wide_rows(dtype, grad):
     ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
     assert bool((bits(ref) == bits(torch.tensor(-0.0).to(dtype))).any())
     assert_bits_equal(gpu_bwd(g, i_ref, shape, k, s), ref, "grad_in")
+
+
+# Values-only forward (idx NULL): y is the same, bit for bit, on every
+# forward path; no index buffer is touched.
+VALUES_ONLY = [
+    ("fwd_s2", (3, 3, 3), (2, 2, 2), None, (1, 2, 9, 20, 48), torch.float16),
+    ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 8, 6, 32), torch.bfloat16),    # 2x2x2 tiling
+    ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 9, 7, 32), torch.float16),
+    ("fwd_slab", None, None, (5, 4, 8), (2, 2, 9, 7, 13), torch.float32),
+    ("fwd_generic", (5, 5, 5), (3, 3, 3), None, (1, 1, 8, 120, 120), torch.float32),
+    ("fwd_global", None, None, (1, 1, 1), (1, 3, 8, 14, 14), torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(VALUES_ONLY)))
+def test_values_only_forward(case):
+    path, k, s, out, shape, dtype = VALUES_ONLY[case]
+    gen = torch.Generator().manual_seed(9000 + case)
+    x = random_input(gen, shape, dtype, "special")
+    if k is not None:
+        assert mp.maxpool3d_fwd_plan(shape, k, s, dtype) == path
+        y_ref, _ = oracle.maxpool3d_fwd(x, k, s)
+    else:
+        assert mp.adaptive_maxpool3d_fwd_plan(shape, out, dtype) == path
+        y_ref, _ = oracle.adaptive_maxpool3d_fwd(x, out)
+    y = torch.empty(y_ref.shape, dtype=dtype, device=DEV)
+    if k is not None:
+        mp.maxpool3d_fwd(x.to(DEV), y, None, k, s)
+    else:
+        mp.adaptive_maxpool3d_fwd(x.to(DEV), y, None, out)
+    torch.cuda.synchronize()
+    assert_bits_equal(y.cpu(), y_ref, "y (values only)")
