@@ -61,6 +61,8 @@ class Oracle:
             "oracle_maxpool3d_fwd": ([i32, vp, vp, vp] + [i64] * 10, i32),
             "oracle_adaptive_maxpool3d_fwd": ([i32, vp, vp, vp] + [i64] * 7, i32),
             "oracle_maxpool3d_bwd": ([i32, vp, vp, vp, i64, i64, i64], i32),
+            "oracle_ex_out_size": ([i64] * 5 + [i32], i64),
+            "oracle_maxpool3d_fwd_ex": ([i32, vp, vp, vp] + [i64] * 16 + [i32], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -126,6 +128,27 @@ class Oracle:
                                                   idx.data_ptr(), N * C, D, H, W, OD, OH, OW)
         if rc:
             raise RuntimeError(f"oracle_adaptive_maxpool3d_fwd failed ({rc})")
+        return y, idx
+
+    def ex_out_size(self, I: int, K: int, S: int, p: int, dl: int, ceil_mode: bool) -> int:
+        """Output length with padding, dilation and ceil mode (0 = invalid)."""
+        return self.L.oracle_ex_out_size(I, K, S, p, dl, 1 if ceil_mode else 0)
+
+    def maxpool3d_fwd_ex(self, x: torch.Tensor, kernel, stride, padding, dilation, ceil_mode=False):
+        """Forward with padding, dilation and ceil mode. Returns (y, idx)."""
+        _check_cpu(x)
+        N, C, D, H, W = x.shape
+        out = tuple(self.ex_out_size(I, K, S, p, dl, ceil_mode)
+                    for I, K, S, p, dl in zip((D, H, W), kernel, stride, padding, dilation))
+        if min(out) < 1:
+            raise ValueError("oracle: invalid window geometry")
+        y = torch.empty((N, C) + out, dtype=x.dtype)
+        idx = torch.empty((N, C) + out, dtype=torch.int64)
+        rc = self.L.oracle_maxpool3d_fwd_ex(_code(x), x.data_ptr(), y.data_ptr(), idx.data_ptr(),
+                                            N * C, D, H, W, *kernel, *stride, *padding, *dilation,
+                                            1 if ceil_mode else 0)
+        if rc:
+            raise RuntimeError(f"oracle_maxpool3d_fwd_ex failed ({rc})")
         return y, idx
 
     def maxpool3d_bwd(self, grad_out: torch.Tensor, idx: torch.Tensor, in_spatial):

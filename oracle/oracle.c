@@ -343,6 +343,97 @@ int oracle_adaptive_maxpool3d_fwd(int dtype, const void* x, void* y, int64_t* id
 }
 
 /* ------------------------------------------------------------------ */
+/* Padding, dilation and ceil-mode output sizes: the fixed-window forward */
+/* beyond [MPF]'s "no padding" constraint (the usual max_pool3d surface). */
+/* ------------------------------------------------------------------ */
+
+/* Output length along one axis with padding p on both sides, dilation dl
+ * and ceil mode, following the usual max_pool3d definition (the pages fix
+ * only the unpadded case). The window of output o takes the positions
+ * o*S - p + k*dl, k = 0 .. K-1, that lie inside [0, I); its span is
+ * e = dl*(K-1) + 1. O = floor((I + 2p - e) / S) + 1, or
+ * floor((I + 2p - e + S - 1) / S) + 1 in ceil mode, where a last window starting
+ * at or past I + p (wholly in the right padding) is dropped. Returns 0 for
+ * invalid arguments: K, S or dl < 1, p < 0, p more than half the kernel
+ * size (2p > K), or no output. */
+int64_t oracle_ex_out_size(int64_t I, int64_t K, int64_t S, int64_t p, int64_t dl, int ceil_mode)
+{
+    int64_t e, num, O;
+    if (I < 1 || K < 1 || S < 1 || dl < 1 || p < 0)
+        return 0;
+    if (2 * p > K)
+        return 0;
+    e = dl * (K - 1) + 1;
+    num = I + 2 * p - e;
+    if (ceil_mode)
+        num += S - 1;
+    O = (num >= 0 ? num / S : -((-num + S - 1) / S)) + 1;   /* floor division */
+    if (ceil_mode && (O - 1) * S >= I + p)
+        O--;
+    return O < 1 ? 0 : O;
+}
+
+/* Forward with padding and dilation: y[p,od,oh,ow] = max over the window
+ * positions (d, h, w) = (od*sd - pd + a*dd, oh*sh - ph + b*dh,
+ * ow*sw - pw + c*dw), a < kd, b < kh, c < kw, that lie inside the input,
+ * scanned in ascending a, b, c (so ascending d, h, w; padding is never
+ * chosen). A window with no position inside the input makes the geometry
+ * invalid (OR_ERR_SHAPE). */
+int oracle_maxpool3d_fwd_ex(int dtype, const void* x, void* y, int64_t* idx,
+                            int64_t P, int64_t D, int64_t H, int64_t W,
+                            int64_t kd, int64_t kh, int64_t kw,
+                            int64_t sd, int64_t sh, int64_t sw,
+                            int64_t pd, int64_t ph, int64_t pw,
+                            int64_t dd, int64_t dh, int64_t dw, int ceil_mode)
+{
+    int64_t OD = oracle_ex_out_size(D, kd, sd, pd, dd, ceil_mode);
+    int64_t OH = oracle_ex_out_size(H, kh, sh, ph, dh, ceil_mode);
+    int64_t OW = oracle_ex_out_size(W, kw, sw, pw, dw, ceil_mode);
+    int64_t vol = D * H * W, p, od, oh, ow, o = 0;
+    int es = elem_size(dtype);
+    if (es == 0)
+        return OR_ERR_DTYPE;
+    if (P < 0 || OD < 1 || OH < 1 || OW < 1)
+        return OR_ERR_SHAPE;
+    for (p = 0; p < P; p++)
+        for (od = 0; od < OD; od++)
+            for (oh = 0; oh < OH; oh++)
+                for (ow = 0; ow < OW; ow++) {
+                    int64_t best = -1, a, b, c;
+                    double m = 0.0;
+                    for (a = 0; a < kd; a++) {
+                        int64_t d = od * sd - pd + a * dd;
+                        if (d < 0 || d >= D)
+                            continue;
+                        for (b = 0; b < kh; b++) {
+                            int64_t h = oh * sh - ph + b * dh;
+                            if (h < 0 || h >= H)
+                                continue;
+                            for (c = 0; c < kw; c++) {
+                                int64_t w = ow * sw - pw + c * dw;
+                                int64_t off;
+                                double v;
+                                if (w < 0 || w >= W)
+                                    continue;
+                                off = (d * H + h) * W + w;
+                                v = load_value(dtype, x, p * vol + off);
+                                if (best < 0 || beats(v, m)) {
+                                    m = v;
+                                    best = off;
+                                }
+                            }
+                        }
+                    }
+                    if (best < 0)
+                        return OR_ERR_SHAPE;
+                    memcpy((char*)y + o * es, (const char*)x + es * (p * vol + best), (size_t)es);
+                    idx[o] = best;
+                    o++;
+                }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* Backward ([AMPB] Summary)                                            */
 /* ------------------------------------------------------------------ */
 

@@ -372,11 +372,102 @@ def check_bwd_against_exact_sum(orc):
                     assert abs(gi[p, j] - exact) <= tol, (p, j, gi[p, j], exact, tol)
 
 
+# ----------------------------------------------------- padding and dilation
+# The forward with padding, dilation and ceil mode against torch's CPU
+# max_pool1d / max_pool3d (a library routine whose tie rule, for values
+# that are not NaN, is the same: a later element replaces only when it is
+# strictly greater).
+
+def _torch_len(I, K, S, p, dl, ceil_mode):
+    """torch's output length, or 0 when torch rejects the arguments."""
+    try:
+        return torch.nn.functional.max_pool1d(torch.zeros(1, 1, I), K, S, p, dl, ceil_mode).shape[-1]
+    except RuntimeError:
+        return 0
+
+
+def check_ex_out_size_vs_torch(orc):
+    for I, K, S, p, dl, cm in itertools.product(range(1, 11), range(1, 5), range(1, 4), range(0, 3),
+                                                 range(1, 4), (False, True)):
+        got = orc.ex_out_size(I, K, S, p, dl, cm)
+        want = _torch_len(I, K, S, p, dl, cm)
+        assert got == max(want, 0), (I, K, S, p, dl, cm, got, want)
+
+
+def _ex_cases(rng, n):
+    out = []
+    while len(out) < n:
+        k = [int(v) for v in rng.integers(1, 4, 3)]
+        s = [int(v) for v in rng.integers(1, 4, 3)]
+        dl = [int(v) for v in rng.integers(1, 3, 3)]
+        p = [int(rng.integers(0, kk // 2 + 1)) for kk in k]
+        shape = (1, 2) + tuple(int(v) for v in rng.integers(1, 9, 3))
+        cm = bool(rng.integers(0, 2))
+        out.append((shape, tuple(k), tuple(s), tuple(p), tuple(dl), cm))
+    return out
+
+
+def check_fwd_ex_vs_torch(orc, cases=120, seed=11):
+    rng = np.random.default_rng(seed)
+    checked = 0
+    for shape, k, s, p, dl, cm in _ex_cases(rng, cases):
+        n = int(np.prod(shape))
+        for kind in ("distinct", "ties"):
+            if kind == "distinct":
+                x = torch.from_numpy(rng.permutation(n).astype(np.float32)).reshape(shape) / n - 0.5
+            else:
+                x = torch.from_numpy(rng.integers(-2, 3, n).astype(np.float32)).reshape(shape)
+            try:
+                yt, it = torch.nn.functional.max_pool3d(x, k, s, p, dl, cm, True)
+            except RuntimeError:
+                assert min(orc.ex_out_size(I, kk, ss, pp, dd, cm)
+                           for I, kk, ss, pp, dd in zip(shape[2:], k, s, p, dl)) == 0
+                continue
+            try:
+                y, i = orc.maxpool3d_fwd_ex(x, k, s, p, dl, cm)
+            except (RuntimeError, ValueError):
+                # a window with no position inside the input: torch leaves -inf there
+                assert bool(torch.isinf(yt).any()), (shape, k, s, p, dl, cm)
+                continue
+            assert torch.equal(i, it), (shape, k, s, p, dl, cm, kind)
+            assert np.array_equal(bits(y), bits(yt)), (shape, k, s, p, dl, cm, kind)
+            checked += 1
+    assert checked >= cases
+
+
+def check_fwd_ex_16bit_vs_torch(orc, cases=40, seed=12):
+    rng = np.random.default_rng(seed)
+    for shape, k, s, p, dl, cm in _ex_cases(rng, cases):
+        for dtype in (torch.float16, torch.bfloat16):
+            n = int(np.prod(shape))
+            x = torch.from_numpy(rng.integers(-3, 4, n).astype(np.float32)).reshape(shape).to(dtype)
+            try:
+                yt, it = torch.nn.functional.max_pool3d(x, k, s, p, dl, cm, True)
+                y, i = orc.maxpool3d_fwd_ex(x, k, s, p, dl, cm)
+            except (RuntimeError, ValueError):
+                continue
+            assert torch.equal(i, it), (shape, k, s, p, dl, cm, dtype)
+            assert np.array_equal(bits(y), bits(yt)), (shape, k, s, p, dl, cm, dtype)
+
+
+def check_fwd_ex_reduces_to_plain(orc, seed=13):
+    rng = np.random.default_rng(seed)
+    for _ in range(30):
+        k = tuple(int(v) for v in rng.integers(1, 4, 3))
+        s = tuple(int(v) for v in rng.integers(1, 4, 3))
+        shape = (2, 2) + tuple(int(kk + rng.integers(0, 6)) for kk in k)
+        x = torch.from_numpy(rng.standard_normal(int(np.prod(shape))).astype(np.float32)).reshape(shape)
+        y0, i0 = orc.maxpool3d_fwd(x, k, s)
+        y1, i1 = orc.maxpool3d_fwd_ex(x, k, s, (0, 0, 0), (1, 1, 1), False)
+        assert torch.equal(i0, i1) and np.array_equal(bits(y0), bits(y1))
+
+
 ALL_CHECKS = [
     check_f16_decode, check_f16_encode, check_bf16_decode, check_bf16_encode,
     check_output_sizes_golden, check_fixed_size_by_counting, check_adaptive_windows,
     check_fixed_windows, check_fwd_bruteforce_fixed, check_fwd_bruteforce_adaptive,
     check_fwd_hand_examples, check_fwd_identity, check_fixed_equals_divisible_adaptive,
     check_bwd_hand_examples, check_bwd_disjoint_bijection, check_bwd_integer_sum_conserved,
-    check_bwd_against_exact_sum,
+    check_bwd_against_exact_sum, check_ex_out_size_vs_torch, check_fwd_ex_vs_torch,
+    check_fwd_ex_16bit_vs_torch, check_fwd_ex_reduces_to_plain,
 ]

@@ -34,6 +34,14 @@ MUTANTS = {
     "f16_exponent_bias": ("((e - 15 + 127) << 23)", "((e - 14 + 127) << 23)"),
     "bf16_subnormal_limit": ("r = round_to_format(fabs((double)f), 7, -126);",
                              "r = round_to_format(fabs((double)f), 7, -125);"),
+    # padding, dilation and ceil mode
+    "ex_no_ceil_drop": ("if (ceil_mode && (O - 1) * S >= I + p)", "if (0)"),
+    "ex_truncating_division": ("O = (num >= 0 ? num / S : -((-num + S - 1) / S)) + 1;",
+                               "O = num / S + 1;"),
+    "ex_padding_limit_loose": ("if (2 * p > K)", "if (2 * p > K + 1)"),
+    "ex_padding_added": ("int64_t d = od * sd - pd + a * dd;", "int64_t d = od * sd + pd + a * dd;"),
+    "ex_dilation_ignored_w": ("int64_t w = ow * sw - pw + c * dw;", "int64_t w = ow * sw - pw + c;"),
+    "ex_y_from_wrong_element": ("es * (p * vol + best)", "es * (p * vol + best - (best > 0))"),
 }
 
 
