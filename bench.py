@@ -460,6 +460,42 @@ def per_config(dev, peak):
     return out
 
 
+# Padded windows (the padding / dilation / ceil-mode entry points): 3x3x3,
+# stride 2, padding 1, fp16, N=8, C=64, 16x56x56 -> 8x28x28. Seeded synthetic
+# inputs: x ~ N(0,1) and grad_out ~ N(0,1), drawn in binary32 then rounded.
+PADDED = {"name": "padded_k3s2p1_f16_8x64x16x56x56", "shape": (8, 64, 16, 56, 56),
+          "k": (3, 3, 3), "s": (2, 2, 2), "p": (1, 1, 1), "dl": (1, 1, 1), "seed": 20261302}
+
+
+def padded_config(dev, peak):
+    """The padded workload's forward and backward timed alone (median of 20,
+    L2 flushed before every launch)."""
+    import bwd_maxpool3d_fwd_gb300 as mp
+    c = PADDED
+    gen = torch.Generator().manual_seed(c["seed"])
+    x = torch.randn(c["shape"], generator=gen).half().to(dev)
+    out = mp.pool_out_size_ex(c["shape"][2:], c["k"], c["s"], c["p"], c["dl"])
+    oshape = c["shape"][:2] + out
+    g = torch.randn(oshape, generator=gen).half().to(dev)
+    y = torch.empty(oshape, dtype=torch.float16, device=dev)
+    idx = torch.empty(oshape, dtype=torch.int64, device=dev)
+    gin = torch.empty(c["shape"], dtype=torch.float16, device=dev)
+    fwd = lambda: mp.maxpool3d_fwd_ex(x, y, idx, c["k"], c["s"], c["p"], c["dl"])
+    bwd = lambda: mp.maxpool3d_bwd_ex(g, idx, gin, c["k"], c["s"], c["p"], c["dl"])
+    tf = time_one(fwd, dev, iters=20, flush=True)
+    tb = time_one(bwd, dev, iters=20, flush=True)
+    nin, nout = x.numel(), y.numel()
+    fb, bb = nin * 2 + nout * (2 + 8), nout * (2 + 8) + nin * 2
+    fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
+    return {"fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2), "fwd_bytes": fb,
+            "bwd_bytes": bb, "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
+            "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
+            "fwd_path": mp.maxpool3d_fwd_ex_plan(c["shape"], c["k"], c["s"], c["p"], c["dl"], False,
+                                                 torch.float16),
+            "bwd_path": mp.maxpool3d_bwd_ex_plan(c["shape"], out, c["k"], c["s"], c["p"], c["dl"],
+                                                 False, torch.float16)}
+
+
 def our_arm(args):
     rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
@@ -525,6 +561,8 @@ def our_arm(args):
     del r
     torch.cuda.empty_cache()
     cfg = per_config(dev, peak) if (rank == 0 and not args.no_per_config) else None
+    if cfg is not None:
+        cfg[PADDED["name"]] = padded_config(dev, peak)
     cpu = cpu_baseline(base) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
         return None

@@ -22,8 +22,10 @@ F32, F16, BF16 = 0, 1, 2
 BWD_AUTO, BWD_GATHER, BWD_ATOMIC = 0, 1, 2
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
-PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 10: "bwd_disjoint",
-         11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll"}
+PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 5: "fwd_padded",
+         10: "bwd_disjoint",
+         11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll",
+         15: "bwd_padded"}
 
 _lib = None
 
@@ -54,10 +56,15 @@ def lib() -> ctypes.CDLL:
     L.maxpool3d_fwd_plan.argtypes = [i64] * 5 + [i32] * 7 + [pi32]
     L.adaptive_maxpool3d_fwd_plan.argtypes = [i64] * 5 + [i32] * 4 + [pi32]
     L.maxpool3d_bwd_plan.argtypes = [i64] * 5 + [i32] * 11 + [pi32]
+    L.maxpool3d_fwd_ex.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 14 + [vp]
+    L.maxpool3d_bwd_ex.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 18 + [vp, sz, vp]
+    L.maxpool3d_fwd_ex_plan.argtypes = [i64] * 5 + [i32] * 14 + [pi32]
+    L.maxpool3d_bwd_ex_plan.argtypes = [i64] * 5 + [i32] * 18 + [pi32]
     L.mp3d_status_string.argtypes = [i32]
     L.mp3d_status_string.restype = ctypes.c_char_p
     for f in (L.maxpool3d_fwd, L.adaptive_maxpool3d_fwd, L.maxpool3d_bwd, L.maxpool3d_fwd_plan,
-              L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan):
+              L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan, L.maxpool3d_fwd_ex,
+              L.maxpool3d_bwd_ex, L.maxpool3d_fwd_ex_plan, L.maxpool3d_bwd_ex_plan):
         f.restype = i32
     _lib = L
     return L
@@ -114,6 +121,68 @@ def _check(status: int, where: str):
 def pool_out_size(size, kernel, stride):
     """Output extent per axis for fixed windows without padding: (I - K) // S + 1."""
     return tuple((i - k) // s + 1 for i, k, s in zip(size, kernel, stride))
+
+
+def pool_out_size_ex(size, kernel, stride, padding=(0, 0, 0), dilation=(1, 1, 1), ceil_mode=False):
+    """Output extent per axis with padding, dilation and ceil mode (the rule
+    documented for maxpool3d_fwd_ex); 0 where the arguments are invalid."""
+    out = []
+    for i, k, s, p, dl in zip(size, kernel, stride, padding, dilation):
+        if i < 1 or k < 1 or s < 1 or dl < 1 or p < 0 or 2 * p > k:
+            out.append(0)
+            continue
+        num = i + 2 * p - dl * (k - 1) - 1 + (s - 1 if ceil_mode else 0)
+        o = num // s + 1
+        if ceil_mode and (o - 1) * s >= i + p:
+            o -= 1
+        out.append(max(o, 0))
+    return tuple(out)
+
+
+def maxpool3d_fwd_ex(x, y, idx, kernel, stride, padding=(0, 0, 0), dilation=(1, 1, 1),
+                     ceil_mode=False, stream=None):
+    """Fixed-window forward with padding, dilation and ceil mode; idx None:
+    values only."""
+    _cuda(x, y, idx)
+    N, C, D, H, W = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().maxpool3d_fwd_ex(x.data_ptr(), y.data_ptr(), _ptr(idx), N, C, D, H, W, *kernel,
+                                    *stride, *padding, *dilation, int(bool(ceil_mode)), _code(x),
+                                    _stream(x, stream))
+    _check(st, "maxpool3d_fwd_ex")
+
+
+def maxpool3d_bwd_ex(grad_out, idx, grad_in, kernel, stride, padding=(0, 0, 0), dilation=(1, 1, 1),
+                     ceil_mode=False, algo=BWD_AUTO, workspace=None, stream=None):
+    """Backward of maxpool3d_fwd_ex into caller-allocated grad_in."""
+    _cuda(grad_out, idx, grad_in, workspace)
+    N, C, D, H, W = grad_in.shape
+    od, oh, ow = grad_out.shape[2:]
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(grad_in.device):
+        st = lib().maxpool3d_bwd_ex(grad_out.data_ptr(), idx.data_ptr(), grad_in.data_ptr(), N, C, D,
+                                    H, W, od, oh, ow, *kernel, *stride, *padding, *dilation,
+                                    int(bool(ceil_mode)), _code(grad_out), algo, ws, wsb,
+                                    _stream(grad_in, stream))
+    _check(st, "maxpool3d_bwd_ex")
+
+
+def maxpool3d_fwd_ex_plan(in_shape, kernel, stride, padding, dilation, ceil_mode, dtype) -> str:
+    p = ctypes.c_int(-1)
+    _check(lib().maxpool3d_fwd_ex_plan(*in_shape, *kernel, *stride, *padding, *dilation,
+                                       int(bool(ceil_mode)), DTYPE_CODE[dtype], ctypes.byref(p)),
+           "maxpool3d_fwd_ex_plan")
+    return PATHS[p.value]
+
+
+def maxpool3d_bwd_ex_plan(in_shape, out_size, kernel, stride, padding, dilation, ceil_mode, dtype,
+                          algo=BWD_AUTO) -> str:
+    p = ctypes.c_int(-1)
+    _check(lib().maxpool3d_bwd_ex_plan(*in_shape, *out_size, *kernel, *stride, *padding, *dilation,
+                                       int(bool(ceil_mode)), DTYPE_CODE[dtype], algo, ctypes.byref(p)),
+           "maxpool3d_bwd_ex_plan")
+    return PATHS[p.value]
 
 
 def maxpool3d_fwd(x, y, idx, kernel, stride, stream=None):

@@ -46,6 +46,8 @@ const char* path_name(int path) {
     case MP3D_PATH_BWD_OVERLAP_DIRECT: return "bwd_overlap_direct";
     case MP3D_PATH_BWD_ATOMIC: return "bwd_atomic";
     case MP3D_PATH_BWD_OVERLAP_ROLL: return "bwd_overlap_roll";
+    case MP3D_PATH_FWD_PADDED: return "fwd_padded";
+    case MP3D_PATH_BWD_PADDED: return "bwd_padded";
     default: return "?";
     }
 }
@@ -85,6 +87,7 @@ int check_dims(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, Geo* g) {
     const long long P = N * C;
     if (P > 0 && P > (1LL << 62) / vol) return MP3D_ERR_SHAPE;
     std::memset(g, 0, sizeof(*g));
+    g->dd = g->dh = g->dw = 1;
     g->P = P;
     g->D = (int)D; g->H = (int)H; g->W = (int)W;
     g->vol = (int)vol;
@@ -113,6 +116,65 @@ int fixed_geo(Geo* g, int kd, int kh, int kw, int sd, int sh, int sw) {
 int adaptive_geo(Geo* g, int od, int oh, int ow) {
     g->adaptive = 1;
     return set_out(g, od, oh, ow);
+}
+
+// Output length along one axis with padding p (both sides), dilation dl
+// and ceil mode, as the usual max_pool3d defines it: padding at most half
+// the kernel, floor (ceil) of (I + 2p - dl*(K-1) - 1)/S plus 1, and in ceil
+// mode a last window wholly in the right padding dropped. 0 when invalid.
+long long ex_out_len(long long I, long long K, long long S, long long p, long long dl, int ceil_mode) {
+    if (I < 1 || K < 1 || S < 1 || dl < 1 || p < 0 || 2 * p > K) return 0;
+    long long num = I + 2 * p - dl * (K - 1) - 1;
+    if (ceil_mode) num += S - 1;
+    long long O = (num >= 0 ? num / S : -((-num + S - 1) / S)) + 1;   // floor division
+    if (ceil_mode && (O - 1) * S >= I + p) --O;
+    return O < 1 ? 0 : O;
+}
+
+// Every window o < O along the axis has a position o*S - p + k*dl inside
+// [0, I). Always true without dilation (padding is at most half the kernel
+// and the last window starts before I); checked window by window otherwise.
+bool ex_windows_nonempty(long long I, long long O, long long K, long long S, long long p,
+                         long long dl) {
+    if (dl == 1) return true;
+    for (long long o = 0; o < O; ++o) {
+        bool any = false;
+        for (long long k = 0; k < K && !any; ++k) {
+            const long long x = o * S - p + k * dl;
+            any = x >= 0 && x < I;
+        }
+        if (!any) return false;
+    }
+    return true;
+}
+
+// Fixed windows with padding, dilation and ceil mode.
+int ex_geo(Geo* g, int kd, int kh, int kw, int sd, int sh, int sw, int pd, int ph, int pw, int dd,
+           int dh, int dw, int ceil_mode) {
+    if (kd < 1 || kh < 1 || kw < 1 || sd < 1 || sh < 1 || sw < 1) return MP3D_ERR_WINDOW;
+    if (dd < 1 || dh < 1 || dw < 1 || pd < 0 || ph < 0 || pw < 0) return MP3D_ERR_WINDOW;
+    if (ceil_mode != 0 && ceil_mode != 1) return MP3D_ERR_WINDOW;
+    const long long od = ex_out_len(g->D, kd, sd, pd, dd, ceil_mode);
+    const long long oh = ex_out_len(g->H, kh, sh, ph, dh, ceil_mode);
+    const long long ow = ex_out_len(g->W, kw, sw, pw, dw, ceil_mode);
+    if (od < 1 || oh < 1 || ow < 1) return MP3D_ERR_WINDOW;
+    if (!ex_windows_nonempty(g->D, od, kd, sd, pd, dd) || !ex_windows_nonempty(g->H, oh, kh, sh, ph, dh) ||
+        !ex_windows_nonempty(g->W, ow, kw, sw, pw, dw))
+        return MP3D_ERR_WINDOW;
+    g->adaptive = 0;
+    g->kd = kd; g->kh = kh; g->kw = kw;
+    g->sd = sd; g->sh = sh; g->sw = sw;
+    g->pd = pd; g->ph = ph; g->pw = pw;
+    g->dd = dd; g->dh = dh; g->dw = dw;
+    return set_out(g, od, oh, ow);
+}
+
+// No padding, no dilation, and the output the unpadded formula gives: the
+// plain fixed-window geometry with its own fast paths.
+bool ex_is_plain(const Geo& g) {
+    return g.pd == 0 && g.ph == 0 && g.pw == 0 && g.dd == 1 && g.dh == 1 && g.dw == 1 &&
+           g.OD == (g.D - g.kd) / g.sd + 1 && g.OH == (g.H - g.kh) / g.sh + 1 &&
+           g.OW == (g.W - g.kw) / g.sw + 1;
 }
 
 // [a, a+na) and [b, b+nb) (bytes) overlap?
@@ -217,6 +279,75 @@ size_t workspace_needed(const Geo& g, int dtype, int algo) {
     return (size_t)(g.P * (long long)g.vol) * sizeof(float);
 }
 
+// Buffer checks of a backward call (before any CUDA call).
+int check_bwd_buffers(const void* grad_out, const int64_t* idx, const void* grad_in,
+                      const void* workspace, size_t workspace_bytes, const Geo& g, int dtype,
+                      int algo) {
+    const int es = elem_size(dtype);
+    const size_t need = workspace_needed(g, dtype, algo);
+    if (g.P == 0) return MP3D_OK;
+    if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
+    if (misaligned(grad_out, es) || misaligned(idx, 8) || misaligned(grad_in, es))
+        return MP3D_ERR_ALIGN;
+    const long long ng = g.P * g.ovol * es, ni = g.P * g.ovol * 8, nin = g.P * g.vol * es;
+    if (overlaps(grad_in, nin, grad_out, ng) || overlaps(grad_in, nin, idx, ni))
+        return MP3D_ERR_ALIAS;
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need || misaligned(workspace, 16))
+            return MP3D_ERR_WORKSPACE;
+        if (overlaps(workspace, (long long)need, grad_in, nin) ||
+            overlaps(workspace, (long long)need, grad_out, ng) ||
+            overlaps(workspace, (long long)need, idx, ni))
+            return MP3D_ERR_ALIAS;
+    }
+    return MP3D_OK;
+}
+
+// Path choice and launch of a checked backward call on the plain (unpadded)
+// geometry.
+int run_bwd(const void* grad_out, const int64_t* idx, void* grad_in, void* workspace, const Geo& g,
+            int dtype, int algo, cudaStream_t stream) {
+    const int path = bwd_path(g, dtype, algo, (uintptr_t)grad_in % 16 == 0);
+    const Geo gk = (path == MP3D_PATH_BWD_DISJOINT) ? as_fixed(g) : g;
+    log_path("bwd", path, gk, dtype);
+    if (path == MP3D_PATH_NOOP) return MP3D_OK;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    cudaError_t e;
+    switch (path) {
+    case MP3D_PATH_BWD_ATOMIC:
+        e = launch_bwd_atomic(grad_out, idx, grad_in, (float*)workspace, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_DISJOINT:
+        e = launch_bwd_disjoint(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_OVERLAP_ROLL:
+        e = launch_bwd_roll(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    case MP3D_PATH_BWD_OVERLAP_TILE:
+        e = launch_bwd_overlap_tile(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    default:
+        e = launch_bwd_overlap_direct(grad_out, idx, grad_in, gk, dtype, sms, stream);
+        break;
+    }
+    return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+// Geometry of a padded / dilated backward call: the given output sizes must
+// be the ones the window yields.
+int bwd_ex_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh, int ow,
+               int kd, int kh, int kw, int sd, int sh, int sw, int pd, int ph, int pw, int dd, int dh,
+               int dw, int ceil_mode, int dtype, int algo) {
+    int st = check_dims(N, C, D, H, W, g);
+    if (!st) st = ex_geo(g, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw, ceil_mode);
+    if (!st && (g->OD != od || g->OH != oh || g->OW != ow)) st = MP3D_ERR_WINDOW;
+    if (st) return st;
+    if (elem_size(dtype) == 0) return MP3D_ERR_DTYPE;
+    if (algo < MP3D_BWD_AUTO || algo > MP3D_BWD_ATOMIC) return MP3D_ERR_ALGO;
+    return MP3D_OK;
+}
+
 }  // namespace
 
 // ==================================================================== C ABI
@@ -288,50 +419,79 @@ int maxpool3d_bwd(const void* grad_out, const int64_t* idx, void* grad_in, int64
                   size_t workspace_bytes, cudaStream_t stream) {
     Geo g;
     int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, algo);
+    if (!st) st = check_bwd_buffers(grad_out, idx, grad_in, workspace, workspace_bytes, g, dtype, algo);
     if (st) return st;
-    const int es = elem_size(dtype);
-    const size_t need = workspace_needed(g, dtype, algo);
-    if (g.P > 0) {
-        if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
-        if (misaligned(grad_out, es) || misaligned(idx, 8) || misaligned(grad_in, es))
-            return MP3D_ERR_ALIGN;
-        const long long ng = g.P * g.ovol * es, ni = g.P * g.ovol * 8, nin = g.P * g.vol * es;
-        if (overlaps(grad_in, nin, grad_out, ng) || overlaps(grad_in, nin, idx, ni))
-            return MP3D_ERR_ALIAS;
-        if (need > 0) {
-            if (!workspace || workspace_bytes < need || misaligned(workspace, 16))
-                return MP3D_ERR_WORKSPACE;
-            if (overlaps(workspace, (long long)need, grad_in, nin) ||
-                overlaps(workspace, (long long)need, grad_out, ng) ||
-                overlaps(workspace, (long long)need, idx, ni))
-                return MP3D_ERR_ALIAS;
-        }
-    }
-    const int path = bwd_path(g, dtype, algo, (uintptr_t)grad_in % 16 == 0);
-    const Geo gk = (path == MP3D_PATH_BWD_DISJOINT) ? as_fixed(g) : g;
-    log_path("bwd", path, gk, dtype);
+    return run_bwd(grad_out, idx, grad_in, workspace, g, dtype, algo, stream);
+}
+
+int maxpool3d_fwd_ex(const void* x, void* y, int64_t* idx, int64_t N, int64_t C, int64_t D,
+                     int64_t H, int64_t W, int kd, int kh, int kw, int sd, int sh, int sw, int pd,
+                     int ph, int pw, int dd, int dh, int dw, int ceil_mode, int dtype,
+                     cudaStream_t stream) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = ex_geo(&g, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw, ceil_mode);
+    if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
+    if (st) return st;
+    if (ex_is_plain(g)) return run_fwd(x, y, idx, g, dtype, stream);
+    const int path = g.P == 0 ? MP3D_PATH_NOOP : MP3D_PATH_FWD_PADDED;
+    log_path("fwd", path, g, dtype);
+    if (path == MP3D_PATH_NOOP) return MP3D_OK;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    return launch_fwd_ex(x, y, idx, g, dtype, sms, stream) == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+int maxpool3d_fwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int kd, int kh,
+                          int kw, int sd, int sh, int sw, int pd, int ph, int pw, int dd, int dh,
+                          int dw, int ceil_mode, int dtype, int* path) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = ex_geo(&g, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw, ceil_mode);
+    if (!st && elem_size(dtype) == 0) st = MP3D_ERR_DTYPE;
+    if (!st && path)
+        *path = ex_is_plain(g) ? fwd_path(g, dtype) : g.P == 0 ? MP3D_PATH_NOOP : MP3D_PATH_FWD_PADDED;
+    return st;
+}
+
+int maxpool3d_bwd_ex(const void* grad_out, const int64_t* idx, void* grad_in, int64_t N, int64_t C,
+                     int64_t D, int64_t H, int64_t W, int od, int oh, int ow, int kd, int kh,
+                     int kw, int sd, int sh, int sw, int pd, int ph, int pw, int dd, int dh, int dw,
+                     int ceil_mode, int dtype, int algo, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    Geo g;
+    int st = bwd_ex_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw,
+                        ceil_mode, dtype, algo);
+    if (!st) st = check_bwd_buffers(grad_out, idx, grad_in, workspace, workspace_bytes, g, dtype, algo);
+    if (st) return st;
+    if (ex_is_plain(g)) return run_bwd(grad_out, idx, grad_in, workspace, g, dtype, algo, stream);
+    const int path = g.P == 0 ? MP3D_PATH_NOOP
+                     : algo == MP3D_BWD_ATOMIC ? MP3D_PATH_BWD_ATOMIC : MP3D_PATH_BWD_PADDED;
+    log_path("bwd", path, g, dtype);
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
     int sms = 0;
     if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
     cudaError_t e;
-    switch (path) {
-    case MP3D_PATH_BWD_ATOMIC:
-        e = launch_bwd_atomic(grad_out, idx, grad_in, (float*)workspace, gk, dtype, sms, stream);
-        break;
-    case MP3D_PATH_BWD_DISJOINT:
-        e = launch_bwd_disjoint(grad_out, idx, grad_in, gk, dtype, sms, stream);
-        break;
-    case MP3D_PATH_BWD_OVERLAP_ROLL:
-        e = launch_bwd_roll(grad_out, idx, grad_in, gk, dtype, sms, stream);
-        break;
-    case MP3D_PATH_BWD_OVERLAP_TILE:
-        e = launch_bwd_overlap_tile(grad_out, idx, grad_in, gk, dtype, sms, stream);
-        break;
-    default:
-        e = launch_bwd_overlap_direct(grad_out, idx, grad_in, gk, dtype, sms, stream);
-        break;
-    }
+    if (path == MP3D_PATH_BWD_ATOMIC)
+        e = launch_bwd_atomic(grad_out, idx, grad_in, (float*)workspace, g, dtype, sms, stream);
+    else
+        e = launch_bwd_ex_direct(grad_out, idx, grad_in, g, dtype, sms, stream);
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+int maxpool3d_bwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+                          int ow, int kd, int kh, int kw, int sd, int sh, int sw, int pd, int ph,
+                          int pw, int dd, int dh, int dw, int ceil_mode, int dtype, int algo,
+                          int* path) {
+    Geo g;
+    int st = bwd_ex_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw,
+                        ceil_mode, dtype, algo);
+    if (!st && path) {
+        if (ex_is_plain(g)) *path = bwd_path(g, dtype, algo);
+        else *path = g.P == 0 ? MP3D_PATH_NOOP
+                     : algo == MP3D_BWD_ATOMIC ? MP3D_PATH_BWD_ATOMIC : MP3D_PATH_BWD_PADDED;
+    }
+    return st;
 }
 
 int mp3d_device_error_flags(unsigned int* flags, int clear) {

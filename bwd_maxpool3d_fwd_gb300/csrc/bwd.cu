@@ -182,6 +182,66 @@ cudaError_t launch_bwd_overlap_direct(const void* go, const int64_t* idx, void* 
     }
 }
 
+// ------------------------------------------------------------------ padded / dilated, direct
+// Fixed windows with padding and dilation. One thread per input position:
+// along each axis the windows that contain position x are the o with
+// x = o*S - p + k*dl for some k in [0, K); stepping k downwards gives them
+// in ascending o. The gradients of those that selected the input are
+// summed in ascending (od, oh, ow) order (first term as the initial value).
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_bwd_ex_direct(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi,
+                Geo g) {
+    const long long total = g.P * (long long)g.vol;
+    const int HW = g.H * g.W;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long p = e / g.vol;
+        const int r = (int)(e - p * g.vol);
+        const int d = r / HW;
+        const int h = (r - d * HW) / g.W;
+        const int w = r - d * HW - h * g.W;
+        float acc = 0.0f;
+        bool any = false;
+        for (int a = g.kd - 1; a >= 0; --a) {
+            const int td = d + g.pd - a * g.dd;
+            if (td < 0 || td % g.sd != 0 || td / g.sd >= g.OD) continue;
+            const int od = td / g.sd;
+            for (int b = g.kh - 1; b >= 0; --b) {
+                const int th = h + g.ph - b * g.dh;
+                if (th < 0 || th % g.sh != 0 || th / g.sh >= g.OH) continue;
+                const long long row = ((p * g.OD + od) * g.OH + th / g.sh) * (long long)g.OW;
+                for (int c = g.kw - 1; c >= 0; --c) {
+                    const int tw = w + g.pw - c * g.dw;
+                    if (tw < 0 || tw % g.sw != 0 || tw / g.sw >= g.OW) continue;
+                    const long long o = row + tw / g.sw;
+                    if (__ldg(idx + o) == r) {
+                        const float v = Elem<T>::to_f(go[o]);
+                        acc = any ? acc + v : v;
+                        any = true;
+                    }
+                }
+            }
+        }
+        gi[e] = any ? Elem<T>::from_f(acc) : Elem<T>::from_f(0.0f);
+    }
+}
+
+cudaError_t launch_bwd_ex_direct(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                 int dtype, int sms, cudaStream_t s) {
+    const long long total = g.P * (long long)g.vol;
+    const int grid = grid_for(total, 256, sms, 8);
+    switch (dtype) {
+    case F32: k_bwd_ex_direct<float><<<grid, 256, 0, s>>>((const float*)go, idx, (float*)gi, g); break;
+    case F16: k_bwd_ex_direct<__half><<<grid, 256, 0, s>>>((const __half*)go, idx, (__half*)gi, g); break;
+    default:
+        k_bwd_ex_direct<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)go, idx,
+                                                            (__nv_bfloat16*)gi, g);
+        break;
+    }
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ atomic ablation
 // Zero n floats; 16-byte stores when the buffer starts on a 16-byte boundary.
 __global__ void __launch_bounds__(256) k_zero_f32(float* __restrict__ a, long long n) {

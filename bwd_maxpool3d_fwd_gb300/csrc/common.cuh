@@ -48,6 +48,8 @@ struct Geo {
     int adaptive;         // 1: adaptive windows
     int vol;              // D*H*W
     int ovol;             // OD*OH*OW
+    int pd, ph, pw;       // fixed windows: padding (0 unless padded)
+    int dd, dh, dw;       // fixed windows: dilation (1 unless dilated)
 };
 
 // Window i along one axis: [start, end).

@@ -53,6 +53,51 @@ k_fwd_generic(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ 
     }
 }
 
+// ------------------------------------------------------------------ padded / dilated
+// Fixed windows with padding and dilation: the window of output o along an
+// axis takes the positions o*S - p + k*dl, k = 0 .. K-1, inside the input
+// (padding is never chosen). One thread per output scans them in ascending
+// (d, h, w) order with the exact rule.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_fwd_ex(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g) {
+    const long long total = g.P * (long long)g.ovol;
+    const int HW = g.H * g.W;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const int ow = (int)(o % g.OW);
+        long long t = o / g.OW;
+        const int oh = (int)(t % g.OH);
+        t /= g.OH;
+        const int od = (int)(t % g.OD);
+        const long long p = t / g.OD;
+        const T* xp = x + p * g.vol;
+        int best = -1;
+        float m = 0.0f;
+        for (int a = 0; a < g.kd; ++a) {
+            const int d = od * g.sd - g.pd + a * g.dd;
+            if (d < 0 || d >= g.D) continue;
+            for (int b = 0; b < g.kh; ++b) {
+                const int h = oh * g.sh - g.ph + b * g.dh;
+                if (h < 0 || h >= g.H) continue;
+                const int row = d * HW + h * g.W;
+                for (int c = 0; c < g.kw; ++c) {
+                    const int w = ow * g.sw - g.pw + c * g.dw;
+                    if (w < 0 || w >= g.W) continue;
+                    const float v = Elem<T>::to_f(xp[row + w]);
+                    if (best < 0 || beats(v, m)) {
+                        m = v;
+                        best = row + w;
+                    }
+                }
+            }
+        }
+        // the host rejects geometries with an empty window, so best >= 0
+        y[o] = xp[best];
+        if (idx) idx[o] = best;
+    }
+}
+
 // ------------------------------------------------------------------ global
 // One window per plane (output 1x1x1). One warp per plane: each lane scans
 // a strided share of the plane with 16-byte loads when every plane starts
@@ -237,6 +282,23 @@ static cudaError_t fwd_generic_t(const void* x, void* y, int64_t* idx, const Geo
     else
         k_fwd_generic<T, false><<<grid, 256, 0, s>>>((const T*)x, (T*)y, idx, g);
     return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t fwd_ex_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
+                            cudaStream_t s) {
+    const long long total = g.P * (long long)g.ovol;
+    k_fwd_ex<T><<<grid_for(total, 256, sms, 8), 256, 0, s>>>((const T*)x, (T*)y, idx, g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_ex(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,
+                          cudaStream_t s) {
+    switch (dtype) {
+    case F32: return fwd_ex_t<float>(x, y, idx, g, sms, s);
+    case F16: return fwd_ex_t<__half>(x, y, idx, g, sms, s);
+    default: return fwd_ex_t<__nv_bfloat16>(x, y, idx, g, sms, s);
+    }
 }
 
 cudaError_t launch_fwd_generic(const void* x, void* y, int64_t* idx, const Geo& g, int dtype,

@@ -19,6 +19,9 @@ cudaError_t launch_fwd_s2(const void* x, void* y, int64_t* idx, const Geo& g,
                           int dtype, int sms, cudaStream_t s);
 cudaError_t launch_fwd_slab(const void* x, void* y, int64_t* idx, const Geo& g,
                             int dtype, int sms, cudaStream_t s);
+// Fixed windows with padding and dilation (g.pd..g.dw): one thread per output.
+cudaError_t launch_fwd_ex(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,
+                          cudaStream_t s);
 // Whether a window-depth slab of this geometry fits the slab kernel's shared memory.
 bool fwd_slab_supported(const Geo& g, int dtype);
 // Whether the stride-2 kernel handles this geometry and type (it needs the
@@ -46,6 +49,9 @@ bool bwd_tile_supported(const Geo& g);
 bool bwd_roll_supported(const Geo& g, int dtype, bool aligned16);
 cudaError_t launch_bwd_roll(const void* go, const int64_t* idx, void* gi, const Geo& g,
                             int dtype, int sms, cudaStream_t s);
+// Fixed windows with padding and dilation: direct gather in ascending order.
+cudaError_t launch_bwd_ex_direct(const void* go, const int64_t* idx, void* gi, const Geo& g,
+                                 int dtype, int sms, cudaStream_t s);
 cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, float* ws,
                               const Geo& g, int dtype, int sms, cudaStream_t s);
 

@@ -83,12 +83,14 @@ typedef enum {
     MP3D_PATH_FWD_S2 = 2,            /* stride-2 register-column kernel       */
     MP3D_PATH_FWD_GLOBAL = 3,        /* one window per plane (global pool)    */
     MP3D_PATH_FWD_SLAB = 4,          /* window-depth slab staged in shared memory */
+    MP3D_PATH_FWD_PADDED = 5,        /* padded / dilated windows, thread per output */
     MP3D_PATH_BWD_DISJOINT = 10,     /* single-pass gather, disjoint windows  */
     MP3D_PATH_BWD_OVERLAP_TILE = 11, /* overlapping gather, staged tile + owner sums */
     MP3D_PATH_BWD_OVERLAP_DIRECT = 12, /* overlapping gather, direct reads    */
     MP3D_PATH_BWD_ATOMIC = 13,       /* zero fill + atomic scatter ablation   */
-    MP3D_PATH_BWD_OVERLAP_ROLL = 14  /* overlapping, ordered scatter into a
+    MP3D_PATH_BWD_OVERLAP_ROLL = 14, /* overlapping, ordered scatter into a
                                         rolling ring of shared depth slices  */
+    MP3D_PATH_BWD_PADDED = 15        /* padded / dilated windows, direct gather */
 } mp3d_path;
 
 /*
@@ -162,6 +164,48 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                        int od, int oh, int ow,
                        int kd, int kh, int kw, int sd, int sh, int sw,
                        int dtype, int algo, int* path);
+
+/*
+ * Padding, dilation and ceil-mode output sizes: the fixed-window forward
+ * and backward beyond [MPF]'s "no padding" constraint, with the usual
+ * max_pool3d definition (the pages fix only the unpadded case). Along each
+ * axis (input I, kernel k, stride s, padding p on both sides, dilation dl):
+ *  - the window of output o takes the positions o*s - p + j*dl, j < k, that
+ *    lie inside [0, I) (padding is never chosen);
+ *  - O = floor((I + 2p - dl*(k-1) - 1) / s) + 1, or with ceil in place of
+ *    floor when ceil_mode = 1, where a last window starting at or past
+ *    I + p is dropped;
+ *  - requires k, s, dl >= 1, 0 <= 2p <= k, O >= 1, ceil_mode 0 or 1, and
+ *    every window holding at least one input position (dilation with
+ *    padding can leave a window empty): else MP3D_ERR_WINDOW.
+ * Ties, NaN, index form and the backward's summation order are those of
+ * maxpool3d_fwd / maxpool3d_bwd. Without padding or dilation, and with the
+ * output size the unpadded formula gives, the calls take the same paths as
+ * maxpool3d_fwd / maxpool3d_bwd. idx may be NULL in the forward (values
+ * only). The backward's (od, oh, ow) must equal the forward's output sizes;
+ * algo and workspace as for maxpool3d_bwd.
+ */
+int maxpool3d_fwd_ex(const void* x, void* y, int64_t* idx,
+                     int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                     int kd, int kh, int kw, int sd, int sh, int sw,
+                     int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                     int dtype, cudaStream_t stream);
+int maxpool3d_bwd_ex(const void* grad_out, const int64_t* idx, void* grad_in,
+                     int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                     int od, int oh, int ow,
+                     int kd, int kh, int kw, int sd, int sh, int sw,
+                     int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                     int dtype, int algo, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+/* Path the padded calls take (mp3d_path), with the same checks. */
+int maxpool3d_fwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                          int kd, int kh, int kw, int sd, int sh, int sw,
+                          int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                          int dtype, int* path);
+int maxpool3d_bwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                          int od, int oh, int ow, int kd, int kh, int kw, int sd, int sh, int sw,
+                          int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                          int dtype, int algo, int* path);
 
 /*
  * Backward without any device allocation (atomic form). The pages have no

@@ -174,3 +174,63 @@ def test_binding_rejects_cpu_tensors(L):
     x = torch.zeros((1, 1, 4, 4, 4))
     with pytest.raises(ValueError):
         mp.maxpool3d_fwd(x, x, x, (2, 2, 2), (2, 2, 2))
+
+
+def fwd_ex(L, x, y, i, N=1, C=1, D=6, H=6, W=6, k=(3, 3, 3), s=(2, 2, 2), p=(1, 1, 1), dl=(1, 1, 1),
+           cm=0, dt=0):
+    return L.maxpool3d_fwd_ex(x, y, i, N, C, D, H, W, *k, *s, *p, *dl, cm, dt, None)
+
+
+def test_padded_argument_errors(L, bufs):
+    # every case fails validation before any CUDA call (host buffers)
+    x, y, i, _ = bufs
+    assert fwd_ex(L, x, y, i, p=(2, 1, 1)) == WINDOW             # padding above half the kernel
+    assert fwd_ex(L, x, y, i, p=(-1, 0, 0)) == WINDOW
+    assert fwd_ex(L, x, y, i, dl=(0, 1, 1)) == WINDOW
+    assert fwd_ex(L, x, y, i, cm=2) == WINDOW
+    assert fwd_ex(L, x, y, i, D=1, k=(4, 3, 3), p=(0, 1, 1)) == WINDOW    # no output
+    # dilation 3 with padding 1 on a length-1 axis: the window {-1, 2} holds no input
+    assert fwd_ex(L, x, y, i, D=1, k=(2, 3, 3), s=(1, 2, 2), p=(1, 1, 1), dl=(3, 1, 1)) == WINDOW
+    assert fwd_ex(L, x, y, i, dt=3) == DTYPE
+    assert fwd_ex(L, None, y, i) == NULLPTR
+    assert fwd_ex(L, None, None, None, N=0) == OK
+    g = L.maxpool3d_bwd_ex
+    # output sizes must be the window's: 6 with k3 s2 p1 gives 3
+    assert g(x, i, y, 1, 1, 6, 6, 6, 4, 3, 3, 3, 3, 3, 2, 2, 2, 1, 1, 1, 1, 1, 1, 0, 0, 0, None, 0,
+             None) == WINDOW
+    assert g(x, i, y, 1, 1, 6, 6, 6, 3, 3, 3, 3, 3, 3, 2, 2, 2, 1, 1, 1, 1, 1, 1, 0, 0, 3, None, 0,
+             None) == ALGO
+
+
+def test_padded_plans(L):
+    f32, f16 = torch.float32, torch.float16
+    # padded or dilated: the padded kernels
+    assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                    False, f16) == "fwd_padded"
+    assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1),
+                                    False, f32) == "fwd_padded"
+    out = mp.pool_out_size_ex((8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1))
+    assert mp.maxpool3d_bwd_ex_plan((2, 3, 8, 9, 10), out, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                    False, f16) == "bwd_padded"
+    assert mp.maxpool3d_bwd_ex_plan((2, 3, 8, 9, 10), out, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                    False, f16, mp.BWD_ATOMIC) == "bwd_atomic"
+    # the plain geometry keeps its fast paths
+    assert mp.maxpool3d_fwd_ex_plan((2, 3, 16, 112, 112), (3, 3, 3), (2, 2, 2), (0, 0, 0), (1, 1, 1),
+                                    False, f16) == "fwd_s2"
+    assert mp.maxpool3d_bwd_ex_plan((2, 3, 16, 112, 112), (7, 55, 55), (3, 3, 3), (2, 2, 2), (0, 0, 0),
+                                    (1, 1, 1), False, f16) == "bwd_overlap_roll"
+    # ceil mode that adds a window is not the plain geometry
+    assert mp.pool_out_size_ex((9, 9, 9), (2, 2, 2), (2, 2, 2), ceil_mode=True) == (5, 5, 5)
+    assert mp.maxpool3d_fwd_ex_plan((1, 1, 9, 9, 9), (2, 2, 2), (2, 2, 2), (0, 0, 0), (1, 1, 1),
+                                    True, f32) == "fwd_padded"
+
+
+def test_padded_out_size_matches_oracle(orc):
+    for I in range(1, 12):
+        for K in range(1, 5):
+            for S in range(1, 4):
+                for p in range(0, 3):
+                    for dl in range(1, 4):
+                        for cm in (False, True):
+                            (got,) = mp.pool_out_size_ex((I,), (K,), (S,), (p,), (dl,), cm)
+                            assert got == orc.ex_out_size(I, K, S, p, dl, cm), (I, K, S, p, dl, cm)

@@ -475,3 +475,69 @@ def test_values_only_forward(case):
         mp.adaptive_maxpool3d_fwd(x.to(DEV), y, None, out)
     torch.cuda.synchronize()
     assert_bits_equal(y.cpu(), y_ref, "y (values only)")
+
+
+# Padding, dilation and ceil mode: forward values and indices, the direct
+# gather backward bit for bit, and the atomic form within its tolerance.
+PADDED_CASES = [
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (2, 3, 9, 20, 33)),
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), True, (1, 2, 8, 17, 30)),
+    ((2, 2, 2), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (1, 3, 7, 11, 16)),
+    ((3, 2, 3), (1, 2, 2), (1, 0, 1), (2, 1, 2), False, (1, 2, 9, 12, 21)),
+    ((2, 3, 2), (2, 1, 3), (0, 1, 1), (3, 2, 1), True, (2, 2, 10, 9, 23)),
+    ((2, 2, 2), (2, 2, 2), (0, 0, 0), (1, 1, 1), True, (1, 2, 9, 9, 9)),       # ceil adds a window
+    ((4, 4, 4), (3, 3, 3), (2, 2, 2), (1, 1, 1), True, (1, 2, 11, 14, 19)),
+]
+
+
+def _gpu_fwd_ex(x_cpu, k, s, p, dl, cm):
+    x = x_cpu.to(DEV)
+    out = mp.pool_out_size_ex(x.shape[2:], k, s, p, dl, cm)
+    y = torch.empty(x.shape[:2] + out, dtype=x.dtype, device=DEV)
+    idx = torch.empty(x.shape[:2] + out, dtype=torch.int64, device=DEV)
+    mp.maxpool3d_fwd_ex(x, y, idx, k, s, p, dl, cm)
+    torch.cuda.synchronize()
+    return y.cpu(), idx.cpu()
+
+
+def _gpu_bwd_ex(g_cpu, idx_cpu, in_shape, k, s, p, dl, cm, algo=mp.BWD_AUTO):
+    g, idx = g_cpu.to(DEV), idx_cpu.to(DEV)
+    gin = torch.empty(in_shape, dtype=g.dtype, device=DEV)
+    nbytes = mp.maxpool3d_bwd_workspace_bytes(in_shape, g.dtype, algo)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=DEV) if nbytes else None
+    mp.maxpool3d_bwd_ex(g, idx, gin, k, s, p, dl, cm, algo=algo, workspace=ws)
+    torch.cuda.synchronize()
+    return gin.cpu()
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(PADDED_CASES)))
+def test_padded_fwd_bwd(case, dtype):
+    k, s, p, dl, cm, shape = PADDED_CASES[case]
+    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, dl, cm, dtype) == "fwd_padded"
+    gen = torch.Generator().manual_seed(9500 + case)
+    x = random_input(gen, shape, dtype, KINDS[case % 3])
+    y_ref, i_ref = oracle.maxpool3d_fwd_ex(x, k, s, p, dl, cm)
+    y, idx = _gpu_fwd_ex(x, k, s, p, dl, cm)
+    assert torch.equal(idx, i_ref)
+    assert_bits_equal(y, y_ref, "y (padded)")
+    g = torch.randn(y_ref.shape, generator=gen).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    assert mp.maxpool3d_bwd_ex_plan(shape, y_ref.shape[2:], k, s, p, dl, cm, dtype) == "bwd_padded"
+    assert_bits_equal(_gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm), gin_ref, "grad_in (padded)")
+    gin_a = _gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm, algo=mp.BWD_ATOMIC)
+    assert _atomic_tolerance_ok(gin_a, gin_ref, g, i_ref, dtype)
+
+
+def test_padded_plain_geometry_matches_plain_entry_points():
+    # no padding, no dilation, floor sizes: the same paths and results
+    gen = torch.Generator().manual_seed(9600)
+    shape, k, s = (1, 2, 16, 40, 48), (3, 3, 3), (2, 2, 2)
+    x = random_input(gen, shape, torch.float16, "ties")
+    y0, i0 = gpu_fwd(x, kernel=k, stride=s)
+    y1, i1 = _gpu_fwd_ex(x, k, s, (0, 0, 0), (1, 1, 1), False)
+    assert torch.equal(i0, i1)
+    assert_bits_equal(y0, y1, "y")
+    g = torch.randn(y0.shape, generator=gen).half()
+    assert_bits_equal(gpu_bwd(g, i0, shape, k, s), _gpu_bwd_ex(g, i0, shape, k, s, (0, 0, 0), (1, 1, 1),
+                                                             False), "grad_in")
