@@ -445,6 +445,18 @@ def per_config(dev, peak):
         tv = time_one(r.fwd_values, dev, iters=20, flush=True)
         vb = fb - w.planes * w.out[0] * w.out[1] * w.out[2] * 8
         vg = vb / (tv * 1e-3) / 1e9
+        # backward without stored indices: timed where the fused 2x2x2 kernel
+        # applies (the direct form rescans every covering window per input)
+        rec = None
+        if w.mode == "fixed" and r.mp.maxpool3d_bwd_recompute_plan(
+                w.in_shape, w.out, w.kernel, w.stride, w.dtype) == "bwd_recompute_k2s2":
+            tr = time_one(lambda: r.mp.maxpool3d_bwd_recompute(r.x, r.g, r.gin, w.kernel, w.stride),
+                          dev, iters=20, flush=True)
+            rb = w.planes * (w.D * w.H * w.W * w.elem_bytes * 2 + w.out[0] * w.out[1] * w.out[2] *
+                             w.elem_bytes)
+            rg = rb / (tr * 1e-3) / 1e9
+            rec = {"us": round(tr * 1e3, 2), "bytes": rb, "gbs": round(rg, 1),
+                   "frac": round(rg / peak, 4), "path": "bwd_recompute_k2s2"}
         out[w.name] = {
             "fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2),
             "fwd_bytes": fb, "bwd_bytes": bb,
@@ -454,7 +466,8 @@ def per_config(dev, peak):
             "bwd_frac_of_nominal_8000": round(bg / NOMINAL_HBM_GBS, 4),
             "fwd_path": pf, "bwd_path": pb,
             "fwd_values_only_us": round(tv * 1e3, 2), "fwd_values_only_bytes": vb,
-            "fwd_values_only_gbs": round(vg, 1), "fwd_values_only_frac": round(vg / peak, 4)}
+            "fwd_values_only_gbs": round(vg, 1), "fwd_values_only_frac": round(vg / peak, 4),
+            "bwd_recompute": rec}
         del r
         torch.cuda.empty_cache()
     return out

@@ -25,7 +25,7 @@ DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 5: "fwd_padded",
          10: "bwd_disjoint",
          11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll",
-         15: "bwd_padded"}
+         15: "bwd_padded", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct"}
 
 _lib = None
 
@@ -60,11 +60,14 @@ def lib() -> ctypes.CDLL:
     L.maxpool3d_bwd_ex.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 18 + [vp, sz, vp]
     L.maxpool3d_fwd_ex_plan.argtypes = [i64] * 5 + [i32] * 14 + [pi32]
     L.maxpool3d_bwd_ex_plan.argtypes = [i64] * 5 + [i32] * 18 + [pi32]
+    L.maxpool3d_bwd_recompute.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 10 + [vp]
+    L.maxpool3d_bwd_recompute_plan.argtypes = [i64] * 5 + [i32] * 10 + [pi32]
     L.mp3d_status_string.argtypes = [i32]
     L.mp3d_status_string.restype = ctypes.c_char_p
     for f in (L.maxpool3d_fwd, L.adaptive_maxpool3d_fwd, L.maxpool3d_bwd, L.maxpool3d_fwd_plan,
               L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan, L.maxpool3d_fwd_ex,
-              L.maxpool3d_bwd_ex, L.maxpool3d_fwd_ex_plan, L.maxpool3d_bwd_ex_plan):
+              L.maxpool3d_bwd_ex, L.maxpool3d_fwd_ex_plan, L.maxpool3d_bwd_ex_plan,
+              L.maxpool3d_bwd_recompute, L.maxpool3d_bwd_recompute_plan):
         f.restype = i32
     _lib = L
     return L
@@ -166,6 +169,30 @@ def maxpool3d_bwd_ex(grad_out, idx, grad_in, kernel, stride, padding=(0, 0, 0), 
                                     int(bool(ceil_mode)), _code(grad_out), algo, ws, wsb,
                                     _stream(grad_in, stream))
     _check(st, "maxpool3d_bwd_ex")
+
+
+def maxpool3d_bwd_recompute(x, grad_out, grad_in, kernel=None, stride=None, stream=None):
+    """Backward without stored indices: the argmax of every window is
+    recomputed from x. kernel/stride None = adaptive windows."""
+    _cuda(x, grad_out, grad_in)
+    N, C, D, H, W = grad_in.shape
+    od, oh, ow = grad_out.shape[2:]
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    with torch.cuda.device(grad_in.device):
+        st = lib().maxpool3d_bwd_recompute(x.data_ptr(), grad_out.data_ptr(), grad_in.data_ptr(), N,
+                                           C, D, H, W, od, oh, ow, *k, *s, _code(grad_out),
+                                           _stream(grad_in, stream))
+    _check(st, "maxpool3d_bwd_recompute")
+
+
+def maxpool3d_bwd_recompute_plan(in_shape, out_size, kernel, stride, dtype) -> str:
+    p = ctypes.c_int(-1)
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    _check(lib().maxpool3d_bwd_recompute_plan(*in_shape, *out_size, *k, *s, DTYPE_CODE[dtype],
+                                              ctypes.byref(p)), "maxpool3d_bwd_recompute_plan")
+    return PATHS[p.value]
 
 
 def maxpool3d_fwd_ex_plan(in_shape, kernel, stride, padding, dilation, ceil_mode, dtype) -> str:

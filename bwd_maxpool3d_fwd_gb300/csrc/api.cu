@@ -48,6 +48,8 @@ const char* path_name(int path) {
     case MP3D_PATH_BWD_OVERLAP_ROLL: return "bwd_overlap_roll";
     case MP3D_PATH_FWD_PADDED: return "fwd_padded";
     case MP3D_PATH_BWD_PADDED: return "bwd_padded";
+    case MP3D_PATH_BWD_RECOMPUTE_TILES: return "bwd_recompute_k2s2";
+    case MP3D_PATH_BWD_RECOMPUTE: return "bwd_recompute_direct";
     default: return "?";
     }
 }
@@ -490,6 +492,42 @@ int maxpool3d_bwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
         if (ex_is_plain(g)) *path = bwd_path(g, dtype, algo);
         else *path = g.P == 0 ? MP3D_PATH_NOOP
                      : algo == MP3D_BWD_ATOMIC ? MP3D_PATH_BWD_ATOMIC : MP3D_PATH_BWD_PADDED;
+    }
+    return st;
+}
+
+int maxpool3d_bwd_recompute(const void* x, const void* grad_out, void* grad_in, int64_t N,
+                            int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh, int ow,
+                            int kd, int kh, int kw, int sd, int sh, int sw, int dtype,
+                            cudaStream_t stream) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, MP3D_BWD_AUTO);
+    if (st) return st;
+    if (g.P == 0) return MP3D_OK;
+    const int es = elem_size(dtype);
+    if (!x || !grad_out || !grad_in) return MP3D_ERR_NULLPTR;
+    if (misaligned(x, es) || misaligned(grad_out, es) || misaligned(grad_in, es)) return MP3D_ERR_ALIGN;
+    const long long nx = g.P * g.vol * es, ng = g.P * g.ovol * es;
+    if (overlaps(grad_in, nx, x, nx) || overlaps(grad_in, nx, grad_out, ng)) return MP3D_ERR_ALIAS;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    int kind = 1;
+    const cudaError_t e = launch_bwd_recompute(x, grad_out, grad_in, g, dtype, sms, stream, &kind);
+    log_path("bwd", kind == 0 ? MP3D_PATH_BWD_RECOMPUTE_TILES : MP3D_PATH_BWD_RECOMPUTE, g, dtype);
+    return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+int maxpool3d_bwd_recompute_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od,
+                                 int oh, int ow, int kd, int kh, int kw, int sd, int sh, int sw,
+                                 int dtype, int* path) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, MP3D_BWD_AUTO);
+    if (!st && path) {
+        const int vec = 16 / elem_size(dtype);
+        const bool tiles = !g.adaptive && g.kd == 2 && g.kh == 2 && g.kw == 2 && g.sd == 2 &&
+                           g.sh == 2 && g.sw == 2 && g.D == 2 * g.OD && g.H == 2 * g.OH &&
+                           g.W == 2 * g.OW && g.W % vec == 0;
+        *path = g.P == 0 ? MP3D_PATH_NOOP : tiles ? MP3D_PATH_BWD_RECOMPUTE_TILES : MP3D_PATH_BWD_RECOMPUTE;
     }
     return st;
 }

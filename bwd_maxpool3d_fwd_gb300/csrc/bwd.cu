@@ -242,6 +242,168 @@ cudaError_t launch_bwd_ex_direct(const void* go, const int64_t* idx, void* gi, c
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ recompute (no stored index)
+// Backward without stored indices: each window's argmax is recomputed from
+// the input x with the forward's rule (scan d, then h, then w; replace only
+// on "beats"), so the result equals the backward through the forward's
+// indices bit for bit.
+
+// Argmax (in-plane offset) of window (od, oh, ow) of plane xp.
+template <typename T, bool ADAPTIVE>
+__device__ __forceinline__ int window_argmax(const T* __restrict__ xp, int od, int oh, int ow,
+                                             const Geo& g) {
+    const int HW = g.H * g.W;
+    const int ds = win_start(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int de = win_end(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+    const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+    const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+    const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+    int best = ds * HW + hs * g.W + ws;
+    float m = Elem<T>::to_f(xp[best]);
+    for (int d = ds; d < de; ++d)
+        for (int h = hs; h < he; ++h) {
+            const int row = d * HW + h * g.W;
+            for (int w = ws; w < we; ++w) {
+                const float v = Elem<T>::to_f(xp[row + w]);
+                if (beats(v, m)) {
+                    m = v;
+                    best = row + w;
+                }
+            }
+        }
+    return best;
+}
+
+// Any geometry: one thread per input position enumerates its covering
+// windows in ascending (od, oh, ow) order, recomputes each one's argmax and
+// sums the gradients of those that chose it (first term as initial value).
+template <typename T, bool ADAPTIVE>
+__global__ void __launch_bounds__(256)
+k_bwd_recompute_direct(const T* __restrict__ x, const T* __restrict__ go, T* __restrict__ gi,
+                       Geo g) {
+    const long long total = g.P * (long long)g.vol;
+    const int HW = g.H * g.W;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long p = e / g.vol;
+        const int r = (int)(e - p * g.vol);
+        const int d = r / HW;
+        const int h = (r - d * HW) / g.W;
+        const int w = r - d * HW - h * g.W;
+        const T* xp = x + p * g.vol;
+        float acc = 0.0f;
+        bool any = false;
+        const int d1 = cover_hi(d, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+        const int h1 = cover_hi(h, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+        const int w1 = cover_hi(w, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+        for (int od = cover_lo(d, g.D, g.OD, g.kd, g.sd, ADAPTIVE); od <= d1; ++od)
+            for (int oh = cover_lo(h, g.H, g.OH, g.kh, g.sh, ADAPTIVE); oh <= h1; ++oh)
+                for (int ow = cover_lo(w, g.W, g.OW, g.kw, g.sw, ADAPTIVE); ow <= w1; ++ow) {
+                    if (window_argmax<T, ADAPTIVE>(xp, od, oh, ow, g) != r) continue;
+                    const float v = Elem<T>::to_f(go[((p * g.OD + od) * g.OH + oh) * (long long)g.OW + ow]);
+                    acc = any ? acc + v : v;
+                    any = true;
+                }
+        gi[e] = any ? Elem<T>::from_f(acc) : Elem<T>::from_f(0.0f);
+    }
+}
+
+// 2x2x2 windows, stride 2, tiling the input, rows of 16-byte chunks: one
+// thread per run of VEC/2 windows of one window row loads the two-by-two
+// input rows of the run (16-byte loads), finds each window's argmax with
+// the exact scalar rule, loads the gradients and writes the run's 2x2 rows
+// of gradient chunks (the gradient at the argmax, zero elsewhere).
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_bwd_recompute_k2s2(const T* __restrict__ x, const T* __restrict__ go, T* __restrict__ gi, Geo g,
+                     FastDiv fSpr, FastDiv fOH) {
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int NW = VEC / 2;
+    const int HW = g.H * g.W;
+    const int spr = g.OW / NW;
+    const int nseg = g.ovol / NW;
+    const T zero = Elem<T>::from_f(0.0f);
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        const T* xp = x + p * g.vol;
+        for (int sg = blockIdx.x * blockDim.x + threadIdx.x; sg < nseg; sg += gridDim.x * blockDim.x) {
+            const int row = fSpr.div(sg);
+            const int ow0 = (sg - row * spr) * NW;
+            const int od = fOH.div(row);
+            const int oh = row - od * g.OH;
+            const int base = 2 * od * HW + 2 * oh * g.W + 2 * ow0;
+            Vec16<T> r[4];
+#pragma unroll
+            for (int dh = 0; dh < 4; ++dh)
+                r[dh].u = __ldg(reinterpret_cast<const uint4*>(xp + base + (dh >> 1) * HW + (dh & 1) * g.W));
+            // code of each window's argmax: dh * 2 + ww (scan d, h, then w)
+            int code[NW];
+#pragma unroll
+            for (int k = 0; k < NW; ++k) {
+                float m = Elem<T>::to_f(r[0].e[2 * k]);
+                int c = 0;
+#pragma unroll
+                for (int q = 1; q < 8; ++q) {
+                    const float v = Elem<T>::to_f(r[q >> 1].e[2 * k + (q & 1)]);
+                    if (beats(v, m)) {
+                        m = v;
+                        c = q;
+                    }
+                }
+                code[k] = c;
+            }
+            const long long o0 = p * (long long)g.ovol + (long long)sg * NW;
+            T gv[NW];
+#pragma unroll
+            for (int k = 0; k < NW; ++k) gv[k] = go[o0 + k];
+            T* out = gi + p * (long long)g.vol + base;
+#pragma unroll
+            for (int dh = 0; dh < 4; ++dh) {
+                Vec16<T> c;
+#pragma unroll
+                for (int k = 0; k < NW; ++k)
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) c.e[2 * k + t] = code[k] == dh * 2 + t ? gv[k] : zero;
+                *reinterpret_cast<uint4*>(out + (dh >> 1) * HW + (dh & 1) * g.W) = c.u;
+            }
+        }
+    }
+}
+
+template <typename T>
+static cudaError_t bwd_recompute_t(const void* x, const void* go, void* gi, const Geo& g, int sms,
+                                   cudaStream_t s, int* kind) {
+    constexpr int VEC = 16 / sizeof(T);
+    const bool tiles = !g.adaptive && g.kd == 2 && g.kh == 2 && g.kw == 2 && g.sd == 2 && g.sh == 2 &&
+                       g.sw == 2 && g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW &&
+                       g.W % VEC == 0 && (uintptr_t)x % 16 == 0 && (uintptr_t)gi % 16 == 0;
+    if (tiles) {
+        *kind = 0;
+        const int nseg = g.ovol / (VEC / 2);
+        dim3 grid((unsigned)((nseg + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
+        k_bwd_recompute_k2s2<T><<<grid, 256, 0, s>>>((const T*)x, (const T*)go, (T*)gi, g,
+                                                     FastDiv((uint32_t)(g.OW / (VEC / 2))),
+                                                     FastDiv((uint32_t)g.OH));
+        return cudaGetLastError();
+    }
+    *kind = 1;
+    const int grid = grid_for(g.P * (long long)g.vol, 256, sms, 8);
+    if (g.adaptive)
+        k_bwd_recompute_direct<T, true><<<grid, 256, 0, s>>>((const T*)x, (const T*)go, (T*)gi, g);
+    else
+        k_bwd_recompute_direct<T, false><<<grid, 256, 0, s>>>((const T*)x, (const T*)go, (T*)gi, g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_recompute(const void* x, const void* go, void* gi, const Geo& g, int dtype,
+                                 int sms, cudaStream_t s, int* kind) {
+    switch (dtype) {
+    case F32: return bwd_recompute_t<float>(x, go, gi, g, sms, s, kind);
+    case F16: return bwd_recompute_t<__half>(x, go, gi, g, sms, s, kind);
+    default: return bwd_recompute_t<__nv_bfloat16>(x, go, gi, g, sms, s, kind);
+    }
+}
+
 // ------------------------------------------------------------------ atomic ablation
 // Zero n floats; 16-byte stores when the buffer starts on a 16-byte boundary.
 __global__ void __launch_bounds__(256) k_zero_f32(float* __restrict__ a, long long n) {

@@ -52,6 +52,10 @@ cudaError_t launch_bwd_roll(const void* go, const int64_t* idx, void* gi, const 
 // Fixed windows with padding and dilation: direct gather in ascending order.
 cudaError_t launch_bwd_ex_direct(const void* go, const int64_t* idx, void* gi, const Geo& g,
                                  int dtype, int sms, cudaStream_t s);
+// Backward without stored indices (argmax recomputed from x). *kind is set
+// to 0 for the fused 2x2x2 tiling kernel, 1 for the direct form.
+cudaError_t launch_bwd_recompute(const void* x, const void* go, void* gi, const Geo& g, int dtype,
+                                 int sms, cudaStream_t s, int* kind);
 cudaError_t launch_bwd_atomic(const void* go, const int64_t* idx, void* gi, float* ws,
                               const Geo& g, int dtype, int sms, cudaStream_t s);
 

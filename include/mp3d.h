@@ -90,7 +90,9 @@ typedef enum {
     MP3D_PATH_BWD_ATOMIC = 13,       /* zero fill + atomic scatter ablation   */
     MP3D_PATH_BWD_OVERLAP_ROLL = 14, /* overlapping, ordered scatter into a
                                         rolling ring of shared depth slices  */
-    MP3D_PATH_BWD_PADDED = 15        /* padded / dilated windows, direct gather */
+    MP3D_PATH_BWD_PADDED = 15,       /* padded / dilated windows, direct gather */
+    MP3D_PATH_BWD_RECOMPUTE_TILES = 16, /* no stored index, 2x2x2 tiling, fused */
+    MP3D_PATH_BWD_RECOMPUTE = 17     /* no stored index, direct form          */
 } mp3d_path;
 
 /*
@@ -164,6 +166,26 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                        int od, int oh, int ow,
                        int kd, int kh, int kw, int sd, int sh, int sw,
                        int dtype, int algo, int* path);
+
+/*
+ * Backward without stored indices [AMPB]: the same grad_in as
+ * maxpool3d_bwd(grad_out, idx, ...) with idx the indices maxpool3d_fwd (or
+ * adaptive_maxpool3d_fwd) would store for x, bit for bit: each window's
+ * argmax is recomputed from x with the forward's rule. For callers that
+ * keep the input but not the int64 indices (8 bytes per output). x:
+ * [N, C, D, H, W] as given to the forward; grad_out [N, C, od, oh, ow];
+ * grad_in like x, every element written. Window arguments as for
+ * maxpool3d_bwd (kd..sw all 0: adaptive). No workspace.
+ */
+int maxpool3d_bwd_recompute(const void* x, const void* grad_out, void* grad_in,
+                            int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                            int od, int oh, int ow,
+                            int kd, int kh, int kw, int sd, int sh, int sw,
+                            int dtype, cudaStream_t stream);
+int maxpool3d_bwd_recompute_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                                 int od, int oh, int ow,
+                                 int kd, int kh, int kw, int sd, int sh, int sw,
+                                 int dtype, int* path);
 
 /*
  * Padding, dilation and ceil-mode output sizes: the fixed-window forward

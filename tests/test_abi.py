@@ -234,3 +234,23 @@ def test_padded_out_size_matches_oracle(orc):
                         for cm in (False, True):
                             (got,) = mp.pool_out_size_ex((I,), (K,), (S,), (p,), (dl,), cm)
                             assert got == orc.ex_out_size(I, K, S, p, dl, cm), (I, K, S, p, dl, cm)
+
+
+def test_recompute_argument_errors_and_plans(L, bufs):
+    x, g, gi, _ = bufs
+    f = L.maxpool3d_bwd_recompute
+    args = (1, 1, 4, 4, 4, 2, 2, 2, 2, 2, 2, 2, 2, 2, 0, None)
+    assert f(None, g, gi, *args) == NULLPTR
+    assert f(x, g, x + 8, *args) == ALIAS                 # grad_in overlaps x
+    assert f(x, g, gi, 1, 1, 4, 4, 4, 3, 2, 2, 2, 2, 2, 2, 2, 2, 0, None) == WINDOW
+    assert f(x, g, gi, 1, 1, 4, 4, 4, 2, 2, 2, 2, 2, 2, 2, 2, 2, 7, None) == DTYPE
+    assert f(None, None, None, 0, 1, 4, 4, 4, 2, 2, 2, 2, 2, 2, 2, 2, 2, 0, None) == OK
+    bf = torch.bfloat16
+    assert mp.maxpool3d_bwd_recompute_plan((2, 3, 8, 8, 32), (4, 4, 16), (2, 2, 2), (2, 2, 2),
+                                           bf) == "bwd_recompute_k2s2"
+    assert mp.maxpool3d_bwd_recompute_plan((2, 3, 9, 8, 32), (4, 4, 16), (2, 2, 2), (2, 2, 2),
+                                           bf) == "bwd_recompute_direct"
+    assert mp.maxpool3d_bwd_recompute_plan((2, 3, 9, 9, 9), (4, 4, 4), (3, 3, 3), (2, 2, 2),
+                                           bf) == "bwd_recompute_direct"
+    assert mp.maxpool3d_bwd_recompute_plan((2, 3, 9, 9, 9), (4, 4, 4), None, None,
+                                           bf) == "bwd_recompute_direct"

@@ -541,3 +541,35 @@ def test_padded_plain_geometry_matches_plain_entry_points():
     g = torch.randn(y0.shape, generator=gen).half()
     assert_bits_equal(gpu_bwd(g, i0, shape, k, s), _gpu_bwd_ex(g, i0, shape, k, s, (0, 0, 0), (1, 1, 1),
                                                              False), "grad_in")
+
+
+# Backward without stored indices: the same bits as the backward through
+# the forward's indices (oracle forward, then oracle backward).
+RECOMPUTE_CASES = [
+    ((2, 2, 2), (2, 2, 2), None, (2, 3, 8, 12, 64)),        # 2x2x2 tiling, fused kernel
+    ((2, 2, 2), (2, 2, 2), None, (1, 2, 9, 11, 40)),        # not a tiling
+    ((3, 3, 3), (2, 2, 2), None, (1, 2, 9, 13, 21)),        # overlapping
+    ((1, 3, 2), (3, 2, 1), None, (1, 2, 10, 9, 14)),
+    (None, None, (3, 4, 5), (1, 2, 9, 12, 15)),             # adaptive, divisible
+    (None, None, (4, 5, 6), (2, 2, 10, 11, 13)),            # adaptive, overlapping
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(RECOMPUTE_CASES)))
+def test_backward_recompute(case, dtype):
+    k, s, out, shape = RECOMPUTE_CASES[case]
+    gen = torch.Generator().manual_seed(9700 + case)
+    x = random_input(gen, shape, dtype, KINDS[case % 3])
+    if k is not None:
+        _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    else:
+        _, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    want = "bwd_recompute_k2s2" if case == 0 else "bwd_recompute_direct"
+    assert mp.maxpool3d_bwd_recompute_plan(shape, i_ref.shape[2:], k, s, dtype) == want
+    gin = torch.empty(shape, dtype=dtype, device=DEV)
+    mp.maxpool3d_bwd_recompute(x.to(DEV), g.to(DEV), gin, k, s)
+    torch.cuda.synchronize()
+    assert_bits_equal(gin.cpu(), ref, "grad_in (recomputed argmax)")
