@@ -509,6 +509,36 @@ def padded_config(dev, peak):
                                                  False, torch.float16)}
 
 
+def ndhwc_configs(dev, peak):
+    """The k2s2 and k3s2 workloads in the channels-last layout (the same
+    values with the channel axis moved last): forward and backward timed
+    alone (median of 20, L2 flushed before every launch)."""
+    import bwd_maxpool3d_fwd_gb300 as mp
+    out = {}
+    for w in workloads.WORKLOADS:
+        if w.mode != "fixed":
+            continue
+        x = workloads.make_x(w).permute(0, 2, 3, 4, 1).contiguous().to(dev)
+        g = workloads.make_grad_out(w).permute(0, 2, 3, 4, 1).contiguous().to(dev)
+        N, D, H, W, C = x.shape
+        oshape = (N,) + tuple(w.out) + (C,)
+        y = torch.empty(oshape, dtype=w.dtype, device=dev)
+        idx = torch.empty(oshape, dtype=torch.int64, device=dev)
+        gin = torch.empty_like(x)
+        tf = time_one(lambda: mp.maxpool3d_fwd_ndhwc(x, y, idx, w.kernel, w.stride), dev, 20, True)
+        tb = time_one(lambda: mp.maxpool3d_bwd_ndhwc(g, idx, gin, w.kernel, w.stride), dev, 20, True)
+        fb, bb = algorithmic_bytes(w)
+        fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
+        out[w.name + "_ndhwc"] = {
+            "fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2), "fwd_bytes": fb,
+            "bwd_bytes": bb, "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
+            "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
+            "fwd_path": "fwd_ndhwc", "bwd_path": "bwd_ndhwc"}
+        del x, g, y, idx, gin
+        torch.cuda.empty_cache()
+    return out
+
+
 def our_arm(args):
     rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
@@ -576,6 +606,7 @@ def our_arm(args):
     cfg = per_config(dev, peak) if (rank == 0 and not args.no_per_config) else None
     if cfg is not None:
         cfg[PADDED["name"]] = padded_config(dev, peak)
+        cfg.update(ndhwc_configs(dev, peak))
     cpu = cpu_baseline(base) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
         return None

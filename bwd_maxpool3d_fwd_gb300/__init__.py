@@ -25,7 +25,8 @@ DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 5: "fwd_padded",
          10: "bwd_disjoint",
          11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll",
-         15: "bwd_padded", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct"}
+         15: "bwd_padded", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct", 6: "fwd_ndhwc",
+         18: "bwd_ndhwc"}
 
 _lib = None
 
@@ -62,12 +63,16 @@ def lib() -> ctypes.CDLL:
     L.maxpool3d_bwd_ex_plan.argtypes = [i64] * 5 + [i32] * 18 + [pi32]
     L.maxpool3d_bwd_recompute.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 10 + [vp]
     L.maxpool3d_bwd_recompute_plan.argtypes = [i64] * 5 + [i32] * 10 + [pi32]
+    L.maxpool3d_fwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 7 + [vp]
+    L.adaptive_maxpool3d_fwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 4 + [vp]
+    L.maxpool3d_bwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 10 + [vp]
     L.mp3d_status_string.argtypes = [i32]
     L.mp3d_status_string.restype = ctypes.c_char_p
     for f in (L.maxpool3d_fwd, L.adaptive_maxpool3d_fwd, L.maxpool3d_bwd, L.maxpool3d_fwd_plan,
               L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan, L.maxpool3d_fwd_ex,
               L.maxpool3d_bwd_ex, L.maxpool3d_fwd_ex_plan, L.maxpool3d_bwd_ex_plan,
-              L.maxpool3d_bwd_recompute, L.maxpool3d_bwd_recompute_plan):
+              L.maxpool3d_bwd_recompute, L.maxpool3d_bwd_recompute_plan, L.maxpool3d_fwd_ndhwc,
+              L.adaptive_maxpool3d_fwd_ndhwc, L.maxpool3d_bwd_ndhwc):
         f.restype = i32
     _lib = L
     return L
@@ -169,6 +174,42 @@ def maxpool3d_bwd_ex(grad_out, idx, grad_in, kernel, stride, padding=(0, 0, 0), 
                                     int(bool(ceil_mode)), _code(grad_out), algo, ws, wsb,
                                     _stream(grad_in, stream))
     _check(st, "maxpool3d_bwd_ex")
+
+
+def maxpool3d_fwd_ndhwc(x, y, idx, kernel, stride, stream=None):
+    """Channels-last fixed-window forward: x (N, D, H, W, C), y and idx
+    (N, OD, OH, OW, C); idx None: values only."""
+    _cuda(x, y, idx)
+    N, D, H, W, C = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().maxpool3d_fwd_ndhwc(x.data_ptr(), y.data_ptr(), _ptr(idx), N, C, D, H, W, *kernel,
+                                       *stride, _code(x), _stream(x, stream))
+    _check(st, "maxpool3d_fwd_ndhwc")
+
+
+def adaptive_maxpool3d_fwd_ndhwc(x, y, idx, out_size, stream=None):
+    """Channels-last adaptive-window forward."""
+    _cuda(x, y, idx)
+    N, D, H, W, C = x.shape
+    with torch.cuda.device(x.device):
+        st = lib().adaptive_maxpool3d_fwd_ndhwc(x.data_ptr(), y.data_ptr(), _ptr(idx), N, C, D, H, W,
+                                                *out_size, _code(x), _stream(x, stream))
+    _check(st, "adaptive_maxpool3d_fwd_ndhwc")
+
+
+def maxpool3d_bwd_ndhwc(grad_out, idx, grad_in, kernel=None, stride=None, stream=None):
+    """Channels-last backward: grad_out and idx (N, OD, OH, OW, C), grad_in
+    (N, D, H, W, C). kernel/stride None = adaptive windows."""
+    _cuda(grad_out, idx, grad_in)
+    N, D, H, W, C = grad_in.shape
+    od, oh, ow = grad_out.shape[1:4]
+    k = tuple(kernel) if kernel is not None else (0, 0, 0)
+    s = tuple(stride) if stride is not None else (0, 0, 0)
+    with torch.cuda.device(grad_in.device):
+        st = lib().maxpool3d_bwd_ndhwc(grad_out.data_ptr(), idx.data_ptr(), grad_in.data_ptr(), N, C,
+                                       D, H, W, od, oh, ow, *k, *s, _code(grad_out),
+                                       _stream(grad_in, stream))
+    _check(st, "maxpool3d_bwd_ndhwc")
 
 
 def maxpool3d_bwd_recompute(x, grad_out, grad_in, kernel=None, stride=None, stream=None):

@@ -3,6 +3,7 @@
 // Every argument error is reported before the first CUDA call, so a bad
 // call touches neither the device nor the buffers. The library allocates
 // nothing and never synchronises; it enqueues on the caller's stream.
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -50,6 +51,8 @@ const char* path_name(int path) {
     case MP3D_PATH_BWD_PADDED: return "bwd_padded";
     case MP3D_PATH_BWD_RECOMPUTE_TILES: return "bwd_recompute_k2s2";
     case MP3D_PATH_BWD_RECOMPUTE: return "bwd_recompute_direct";
+    case MP3D_PATH_FWD_NDHWC: return "fwd_ndhwc";
+    case MP3D_PATH_BWD_NDHWC: return "bwd_ndhwc";
     default: return "?";
     }
 }
@@ -530,6 +533,59 @@ int maxpool3d_bwd_recompute_plan(int64_t N, int64_t C, int64_t D, int64_t H, int
         *path = g.P == 0 ? MP3D_PATH_NOOP : tiles ? MP3D_PATH_BWD_RECOMPUTE_TILES : MP3D_PATH_BWD_RECOMPUTE;
     }
     return st;
+}
+
+// Channels-last entry points: the checks of the NCDHW ones (same byte
+// counts), then the channels-last kernels with the batch as the plane count.
+static int run_fwd_ndhwc(const void* x, void* y, int64_t* idx, Geo g, int64_t C, int dtype,
+                         cudaStream_t stream) {
+    if (g.P == 0) return MP3D_OK;
+    if (C > INT32_MAX) return MP3D_ERR_SHAPE;
+    g.P /= C;                                   // planes -> batch
+    log_path("fwd", MP3D_PATH_FWD_NDHWC, g, dtype);
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    return launch_fwd_ndhwc(x, y, idx, g, (int)C, dtype, sms, stream) == cudaSuccess ? MP3D_OK
+                                                                                     : MP3D_ERR_CUDA;
+}
+
+int maxpool3d_fwd_ndhwc(const void* x, void* y, int64_t* idx, int64_t N, int64_t C, int64_t D,
+                        int64_t H, int64_t W, int kd, int kh, int kw, int sd, int sh, int sw,
+                        int dtype, cudaStream_t stream) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = fixed_geo(&g, kd, kh, kw, sd, sh, sw);
+    if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
+    if (st) return st;
+    return run_fwd_ndhwc(x, y, idx, g, C, dtype, stream);
+}
+
+int adaptive_maxpool3d_fwd_ndhwc(const void* x, void* y, int64_t* idx, int64_t N, int64_t C,
+                                 int64_t D, int64_t H, int64_t W, int od, int oh, int ow, int dtype,
+                                 cudaStream_t stream) {
+    Geo g;
+    int st = check_dims(N, C, D, H, W, &g);
+    if (!st) st = adaptive_geo(&g, od, oh, ow);
+    if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
+    if (st) return st;
+    return run_fwd_ndhwc(x, y, idx, g, C, dtype, stream);
+}
+
+int maxpool3d_bwd_ndhwc(const void* grad_out, const int64_t* idx, void* grad_in, int64_t N,
+                        int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh, int ow, int kd,
+                        int kh, int kw, int sd, int sh, int sw, int dtype, cudaStream_t stream) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, MP3D_BWD_AUTO);
+    if (!st) st = check_bwd_buffers(grad_out, idx, grad_in, nullptr, 0, g, dtype, MP3D_BWD_AUTO);
+    if (st) return st;
+    if (g.P == 0) return MP3D_OK;
+    if (C > INT32_MAX) return MP3D_ERR_SHAPE;
+    g.P /= C;
+    log_path("bwd", MP3D_PATH_BWD_NDHWC, g, dtype);
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
+    return launch_bwd_ndhwc(grad_out, idx, grad_in, g, (int)C, dtype, sms, stream) == cudaSuccess
+               ? MP3D_OK : MP3D_ERR_CUDA;
 }
 
 int mp3d_device_error_flags(unsigned int* flags, int clear) {

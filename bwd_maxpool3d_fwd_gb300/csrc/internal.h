@@ -28,6 +28,12 @@ bool fwd_slab_supported(const Geo& g, int dtype);
 // input on a 16-byte boundary; plan queries assume an aligned buffer).
 bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16);
 
+// Channels-last layout (ndhwc.cu): g.P is the batch N, C the channel count.
+cudaError_t launch_fwd_ndhwc(const void* x, void* y, int64_t* idx, const Geo& g, int C, int dtype,
+                             int sms, cudaStream_t s);
+cudaError_t launch_bwd_ndhwc(const void* go, const int64_t* idx, void* gi, const Geo& g, int C,
+                             int dtype, int sms, cudaStream_t s);
+
 // Error flags set by kernels whose bounded waits gave up (fwd.cu).
 cudaError_t read_device_error(unsigned int* flags, bool clear);
 

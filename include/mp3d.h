@@ -84,6 +84,7 @@ typedef enum {
     MP3D_PATH_FWD_GLOBAL = 3,        /* one window per plane (global pool)    */
     MP3D_PATH_FWD_SLAB = 4,          /* window-depth slab staged in shared memory */
     MP3D_PATH_FWD_PADDED = 5,        /* padded / dilated windows, thread per output */
+    MP3D_PATH_FWD_NDHWC = 6,         /* channels-last layout                  */
     MP3D_PATH_BWD_DISJOINT = 10,     /* single-pass gather, disjoint windows  */
     MP3D_PATH_BWD_OVERLAP_TILE = 11, /* overlapping gather, staged tile + owner sums */
     MP3D_PATH_BWD_OVERLAP_DIRECT = 12, /* overlapping gather, direct reads    */
@@ -92,7 +93,8 @@ typedef enum {
                                         rolling ring of shared depth slices  */
     MP3D_PATH_BWD_PADDED = 15,       /* padded / dilated windows, direct gather */
     MP3D_PATH_BWD_RECOMPUTE_TILES = 16, /* no stored index, 2x2x2 tiling, fused */
-    MP3D_PATH_BWD_RECOMPUTE = 17     /* no stored index, direct form          */
+    MP3D_PATH_BWD_RECOMPUTE = 17,    /* no stored index, direct form          */
+    MP3D_PATH_BWD_NDHWC = 18         /* channels-last layout                  */
 } mp3d_path;
 
 /*
@@ -166,6 +168,31 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                        int od, int oh, int ow,
                        int kd, int kh, int kw, int sd, int sh, int sw,
                        int dtype, int algo, int* path);
+
+/*
+ * Channels-last (NDHWC) layout: x [N, D, H, W, C], y and idx
+ * [N, OD, OH, OW, C], grad_out like y, grad_in like x, all dense. Windows,
+ * ties, NaN rule, index form (the spatial offset d*H*W + h*W + w of the
+ * winner inside its own (n, c) volume) and the backward's order are those
+ * of maxpool3d_fwd / adaptive_maxpool3d_fwd / maxpool3d_bwd: the results
+ * are theirs with the channel axis moved last. Arguments and checks as for
+ * those entry points (idx may be NULL in the forwards); the backward takes
+ * no algorithm or workspace (gather form). Channel counts that are a
+ * multiple of 16 bytes' worth of elements, on 16-byte aligned buffers, use
+ * 16-byte accesses across channels; others take element accesses.
+ */
+int maxpool3d_fwd_ndhwc(const void* x, void* y, int64_t* idx,
+                        int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                        int kd, int kh, int kw, int sd, int sh, int sw,
+                        int dtype, cudaStream_t stream);
+int adaptive_maxpool3d_fwd_ndhwc(const void* x, void* y, int64_t* idx,
+                                 int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                                 int od, int oh, int ow, int dtype, cudaStream_t stream);
+int maxpool3d_bwd_ndhwc(const void* grad_out, const int64_t* idx, void* grad_in,
+                        int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                        int od, int oh, int ow,
+                        int kd, int kh, int kw, int sd, int sh, int sw,
+                        int dtype, cudaStream_t stream);
 
 /*
  * Backward without stored indices [AMPB]: the same grad_in as

@@ -573,3 +573,55 @@ def test_backward_recompute(case, dtype):
     mp.maxpool3d_bwd_recompute(x.to(DEV), g.to(DEV), gin, k, s)
     torch.cuda.synchronize()
     assert_bits_equal(gin.cpu(), ref, "grad_in (recomputed argmax)")
+
+
+# Channels-last layout: the NCDHW results (oracle) with the channel axis
+# moved last; 16-byte chunks across channels when C allows, element access
+# otherwise (odd C, or buffers one element off a 16-byte boundary).
+NDHWC_CASES = [
+    ((3, 3, 3), (2, 2, 2), None, (2, 9, 13, 11, 16)),
+    ((2, 2, 2), (2, 2, 2), None, (1, 8, 10, 12, 24)),
+    ((2, 3, 2), (1, 2, 3), None, (2, 7, 9, 10, 5)),         # odd channel count
+    (None, None, (4, 5, 3), (1, 10, 11, 9, 8)),             # adaptive, overlapping
+    (None, None, (1, 1, 1), (2, 4, 6, 5, 32)),              # global
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(NDHWC_CASES)))
+@pytest.mark.parametrize("offset", [0, 1], ids=["aligned", "offset"])
+def test_channels_last(case, dtype, offset):
+    k, s, out, shape = NDHWC_CASES[case]
+    gen = torch.Generator().manual_seed(9800 + case)
+    x = random_input(gen, shape, dtype, KINDS[case % 3])          # (N, D, H, W, C)
+    xc = x.permute(0, 4, 1, 2, 3).contiguous()                    # (N, C, D, H, W)
+    if k is not None:
+        y_ref, i_ref = oracle.maxpool3d_fwd(xc, k, s)
+    else:
+        y_ref, i_ref = oracle.adaptive_maxpool3d_fwd(xc, out)
+    oshape = (shape[0],) + tuple(y_ref.shape[2:]) + (shape[4],)
+
+    def buf(shp, dt):
+        n = 1
+        for v in shp:
+            n *= v
+        return torch.empty(n + offset, dtype=dt, device=DEV)[offset:].view(shp)
+
+    xd = buf(shape, dtype)
+    xd.copy_(x.to(DEV))
+    y, idx = buf(oshape, dtype), buf(oshape, torch.int64)
+    if k is not None:
+        mp.maxpool3d_fwd_ndhwc(xd, y, idx, k, s)
+    else:
+        mp.adaptive_maxpool3d_fwd_ndhwc(xd, y, idx, out)
+    torch.cuda.synchronize()
+    assert torch.equal(idx.cpu(), i_ref.permute(0, 2, 3, 4, 1))
+    assert_bits_equal(y.cpu(), y_ref.permute(0, 2, 3, 4, 1).contiguous(), "y (channels last)")
+    g = torch.randn(y_ref.shape, generator=gen).to(dtype)         # (N, C, OD, OH, OW)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[1:4])
+    gd = buf(oshape, dtype)
+    gd.copy_(g.permute(0, 2, 3, 4, 1).to(DEV))
+    gin = buf(shape, dtype)
+    mp.maxpool3d_bwd_ndhwc(gd, idx, gin, k, s)
+    torch.cuda.synchronize()
+    assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(), "grad_in (channels last)")
