@@ -339,6 +339,16 @@ int run_bwd(const void* grad_out, const int64_t* idx, void* grad_in, void* works
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
 }
 
+// Path of a padded / dilated backward: ATOMIC on request; the rolling
+// ordered scatter when it takes the geometry (no dilation, at most two
+// windows over any position); else the direct gather.
+int bwd_ex_path(const Geo& g, int dtype, int algo, bool aligned16 = true) {
+    if (g.P == 0) return MP3D_PATH_NOOP;
+    if (algo == MP3D_BWD_ATOMIC) return MP3D_PATH_BWD_ATOMIC;
+    if (bwd_roll_supported(g, dtype, aligned16)) return MP3D_PATH_BWD_OVERLAP_ROLL;
+    return MP3D_PATH_BWD_PADDED;
+}
+
 // Geometry of a padded / dilated backward call: the given output sizes must
 // be the ones the window yields.
 int bwd_ex_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh, int ow,
@@ -470,8 +480,7 @@ int maxpool3d_bwd_ex(const void* grad_out, const int64_t* idx, void* grad_in, in
     if (!st) st = check_bwd_buffers(grad_out, idx, grad_in, workspace, workspace_bytes, g, dtype, algo);
     if (st) return st;
     if (ex_is_plain(g)) return run_bwd(grad_out, idx, grad_in, workspace, g, dtype, algo, stream);
-    const int path = g.P == 0 ? MP3D_PATH_NOOP
-                     : algo == MP3D_BWD_ATOMIC ? MP3D_PATH_BWD_ATOMIC : MP3D_PATH_BWD_PADDED;
+    const int path = bwd_ex_path(g, dtype, algo, (uintptr_t)grad_in % 16 == 0);
     log_path("bwd", path, g, dtype);
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
     int sms = 0;
@@ -479,6 +488,8 @@ int maxpool3d_bwd_ex(const void* grad_out, const int64_t* idx, void* grad_in, in
     cudaError_t e;
     if (path == MP3D_PATH_BWD_ATOMIC)
         e = launch_bwd_atomic(grad_out, idx, grad_in, (float*)workspace, g, dtype, sms, stream);
+    else if (path == MP3D_PATH_BWD_OVERLAP_ROLL)
+        e = launch_bwd_roll(grad_out, idx, grad_in, g, dtype, sms, stream);
     else
         e = launch_bwd_ex_direct(grad_out, idx, grad_in, g, dtype, sms, stream);
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
@@ -493,8 +504,7 @@ int maxpool3d_bwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                         ceil_mode, dtype, algo);
     if (!st && path) {
         if (ex_is_plain(g)) *path = bwd_path(g, dtype, algo);
-        else *path = g.P == 0 ? MP3D_PATH_NOOP
-                     : algo == MP3D_BWD_ATOMIC ? MP3D_PATH_BWD_ATOMIC : MP3D_PATH_BWD_PADDED;
+        else *path = bwd_ex_path(g, dtype, algo);
     }
     return st;
 }

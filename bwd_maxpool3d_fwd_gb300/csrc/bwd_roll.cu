@@ -55,25 +55,28 @@ struct RollGeo {
 
 // Window arithmetic along one axis with the window kind known at compile
 // time (fixed: [o*S, o*S + K); adaptive: [floor(o*I/O), ceil((o+1)*I/O))).
+// Fixed windows may be padded: window o starts at o*S - pad (possibly
+// before the first position; only positions inside the input are ever
+// chosen).
 template <bool AD>
 __device__ __forceinline__ int ax_start(const AxisMap& a, int o) {
     if constexpr (AD) return a.fO.div(o * a.I);
-    else return o * a.S;
+    else return o * a.S - a.pad;
 }
 template <bool AD>
 __device__ __forceinline__ int ax_end(const AxisMap& a, int o) {
     if constexpr (AD) return a.fO.div((o + 1) * a.I + a.O - 1);
-    else return o * a.S + a.K;
+    else return o * a.S - a.pad + a.K;
 }
 template <bool AD>
 __device__ __forceinline__ int ax_lo(const AxisMap& a, int x) {
     if constexpr (AD) return a.fI.div(x * a.O);
-    else return x < a.K ? 0 : a.fS.div(x - a.K) + 1;
+    else return x + a.pad < a.K ? 0 : a.fS.div(x + a.pad - a.K) + 1;
 }
 template <bool AD>
 __device__ __forceinline__ int ax_hi(const AxisMap& a, int x) {
     if constexpr (AD) return a.fI.div((x + 1) * a.O - 1);
-    else return min(a.fS.div(x), a.O - 1);
+    else return min(a.fS.div(x + a.pad), a.O - 1);
 }
 
 // Whether every window that chose input j of plane p has a -0 gradient
@@ -194,12 +197,16 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
             rj[k] = in ? __ldg(ip + k * NT) : -1;
             rgd[k] = in ? gp[k * NT] : Elem<T>::from_f(0.0f);
         }
-        int ds = 0, sbase = 0;          // first slice of the row and its ring slot
+        int cs = 0, sbc = 0;            // first slice the row completes and its ring slot
         __syncthreads();   // the ring is clear (first unit: initialised) before any pass
         for (int od = 0; od < OD; ++od) {
-            const int de = ax_end<AD>(rg.ad, od);      // slices at or beyond de are in no window
-            const int kd = de - ds;
-            const int dsHW = ds * HW;
+            const int ods = ax_start<AD>(rg.ad, od);   // window origin (before 0 when padded)
+            const int oe = ax_end<AD>(rg.ad, od);
+            const int kd = oe - ods;                   // window length along d
+            const int de = min(oe, g.D);               // slices at or beyond de are in no window
+            int sbo = ods % RS;                        // ring slot of the origin
+            sbo += sbo < 0 ? RS : 0;
+            const int dsHW = ods * HW;
             const int pvt = pv + dsHW + h0W;
             // 1. decode this row (key 4: the window adds nothing here);
             //    mark inputs reached by -0 gradients
@@ -226,7 +233,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 const int loc = wo[k] - h0W + rem;      // place inside the h-tile's rows
                 const bool ok = (uint64_t)j < (uint64_t)g.vol && rel >= 0 && offd < kd && offh < kh &&
                                 offw < kw && (unsigned)loc < (unsigned)L;
-                int slot = sbase + offd;
+                int slot = sbo + offd;
                 slot -= slot >= RS ? RS : 0;
                 const int ph = AL ? 0 : (pvt + offd * HW) & (VEC - 1);
                 off[k] = (slot * SSTR + ph + loc) * (int)sizeof(float);
@@ -260,18 +267,18 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     }
                 __syncthreads();
             }
-            // 3. round and store the completed slices [ds, dn), clear their accumulators
-            const int dn = od + 1 < OD ? ax_start<AD>(rg.ad, od + 1) : g.D;
-            const int nring = min(dn, de) - ds;        // completed slices held in the ring
-            const int stored = ((1 << nring) - 1) << sbase | ((1 << nring) - 1) >> (RS - sbase);
+            // 3. round and store the completed slices [cs, dn), clear their accumulators
+            const int dn = od + 1 < OD ? max(ax_start<AD>(rg.ad, od + 1), 0) : g.D;
+            const int nring = min(dn, de) - cs;        // completed slices held in the ring
+            const int stored = ((1 << nring) - 1) << sbc | ((1 << nring) - 1) >> (RS - sbc);
             const int marked = *slotmask & stored;
             if (marked) {
                 // inputs chosen only by -0 gradients: accumulator +0 -> -0
                 for (int s = 0; s < nring; ++s) {
-                    int slot = sbase + s;
+                    int slot = sbc + s;
                     slot -= slot >= RS ? RS : 0;
                     if (!((marked >> slot) & 1)) continue;
-                    const int off0 = (ds + s) * HW + h0W;
+                    const int off0 = (cs + s) * HW + h0W;
                     const int ph = AL ? 0 : (pv + off0) & (VEC - 1);
                     for (int i = tid; i < SSTR / 32; i += NT) {
                         unsigned m = negbits[slot * (SSTR / 32) + i];
@@ -290,10 +297,10 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 if (tid == 0) *slotmask &= ~stored;
             }
             if constexpr (AL) {
-                for (int s = 0; s < dn - ds; ++s) {
-                    T* dst = gplane + (ds + s) * HW + h0W;     // on a 16-byte boundary
+                for (int s = 0; s < dn - cs; ++s) {
+                    T* dst = gplane + (cs + s) * HW + h0W;     // on a 16-byte boundary
                     const bool cov = s < nring;
-                    int slot = sbase + s;
+                    int slot = sbc + s;
                     slot -= slot >= RS ? RS : 0;
                     float* src = ring + slot * SSTR;
                     for (int c = tid; c < L / VEC; c += NT) {
@@ -303,13 +310,13 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     }
                 }
             }
-            for (int s = 0; !AL && s < dn - ds; ++s) {
-                const int off0 = (ds + s) * HW + h0W;
+            for (int s = 0; !AL && s < dn - cs; ++s) {
+                const int off0 = (cs + s) * HW + h0W;
                 const int ph = (pv + off0) & (VEC - 1);
                 T* dst = gplane + (off0 - ph);          // on a 16-byte boundary
                 const int nch = (ph + L + VEC - 1) / VEC;
                 const bool cov = s < nring;
-                int slot = sbase + s;
+                int slot = sbc + s;
                 slot -= slot >= RS ? RS : 0;
                 float* src = ring + slot * SSTR;
                 for (int c = tid; c < nch; c += NT) {
@@ -326,10 +333,10 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     }
                 }
             }
-            // the next row starts at dn; its slot follows
-            sbase += dn - ds;
-            while (sbase >= RS) sbase -= RS;
-            ds = dn;
+            // the next row completes from dn; its slot follows
+            sbc += dn - cs;
+            while (sbc >= RS) sbc -= RS;
+            cs = dn;
             __syncthreads();
         }
     }
@@ -343,17 +350,18 @@ namespace {
 struct HostAxis {
     int I, O, K, S;
     bool adaptive;
-    long long start(int o) const { return adaptive ? (long long)o * I / O : (long long)o * S; }
+    int pad;      // fixed windows: window o starts at o*S - pad
+    long long start(int o) const { return adaptive ? (long long)o * I / O : (long long)o * S - pad; }
     long long end(int o) const {
-        return adaptive ? ((long long)(o + 1) * I + O - 1) / O : (long long)o * S + K;
+        return adaptive ? ((long long)(o + 1) * I + O - 1) / O : (long long)o * S - pad + K;
     }
     int lo(int x) const {
         if (adaptive) return (int)((long long)x * O / I);
-        return x < K ? 0 : (x - K) / S + 1;
+        return x + pad < K ? 0 : (x + pad - K) / S + 1;
     }
     int hi(int x) const {
         if (adaptive) return (int)(((long long)(x + 1) * O - 1) / I);
-        const int h = x / S;
+        const int h = (x + pad) / S;
         return h < O - 1 ? h : O - 1;
     }
     // At most two windows cover any position.
@@ -371,9 +379,9 @@ struct HostAxis {
     }
 };
 
-HostAxis host_axis(int I, int O, int K, int S, bool adaptive) {
+HostAxis host_axis(int I, int O, int K, int S, bool adaptive, int pad = 0) {
     HostAxis a;
-    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive;
+    a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive; a.pad = adaptive ? 0 : pad;
     return a;
 }
 
@@ -413,9 +421,12 @@ bool roll_plan(const Geo& g, int es, long long min_units, const RollCfg& cfg, Ro
             return false;
         if (g.OD > (1 << 20) || g.OH > (1 << 20) || g.OW > (1 << 20)) return false;
     }
-    const HostAxis ad = host_axis(g.D, g.OD, g.kd, g.sd, a);
-    const HostAxis ah = host_axis(g.H, g.OH, g.kh, g.sh, a);
-    const HostAxis aw = host_axis(g.W, g.OW, g.kw, g.sw, a);
+    if (!a && (g.dd != 1 || g.dh != 1 || g.dw != 1)) return false;      // no dilation
+    if (!a && (g.pd || g.ph || g.pw) && (g.kd > g.D || g.kh > g.H || g.kw > g.W))
+        return false;      // padded windows no longer than the input (offsets decode per axis)
+    const HostAxis ad = host_axis(g.D, g.OD, g.kd, g.sd, a, g.pd);
+    const HostAxis ah = host_axis(g.H, g.OH, g.kh, g.sh, a, g.ph);
+    const HostAxis aw = host_axis(g.W, g.OW, g.kw, g.sw, a, g.pw);
     if (!ad.two_cover() || !ah.two_cover() || !aw.two_cover()) return false;
     const int vec = 16 / es;
     const int RS = ad.longest();
@@ -451,9 +462,9 @@ bool roll_plan(const Geo& g, int es, long long min_units, const RollCfg& cfg, Ro
         rg->nht = nht;
         rg->RS = RS;
         rg->SSTR = (int)SSTR;
-        rg->ad = axis_map(g.D, g.OD, g.kd, g.sd, a);
-        rg->ah = axis_map(g.H, g.OH, g.kh, g.sh, a);
-        rg->aw = axis_map(g.W, g.OW, g.kw, g.sw, a);
+        rg->ad = axis_map(g.D, g.OD, g.kd, g.sd, a, g.pd);
+        rg->ah = axis_map(g.H, g.OH, g.kh, g.sh, a, g.ph);
+        rg->aw = axis_map(g.W, g.OW, g.kw, g.sw, a, g.pw);
         rg->fHW = FastDiv((uint32_t)(g.H * g.W));
         rg->fW = FastDiv((uint32_t)g.W);
         rg->fOW = FastDiv((uint32_t)g.OW);
@@ -485,7 +496,8 @@ cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, i
     int wpt = 0;
     // one wave of CTAs at minb per SM
     const bool k3 = !g.adaptive && g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 &&
-                    g.sw == 2 && g.W % VEC == 0 && g.vol % VEC == 0;
+                    g.sw == 2 && g.pd == 0 && g.ph == 0 && g.pw == 0 && g.W % VEC == 0 &&
+                    g.vol % VEC == 0;
     if (k3 && roll_plan(g, sizeof(T), 1LL * sms * kRollCfgK3.minb, kRollCfgK3, &rg, &smem, &wpt) &&
         wpt == 4)
         return roll_launch<T, false, 4, true, true>(go, idx, gi, g, rg, smem, s);

@@ -104,6 +104,7 @@ struct FastDiv {
 struct AxisMap {
     int I, O, K, S;
     int adaptive;
+    int pad;      // fixed windows: padding before the first position (window o starts at o*S - pad)
     FastDiv fS;   // fixed: divide by S
     FastDiv fI;   // adaptive: divide by I
     FastDiv fO;   // adaptive: divide by O
@@ -133,9 +134,10 @@ struct AxisMap {
 };
 
 // Host-side construction of an AxisMap.
-inline AxisMap axis_map(int I, int O, int K, int S, bool adaptive) {
+inline AxisMap axis_map(int I, int O, int K, int S, bool adaptive, int pad = 0) {
     AxisMap a;
     a.I = I; a.O = O; a.K = K; a.S = S; a.adaptive = adaptive ? 1 : 0;
+    a.pad = adaptive ? 0 : pad;
     a.fS = FastDiv((uint32_t)(S > 0 ? S : 1));
     a.fI = FastDiv((uint32_t)I);
     a.fO = FastDiv((uint32_t)O);

@@ -55,8 +55,9 @@ extern "C" {
 
 typedef enum { MP3D_F32 = 0, MP3D_F16 = 1, MP3D_BF16 = 2 } mp3d_dtype;
 
-/* Backward algorithm. AUTO picks the gather (disjoint or overlapping) from
- * the shape; GATHER forces the deterministic gather; ATOMIC runs the
+/* Backward algorithm. AUTO and GATHER both pick a deterministic form (a
+ * gather, or the ordered rolling scatter, from the shape) whose sums are
+ * bit-identical to the ordered definition; ATOMIC runs the
  * ablation of [AMPB]'s non-divisible path: zero fill, atomicAdd scatter in
  * binary32 and, for f16/bf16, a final rounding pass. */
 typedef enum { MP3D_BWD_AUTO = 0, MP3D_BWD_GATHER = 1, MP3D_BWD_ATOMIC = 2 } mp3d_bwd_algo;

@@ -209,9 +209,14 @@ def test_padded_plans(L):
                                     False, f16) == "fwd_padded"
     assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1),
                                     False, f32) == "fwd_padded"
+    # backward: padding alone keeps the rolling ordered scatter, dilation
+    # takes the direct gather
     out = mp.pool_out_size_ex((8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1))
     assert mp.maxpool3d_bwd_ex_plan((2, 3, 8, 9, 10), out, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
-                                    False, f16) == "bwd_padded"
+                                    False, f16) == "bwd_overlap_roll"
+    out_dl = mp.pool_out_size_ex((8, 9, 10), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1))
+    assert mp.maxpool3d_bwd_ex_plan((2, 3, 8, 9, 10), out_dl, (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1),
+                                    False, f32) == "bwd_padded"
     assert mp.maxpool3d_bwd_ex_plan((2, 3, 8, 9, 10), out, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
                                     False, f16, mp.BWD_ATOMIC) == "bwd_atomic"
     # the plain geometry keeps its fast paths

@@ -477,8 +477,8 @@ def test_values_only_forward(case):
     assert_bits_equal(y.cpu(), y_ref, "y (values only)")
 
 
-# Padding, dilation and ceil mode: forward values and indices, the direct
-# gather backward bit for bit, and the atomic form within its tolerance.
+# Padding, dilation and ceil mode: forward values and indices, the ordered
+# backward bit for bit, and the atomic form within its tolerance.
 PADDED_CASES = [
     ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (2, 3, 9, 20, 33)),
     ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), True, (1, 2, 8, 17, 30)),
@@ -487,6 +487,7 @@ PADDED_CASES = [
     ((2, 3, 2), (2, 1, 3), (0, 1, 1), (3, 2, 1), True, (2, 2, 10, 9, 23)),
     ((2, 2, 2), (2, 2, 2), (0, 0, 0), (1, 1, 1), True, (1, 2, 9, 9, 9)),       # ceil adds a window
     ((4, 4, 4), (3, 3, 3), (2, 2, 2), (1, 1, 1), True, (1, 2, 11, 14, 19)),
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (1, 2, 6, 112, 112)),  # wide planes
 ]
 
 
@@ -523,7 +524,10 @@ def test_padded_fwd_bwd(case, dtype):
     assert_bits_equal(y, y_ref, "y (padded)")
     g = torch.randn(y_ref.shape, generator=gen).to(dtype)
     gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
-    assert mp.maxpool3d_bwd_ex_plan(shape, y_ref.shape[2:], k, s, p, dl, cm, dtype) == "bwd_padded"
+    # undilated windows take the rolling ordered scatter, dilated ones the
+    # direct gather; both are bit-exact
+    want = "bwd_overlap_roll" if dl == (1, 1, 1) else "bwd_padded"
+    assert mp.maxpool3d_bwd_ex_plan(shape, y_ref.shape[2:], k, s, p, dl, cm, dtype) == want
     assert_bits_equal(_gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm), gin_ref, "grad_in (padded)")
     gin_a = _gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm, algo=mp.BWD_ATOMIC)
     assert _atomic_tolerance_ok(gin_a, gin_ref, g, i_ref, dtype)
