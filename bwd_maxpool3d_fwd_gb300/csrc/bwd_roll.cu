@@ -112,9 +112,15 @@ template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float a, fl
     return *reinterpret_cast<const unsigned*>(&h);
 }
 
-// One 16-byte output chunk from the accumulators at src (reset to +0).
+// One 16-byte output chunk c from its accumulators at src (reset to +0).
+// For 16-bit types a chunk is 32 bytes of accumulators, read and cleared as
+// two 16-byte halves. Taken in the same order by every thread, eight
+// neighbouring chunks would put their halves two to a bank group; chunks
+// with bit 2 of c set take the upper half first, so each quarter-warp's
+// accesses cover all eight 16-byte bank groups once (the chunks a warp
+// handles together are consecutive).
 template <typename T>
-__device__ __forceinline__ uint4 roll_take(float* src) {
+__device__ __forceinline__ uint4 roll_take(float* src, int c) {
     float4* s4 = reinterpret_cast<float4*>(src);
     uint4 out;
     if constexpr (sizeof(T) == 4) {
@@ -123,11 +129,13 @@ __device__ __forceinline__ uint4 roll_take(float* src) {
         out = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z),
                          __float_as_uint(a.w));
     } else {
-        const float4 a = s4[0], b = s4[1];
-        s4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        s4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        out = make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y),
-                         pack2<T>(b.z, b.w));
+        const int f = (c >> 2) & 1;
+        const float4 a = s4[f], b = s4[f ^ 1];
+        s4[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+        s4[f ^ 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const unsigned a0 = pack2<T>(a.x, a.y), a1 = pack2<T>(a.z, a.w);
+        const unsigned b0 = pack2<T>(b.x, b.y), b1 = pack2<T>(b.z, b.w);
+        out = f ? make_uint4(b0, b1, a0, a1) : make_uint4(a0, a1, b0, b1);
     }
     return out;
 }
@@ -305,7 +313,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     float* src = ring + slot * SSTR;
                     for (int c = tid; c < L / VEC; c += NT) {
                         uint4 out = make_uint4(0u, 0u, 0u, 0u);
-                        if (cov) out = roll_take<T>(src + c * VEC);
+                        if (cov) out = roll_take<T>(src + c * VEC, c);
                         *reinterpret_cast<uint4*>(dst + c * VEC) = out;
                     }
                 }
@@ -322,7 +330,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 for (int c = tid; c < nch; c += NT) {
                     const int e0 = c * VEC - ph;
                     Vec16<T> out;
-                    if (cov) out.u = roll_take<T>(src + c * VEC);
+                    if (cov) out.u = roll_take<T>(src + c * VEC, c);
                     else out.u = make_uint4(0u, 0u, 0u, 0u);
                     if (e0 >= 0 && e0 + VEC <= L) {
                         *reinterpret_cast<uint4*>(dst + c * VEC) = out.u;
