@@ -112,15 +112,15 @@ template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float a, fl
     return *reinterpret_cast<const unsigned*>(&h);
 }
 
-// One 16-byte output chunk c from its accumulators at src (reset to +0).
+// One 16-byte output chunk from its accumulators at src (reset to +0).
 // For 16-bit types a chunk is 32 bytes of accumulators, read and cleared as
 // two 16-byte halves. Taken in the same order by every thread, eight
-// neighbouring chunks would put their halves two to a bank group; chunks
-// with bit 2 of c set take the upper half first, so each quarter-warp's
-// accesses cover all eight 16-byte bank groups once (the chunks a warp
-// handles together are consecutive).
+// neighbouring chunks would put their halves two to a bank group; with
+// f = bit 2 of the chunk's place in its warp (lanes 4-7 of each
+// quarter-warp take the upper half first), each quarter-warp's accesses
+// cover all eight 16-byte bank groups once.
 template <typename T>
-__device__ __forceinline__ uint4 roll_take(float* src, int c) {
+__device__ __forceinline__ uint4 roll_take(float* src, int f) {
     float4* s4 = reinterpret_cast<float4*>(src);
     uint4 out;
     if constexpr (sizeof(T) == 4) {
@@ -129,7 +129,6 @@ __device__ __forceinline__ uint4 roll_take(float* src, int c) {
         out = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z),
                          __float_as_uint(a.w));
     } else {
-        const int f = (c >> 2) & 1;
         const float4 a = s4[f], b = s4[f ^ 1];
         s4[f] = make_float4(0.f, 0.f, 0.f, 0.f);
         s4[f ^ 1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -149,12 +148,14 @@ __global__ void __launch_bounds__(NT, MINB)
 k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
            RollGeo rg) {
     constexpr int VEC = 16 / sizeof(T);
+    static_assert(NT % 32 == 0, "the store's chunk c and its thread share lane bits");
     extern __shared__ __align__(16) float ring[];
     const int RS = rg.RS, SSTR = rg.SSTR;
     const int nacc = RS * SSTR;
     unsigned* negbits = reinterpret_cast<unsigned*>(ring + nacc);   // one bit per accumulator
     int* slotmask = reinterpret_cast<int*>(negbits + nacc / 32);    // slots holding a set bit
     const int tid = threadIdx.x;
+    const int fh = (tid >> 2) & 1;       // half order of this thread's store chunks
     const int W = g.W, HW = g.H * g.W, OW = g.OW, OD = g.OD;
     {
         float4* r4 = reinterpret_cast<float4*>(ring);
@@ -313,7 +314,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     float* src = ring + slot * SSTR;
                     for (int c = tid; c < L / VEC; c += NT) {
                         uint4 out = make_uint4(0u, 0u, 0u, 0u);
-                        if (cov) out = roll_take<T>(src + c * VEC, c);
+                        if (cov) out = roll_take<T>(src + c * VEC, fh);
                         *reinterpret_cast<uint4*>(dst + c * VEC) = out;
                     }
                 }
@@ -330,7 +331,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 for (int c = tid; c < nch; c += NT) {
                     const int e0 = c * VEC - ph;
                     Vec16<T> out;
-                    if (cov) out.u = roll_take<T>(src + c * VEC, c);
+                    if (cov) out.u = roll_take<T>(src + c * VEC, fh);
                     else out.u = make_uint4(0u, 0u, 0u, 0u);
                     if (e0 >= 0 && e0 + VEC <= L) {
                         *reinterpret_cast<uint4*>(dst + c * VEC) = out.u;
@@ -407,7 +408,7 @@ struct RollCfg {
 // 896 slots rather than 1024; measured 631 us against 658 us on the
 // 32x128x16x112x112 fp16 backward).
 constexpr RollCfg kRollCfg = {256, 4, 4, 54 * 1024};
-constexpr RollCfg kRollCfgK3 = {224, 4, 4, 54 * 1024};
+constexpr RollCfg kRollCfgK3 = {192, 4, 5, 44 * 1024};
 
 size_t roll_smem(int RS, int SSTR) {
     const size_t nacc = (size_t)RS * SSTR;

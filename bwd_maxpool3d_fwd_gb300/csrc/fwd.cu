@@ -219,6 +219,148 @@ k_fwd_slab(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     }
 }
 
+// ------------------------------------------------------------ keyed slab
+// 16-bit types: the slab of one (plane, od) is staged as one 32-bit word
+// per element whose unsigned order is the scan's preference, so that the
+// winner of a window is the plain unsigned maximum of its words.
+//   high half: an order key of the value: +0 and -0 the same key, negative
+//              values below positive ones by magnitude, every NaN above
+//              +inf (all NaNs one key);
+//   low half:  0xFFFF minus the element's offset in the slab, so that among
+//              equal keys (equal values, or NaNs) the earliest in (d, h, w)
+//              order is the largest word.
+// This is the rule of the scan ("beats": strictly greater, or a NaN over a
+// number; the first occurrence kept) as one total order. The value written
+// to y is re-read from x at the winning offset, so its bits (sign of zero,
+// NaN payload) are the input element's.
+
+// Two 16-bit values (one per half of w) -> their order keys, half by half.
+// NANADD = 0x7FFF - (largest non-NaN magnitude): bit 15 of mag + NANADD is
+// set exactly for NaN magnitudes.
+template <unsigned NANADD>
+__device__ __forceinline__ unsigned order_keys2(unsigned w) {
+    const unsigned mag = w & 0x7FFF7FFFu;
+    unsigned neg, nan;
+    // prmt with selector nibbles 9 / B: each result byte is the sign of
+    // byte 1 (low half) or byte 3 (high half), replicated
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(nan) : "r"(mag + NANADD * 0x10001u));
+    const unsigned up = 0x80008000u + mag, down = 0x80008000u - mag;   // no carry between halves
+    return (down & neg) | (up & ~neg) | nan;
+}
+
+template <typename T> struct KeyConst;
+template <> struct KeyConst<__half> { static constexpr unsigned nanadd = 0x7FFFu - 0x7C00u; };
+template <> struct KeyConst<__nv_bfloat16> { static constexpr unsigned nanadd = 0x7FFFu - 0x7F80u; };
+
+template <typename T>
+__device__ __forceinline__ unsigned order_word(unsigned short b, int e) {
+    const unsigned k = order_keys2<KeyConst<T>::nanadd>(b) & 0xFFFFu;
+    return k << 16 | (0xFFFFu - (unsigned)e);
+}
+
+constexpr int KS_NT = 256;
+
+// KH, KW > 0: every window along h (w) is exactly KH (KW) long, and the
+// window scan unrolls; 0: lengths read from the tables.
+template <typename T, bool ADAPTIVE, int KH, int KW>
+__global__ void __launch_bounds__(KS_NT)
+k_fwd_keyslab(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
+              int nwords, FastDiv fnout, FastDiv fOW) {
+    // shared: the slab words (nwords, a multiple of 32), the winning word of
+    // each output of the plane-depth, the window rows of each oh and the
+    // window columns of each ow
+    extern __shared__ __align__(128) unsigned smem_ks[];
+    constexpr int VEC = 8;                       // 16-bit elements per 16-byte load
+    constexpr unsigned NANADD = KeyConst<T>::nanadd;
+    const int od = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int HW = g.H * g.W;
+    const int nout = g.OH * g.OW;
+    unsigned* words = smem_ks;                                // [nwords]
+    unsigned* win = words + nwords;                           // [OH*OW]
+    int2* htab = reinterpret_cast<int2*>(win + ((nout + 1) & ~1));   // [OH] (hs, he)
+    int2* wtab = htab + g.OH;                                 // [OW] (ws, we)
+    for (int i = tid; i < g.OH; i += KS_NT)
+        htab[i] = make_int2(win_start(i, g.H, g.OH, g.kh, g.sh, ADAPTIVE),
+                            win_end(i, g.H, g.OH, g.kh, g.sh, ADAPTIVE));
+    for (int i = tid; i < g.OW; i += KS_NT)
+        wtab[i] = make_int2(win_start(i, g.W, g.OW, g.kw, g.sw, ADAPTIVE),
+                            win_end(i, g.W, g.OW, g.kw, g.sw, ADAPTIVE));
+    for (int i = tid; i < nout; i += KS_NT) win[i] = 0u;
+    const int ds = win_start(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int de = win_end(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+    const int nd = de - ds;
+    const int n = nd * HW;                       // slab elements (<= 65536)
+    for (long long p = blockIdx.y; p < g.P; p += gridDim.y) {
+        const T* src = x + p * g.vol + (long long)ds * HW;
+        const unsigned short* sb = reinterpret_cast<const unsigned short*>(src);
+        const int mis = (int)(((uintptr_t)src % 16) / sizeof(T));   // elements before a 16-byte boundary
+        unsigned* wl = words + mis;              // wl[e] = word of slab element e
+        const int head = mis ? min(VEC - mis, n) : 0;
+        const int nvec = (n - head) / VEC;
+        const uint4* gv = reinterpret_cast<const uint4*>(src + head);
+        // U loads per thread in flight together, then their words
+        constexpr int U = 8;
+        for (int c0 = tid; c0 < nvec; c0 += U * KS_NT) {
+            uint4 u[U];
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+                if (c0 + i * KS_NT < nvec) u[i] = __ldg(gv + c0 + i * KS_NT);
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                const int c = c0 + i * KS_NT;
+                if (c >= nvec) break;
+                const unsigned k0 = order_keys2<NANADD>(u[i].x), k1 = order_keys2<NANADD>(u[i].y);
+                const unsigned k2 = order_keys2<NANADD>(u[i].z), k3 = order_keys2<NANADD>(u[i].w);
+                const unsigned inv = 0xFFFFu - (unsigned)(head + c * VEC);   // low half of element 0
+                // word of element j: key j in the high half, inv - j in the low half
+                const uint4 lo = make_uint4(__byte_perm(k0, inv, 0x1054), __byte_perm(k0, inv - 1, 0x3254),
+                                            __byte_perm(k1, inv - 2, 0x1054), __byte_perm(k1, inv - 3, 0x3254));
+                const uint4 hi = make_uint4(__byte_perm(k2, inv - 4, 0x1054), __byte_perm(k2, inv - 5, 0x3254),
+                                            __byte_perm(k3, inv - 6, 0x1054), __byte_perm(k3, inv - 7, 0x3254));
+                uint4* dst = reinterpret_cast<uint4*>(wl + head + c * VEC);   // 16-byte aligned
+                dst[0] = lo;
+                dst[1] = hi;
+            }
+        }
+        for (int e = tid; e < head; e += KS_NT) wl[e] = order_word<T>(sb[e], e);
+        for (int e = head + nvec * VEC + tid; e < n; e += KS_NT) wl[e] = order_word<T>(sb[e], e);
+        __syncthreads();
+        // one item per (d, oh, ow): the best word of that depth row of the
+        // window; the items of a window meet in an unsigned max (the word
+        // order does not depend on the order they arrive in)
+        for (int t = tid; t < nd * nout; t += KS_NT) {
+            const int d = fnout.div(t);
+            const int o = t - d * nout;
+            const int oh = fOW.div(o), ow = o - oh * g.OW;
+            const int2 hr = htab[oh], wr = wtab[ow];
+            unsigned best = 0u;                  // every word is above 0 (keys are at least 0x80)
+            const unsigned* base = wl + d * HW + hr.x * g.W + wr.x;
+            if constexpr (KH > 0 && KW > 0) {
+#pragma unroll
+                for (int h = 0; h < KH; ++h)
+#pragma unroll
+                    for (int w = 0; w < KW; ++w) best = max(best, base[h * g.W + w]);
+            } else {
+                for (int h = 0; h < hr.y - hr.x; ++h)
+                    for (int w = 0; w < wr.y - wr.x; ++w) best = max(best, base[h * g.W + w]);
+            }
+            atomicMax(win + o, best);
+        }
+        __syncthreads();
+        const long long obase = ((p * g.OD + od) * (long long)g.OH) * g.OW;
+        for (int t = tid; t < nout; t += KS_NT) {
+            const unsigned best = win[t];
+            win[t] = 0u;                         // ready for the next plane
+            const int off = (int)(0xFFFFu - (best & 0xFFFFu));
+            y[obase + t] = src[off];
+            if (idx) idx[obase + t] = (int64_t)ds * HW + off;
+        }
+        __syncthreads();
+    }
+}
+
 static constexpr int kSlabBytes = 96 * 1024;
 
 // Deepest window along D (slices the slab must hold).
@@ -238,8 +380,67 @@ bool fwd_slab_supported(const Geo& g, int dtype) {
     return (long long)max_depth(g) * g.H * g.W * es + 16 <= kSlabBytes;
 }
 
+// The keyed form: 16-bit types, slab offsets that fit the low half of a
+// word, and four bytes per slab element in shared memory.
+static constexpr int kKeySlabBytes = 100 * 1024;
+// Slab words: the deepest slab plus up to 7 elements before a 16-byte
+// boundary, rounded up to 32.
+static int keyslab_words(const Geo& g) {
+    return (int)(((long long)max_depth(g) * g.H * g.W + 7 + 31) / 32 * 32);
+}
+static size_t keyslab_smem(const Geo& g) {
+    const long long nout = (long long)g.OH * g.OW;
+    return (size_t)(4LL * keyslab_words(g) + 4 * ((nout + 1) / 2 * 2) + 8LL * (g.OH + g.OW));
+}
+static bool keyslab_fits(const Geo& g) {
+    const long long n = (long long)max_depth(g) * g.H * g.W;
+    return n <= 65536 && (long long)g.OH + g.OW <= 4096 && (long long)g.OH * g.OW <= 8192 &&
+           keyslab_smem(g) <= (size_t)kKeySlabBytes;
+}
+
+// The one window length along an axis, or 0 when lengths differ.
+static int uniform_len(int I, int O, int K, bool adaptive) {
+    if (!adaptive) return K;
+    int len = -1;
+    for (int i = 0; i < O; ++i) {
+        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
+        if (len >= 0 && l != len) return 0;
+        len = l;
+    }
+    return len;
+}
+
+template <typename T, bool AD>
+static auto keyslab_kernel(int kh, int kw) {
+    if (kh == kw) {
+        switch (kh) {
+        case 2: return k_fwd_keyslab<T, AD, 2, 2>;
+        case 3: return k_fwd_keyslab<T, AD, 3, 3>;
+        case 4: return k_fwd_keyslab<T, AD, 4, 4>;
+        case 5: return k_fwd_keyslab<T, AD, 5, 5>;
+        default: break;
+        }
+    }
+    return k_fwd_keyslab<T, AD, 0, 0>;
+}
+
+template <typename T>
+static cudaError_t keyslab_t(const void* x, void* y, int64_t* idx, const Geo& g, cudaStream_t s) {
+    const size_t smem = keyslab_smem(g);
+    dim3 grid((unsigned)g.OD, (unsigned)(g.P < 65535 ? g.P : 65535));
+    const int kh = uniform_len(g.H, g.OH, g.kh, g.adaptive), kw = uniform_len(g.W, g.OW, g.kw, g.adaptive);
+    auto kern = g.adaptive ? keyslab_kernel<T, true>(kh, kw) : keyslab_kernel<T, false>(kh, kw);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, KS_NT, smem, s>>>((const T*)x, (T*)y, idx, g, keyslab_words(g),
+                                   FastDiv((uint32_t)(g.OH * g.OW)), FastDiv((uint32_t)g.OW));
+    return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t fwd_slab_t(const void* x, void* y, int64_t* idx, const Geo& g, cudaStream_t s) {
+    if constexpr (sizeof(T) == 2)
+        if (keyslab_fits(g)) return keyslab_t<T>(x, y, idx, g, s);
     const size_t smem = (size_t)max_depth(g) * g.H * g.W * sizeof(T) + 16;
     dim3 grid((unsigned)g.OD, (unsigned)(g.P < 65535 ? g.P : 65535));
     if (g.adaptive) {

@@ -452,6 +452,8 @@ VALUES_ONLY = [
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 8, 6, 32), torch.bfloat16),    # 2x2x2 tiling
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 9, 7, 32), torch.float16),
     ("fwd_slab", None, None, (5, 4, 8), (2, 2, 9, 7, 13), torch.float32),
+    ("fwd_slab", None, None, (8, 12, 12), (1, 3, 30, 50, 50), torch.float16),     # keyed slab
+    ("fwd_slab", None, None, (3, 4, 5), (2, 3, 7, 9, 13), torch.bfloat16),
     ("fwd_generic", (5, 5, 5), (3, 3, 3), None, (1, 1, 8, 120, 120), torch.float32),
     ("fwd_global", None, None, (1, 1, 1), (1, 3, 8, 14, 14), torch.float32),
 ]
@@ -629,3 +631,45 @@ def test_channels_last(case, dtype, offset):
     mp.maxpool3d_bwd_ndhwc(gd, idx, gin, k, s)
     torch.cuda.synchronize()
     assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(), "grad_in (channels last)")
+
+
+# The slab forward for 16-bit types ranks elements by one unsigned word
+# (value order key, then earliest offset). Arbitrary bit patterns pin that
+# order against the scan's rule: NaNs of either sign and any payload (the
+# first NaN wins), +0 against -0 (the first wins), subnormals, +-inf. Slab
+# starts off a 16-byte boundary take the element-wise head and tail.
+ANY_BITS_CASES = [
+    ((2, 3, 30, 50, 50), (8, 12, 12)),
+    ((2, 3, 7, 9, 13), (3, 4, 5)),
+    ((1, 2, 5, 3, 3), (5, 3, 3)),       # one-element windows
+    ((3, 1, 6, 6, 6), (1, 1, 1)),       # one window over a whole plane
+]
+
+
+def _any_bits(gen, shape, dtype, nan_share):
+    b = torch.randint(0, 1 << 16, shape, generator=gen, dtype=torch.int32)
+    if nan_share:
+        exp_bits = 0x7C00 if dtype == torch.float16 else 0x7F80
+        mant = (~exp_bits) & 0x7FFF
+        nan = (torch.randint(0, 2, shape, generator=gen, dtype=torch.int32) << 15) | exp_bits | \
+            (torch.randint(1, mant + 1, shape, generator=gen, dtype=torch.int32))
+        pick = torch.rand(shape, generator=gen) < nan_share
+        b = torch.where(pick, nan, b)
+    zeros = torch.rand(shape, generator=gen) < 0.15        # many +-0 ties
+    b = torch.where(zeros, torch.randint(0, 2, shape, generator=gen, dtype=torch.int32) << 15, b)
+    b = torch.where(b >= 1 << 15, b - (1 << 16), b)      # the same 16 bits as a signed value
+    return b.to(torch.int16).view(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=str)
+@pytest.mark.parametrize("nan_share", [0.0, 0.02, 0.5])
+@pytest.mark.parametrize("case", range(len(ANY_BITS_CASES)))
+def test_slab_forward_any_bits(case, nan_share, dtype):
+    shape, out = ANY_BITS_CASES[case]
+    assert mp.adaptive_maxpool3d_fwd_plan(shape, out, dtype) in ("fwd_slab", "fwd_global")
+    gen = torch.Generator().manual_seed(9700 + 10 * case + int(100 * nan_share))
+    x = _any_bits(gen, shape, dtype, nan_share)
+    y_ref, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    y, idx = gpu_fwd(x, out_size=out)
+    assert torch.equal(idx, i_ref), f"idx differs ({shape} -> {out}, nan share {nan_share})"
+    assert torch.equal(bits(y), bits(y_ref)), "y must be the chosen element's own bits"
