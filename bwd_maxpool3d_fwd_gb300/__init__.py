@@ -25,7 +25,7 @@ DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab", 5: "fwd_padded",
          10: "bwd_disjoint",
          11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll",
-         15: "bwd_padded", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct", 6: "fwd_ndhwc",
+         15: "bwd_padded", 19: "fwd_roll", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct", 6: "fwd_ndhwc",
          18: "bwd_ndhwc"}
 
 _lib = None

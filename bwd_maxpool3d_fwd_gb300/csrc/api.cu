@@ -42,6 +42,7 @@ const char* path_name(int path) {
     case MP3D_PATH_FWD_S2: return "fwd_s2";
     case MP3D_PATH_FWD_GLOBAL: return "fwd_global";
     case MP3D_PATH_FWD_SLAB: return "fwd_slab";
+    case MP3D_PATH_FWD_ROLL: return "fwd_roll";
     case MP3D_PATH_BWD_DISJOINT: return "bwd_disjoint";
     case MP3D_PATH_BWD_OVERLAP_TILE: return "bwd_overlap_tile";
     case MP3D_PATH_BWD_OVERLAP_DIRECT: return "bwd_overlap_direct";
@@ -220,6 +221,7 @@ int fwd_path(const Geo& g, int dtype, bool aligned16 = true) {
     if (g.P == 0) return MP3D_PATH_NOOP;
     if (is_global(g)) return MP3D_PATH_FWD_GLOBAL;
     if (fwd_s2_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_S2;
+    if (fwd_roll_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_ROLL;
     if (fwd_slab_supported(g, dtype)) return MP3D_PATH_FWD_SLAB;
     return MP3D_PATH_FWD_GENERIC;
 }
@@ -244,6 +246,7 @@ int run_fwd(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, cudaS
     case MP3D_PATH_FWD_GLOBAL: e = launch_fwd_global(x, y, idx, g, dtype, sms, s); break;
     case MP3D_PATH_FWD_S2: e = launch_fwd_s2(x, y, idx, g, dtype, sms, s); break;
     case MP3D_PATH_FWD_SLAB: e = launch_fwd_slab(x, y, idx, g, dtype, sms, s); break;
+    case MP3D_PATH_FWD_ROLL: e = launch_fwd_roll(x, y, idx, g, dtype, sms, s); break;
     default: e = launch_fwd_generic(x, y, idx, g, dtype, sms, s); break;
     }
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;

@@ -153,4 +153,28 @@ template <typename T> struct Vec16 {
     union { uint4 u; T e[N]; };
 };
 
+// ------------------------------------------------------ order keys (16-bit)
+// An order key of a 16-bit float: an unsigned 16-bit number whose order is
+// the forward scan's preference among values: +0 and -0 share a key,
+// negative values rank below positive ones by magnitude, and every NaN
+// ranks above +inf (all NaNs one key).
+// Two 16-bit values (one per half of w) -> their order keys, half by half.
+// NANADD = 0x7FFF - (largest non-NaN magnitude): bit 15 of mag + NANADD is
+// set exactly for NaN magnitudes.
+template <unsigned NANADD>
+__device__ __forceinline__ unsigned order_keys2(unsigned w) {
+    const unsigned mag = w & 0x7FFF7FFFu;
+    unsigned neg, nan;
+    // prmt with selector nibbles 9 / B: each result byte is the sign of
+    // byte 1 (low half) or byte 3 (high half), replicated
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(nan) : "r"(mag + NANADD * 0x10001u));
+    const unsigned up = 0x80008000u + mag, down = 0x80008000u - mag;   // no carry between halves
+    return (down & neg) | (up & ~neg) | nan;
+}
+
+template <typename T> struct KeyConst;
+template <> struct KeyConst<__half> { static constexpr unsigned nanadd = 0x7FFFu - 0x7C00u; };
+template <> struct KeyConst<__nv_bfloat16> { static constexpr unsigned nanadd = 0x7FFFu - 0x7F80u; };
+
 }  // namespace mp3d

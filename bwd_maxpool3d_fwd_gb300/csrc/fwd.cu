@@ -234,25 +234,6 @@ k_fwd_slab(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
 // to y is re-read from x at the winning offset, so its bits (sign of zero,
 // NaN payload) are the input element's.
 
-// Two 16-bit values (one per half of w) -> their order keys, half by half.
-// NANADD = 0x7FFF - (largest non-NaN magnitude): bit 15 of mag + NANADD is
-// set exactly for NaN magnitudes.
-template <unsigned NANADD>
-__device__ __forceinline__ unsigned order_keys2(unsigned w) {
-    const unsigned mag = w & 0x7FFF7FFFu;
-    unsigned neg, nan;
-    // prmt with selector nibbles 9 / B: each result byte is the sign of
-    // byte 1 (low half) or byte 3 (high half), replicated
-    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(w));
-    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(nan) : "r"(mag + NANADD * 0x10001u));
-    const unsigned up = 0x80008000u + mag, down = 0x80008000u - mag;   // no carry between halves
-    return (down & neg) | (up & ~neg) | nan;
-}
-
-template <typename T> struct KeyConst;
-template <> struct KeyConst<__half> { static constexpr unsigned nanadd = 0x7FFFu - 0x7C00u; };
-template <> struct KeyConst<__nv_bfloat16> { static constexpr unsigned nanadd = 0x7FFFu - 0x7F80u; };
-
 template <typename T>
 __device__ __forceinline__ unsigned order_word(unsigned short b, int e) {
     const unsigned k = order_keys2<KeyConst<T>::nanadd>(b) & 0xFFFFu;

@@ -1,0 +1,316 @@
+// Forward for 16-bit types as a walk along depth: one CTA takes one plane
+// and a group of consecutive output depths, and streams the depth slices
+// its windows cover, in ascending order, through shared memory.
+//
+// Definition followed (teenygrad docs "Struct Maxpool3dForward",
+// description and Constraints; adaptive windows
+// [floor(i*I/O), ceil((i+1)*I/O)) per axis): y is the maximum of the window
+// and idx the in-plane offset d*H*W + h*W + w of the first element, in
+// (d, h, w) order, that attains it; a NaN beats every number.
+//
+// Per slice:
+//  1. its bytes arrive by 16-byte asynchronous copies issued NS - 1 slices
+//     ahead (cp.async groups, one per slice), so loads overlap the work on
+//     earlier slices;
+//  2. every element becomes one 32-bit word: the value's order key in the
+//     high half (+0 and -0 one key, NaN above everything, all NaNs one key),
+//     0xFFFF minus the element's in-slice offset h*W + w in the low half;
+//     the unsigned maximum of a window's words is then the slice's winner
+//     of that window (the earliest (h, w) among equal keys);
+//  3. thread t owns output (oh, ow) = t: it takes the maximum word over its
+//     (h, w) window in the slice and folds it into the accumulators of the
+//     (at most two) depth windows that contain the slice, replacing an
+//     accumulator only for a strictly larger key, so an earlier slice keeps
+//     a tie. When the last slice of a depth window has been folded in, the
+//     output is written: idx from the slice and the in-slice offset, y
+//     re-read from x at that offset (the element's own bits).
+// Scope: 16-bit types, no padding or dilation, at most two windows over any
+// slice along d (fixed K <= 2 * S, or adaptive end(i) <= start(i + 2)),
+// H * W <= 65536 (in-slice offsets fit 16 bits), OH * OW <= threads, x on a
+// 16-byte boundary.
+#include <climits>
+#include <vector>
+
+#include "internal.h"
+
+namespace mp3d {
+
+namespace {
+
+constexpr int RF_NT = 256;      // threads per CTA (and the most outputs per plane-depth)
+constexpr int RF_NS = 4;        // slices in flight: the current one plus NS - 1 ahead
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct RollFwdGeo {
+    int odg, ngrp;      // output depths per CTA, groups per plane
+    int wstr;           // words per slice buffer (multiple of 32)
+    int rstr;           // bytes per raw stage (multiple of 128)
+};
+
+// The output (oh * OW + ow) each thread owns, 0xFFFF for none. Outputs are
+// dealt to warps so that the first words of the windows of one warp lie in
+// different shared-memory banks wherever the geometry allows: every lane
+// then adds the same offsets as the scan proceeds, so every load of the
+// window scan is one wavefront.
+struct OutMap {
+    uint16_t t[RF_NT];
+};
+
+}  // namespace
+
+template <typename T, bool AD, int KH, int KW>
+__global__ void __launch_bounds__(RF_NT)
+k_fwd_roll(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
+           RollFwdGeo rg, const unsigned char* __restrict__ x_end, const __grid_constant__ OutMap om) {
+    extern __shared__ __align__(128) unsigned char smem_rf[];
+    constexpr unsigned NANADD = KeyConst<T>::nanadd;
+    unsigned* words = reinterpret_cast<unsigned*>(smem_rf);                  // [2][wstr]
+    unsigned char* raw = smem_rf + 2 * rg.wstr * sizeof(unsigned);          // [NS][rstr]
+    const int tid = threadIdx.x;
+    const int fh = (tid >> 2) & 1;          // half order of this thread's 32-byte word stores
+    const int HW = g.H * g.W;
+    const long long p = blockIdx.x / rg.ngrp;
+    const int grp = (int)(blockIdx.x - p * rg.ngrp);
+    const int od0 = grp * rg.odg;
+    const int od1 = min(od0 + rg.odg, g.OD);          // output depths [od0, od1)
+    const int d_first = win_start(od0, g.D, g.OD, g.kd, g.sd, AD);
+    const int d_last = win_end(od1 - 1, g.D, g.OD, g.kd, g.sd, AD);   // exclusive
+    const int ns = d_last - d_first;
+
+    // this thread's output and its (h, w) window
+    const int mine = om.t[tid];
+    const bool owner = mine != 0xFFFF;
+    const int oh = owner ? mine / g.OW : 0;
+    const int ow = owner ? mine - oh * g.OW : 0;
+    const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, AD);
+    const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, AD);
+    const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, AD);
+    const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, AD);
+    const int woff = hs * g.W + ws;
+
+    const unsigned char* xb = reinterpret_cast<const unsigned char*>(x + p * g.vol);
+    // slice i of this CTA: global bytes [a, a + HW*2) copied from the 16-byte
+    // boundary at or below a
+    auto issue = [&](int i) {
+        if (i < ns) {
+            const unsigned char* sa = xb + (size_t)(d_first + i) * HW * sizeof(T);
+            const unsigned char* a0 = reinterpret_cast<const unsigned char*>((uintptr_t)sa & ~(uintptr_t)15);
+            const int nvec = (int)((sa + HW * sizeof(T) - a0 + 15) / 16);
+            unsigned char* st = raw + (i % RF_NS) * rg.rstr;
+            for (int v = tid; v < nvec; v += RF_NT) {
+                const unsigned char* src = a0 + 16 * v;
+                if (src + 16 <= x_end) {
+                    cp_async16((uint32_t)__cvta_generic_to_shared(st + 16 * v), src);
+                } else {
+                    // the last vector of the tensor: only its bytes inside x
+                    for (int b = 0; b < 16; b += 2)
+                        *reinterpret_cast<unsigned short*>(st + 16 * v + b) =
+                            src + b < x_end ? *reinterpret_cast<const unsigned short*>(src + b) : 0;
+                }
+            }
+        }
+        cp_async_commit();   // one group per slice, empty past the end
+    };
+#pragma unroll
+    for (int i = 0; i < RF_NS - 1; ++i) issue(i);
+
+    unsigned acc0 = 0u, acc1 = 0u;     // best words of depth windows a and a + 1 (key 0: none yet)
+    int dd0 = 0, dd1 = 0;              // their slices
+    int a = od0;                       // lowest depth window not yet written
+    int a_start = d_first;             // its slices [a_start, a_end)
+    int a_end = win_end(a, g.D, g.OD, g.kd, g.sd, AD);
+    int b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+    for (int i = 0; i < ns; ++i) {
+        cp_async_wait<RF_NS - 2>();    // this thread's copies of slice i have landed
+        __syncthreads();               // everyone's have; slice i - 1's stage is free again
+        issue(i + RF_NS - 1);
+        // 2. order words of slice i
+        const unsigned char* a_ptr = xb + (size_t)(d_first + i) * HW * sizeof(T);
+        const int mis = (int)(((uintptr_t)a_ptr & 15) / sizeof(T));   // elements before the slice
+        const int nvec = (int)((mis * sizeof(T) + HW * sizeof(T) + 15) / 16);
+        const uint4* st = reinterpret_cast<const uint4*>(raw + (i % RF_NS) * rg.rstr);
+        unsigned* wb = words + (i & 1) * rg.wstr;
+        for (int v = tid; v < nvec; v += RF_NT) {
+            const uint4 u = st[v];
+            const unsigned k0 = order_keys2<NANADD>(u.x), k1 = order_keys2<NANADD>(u.y);
+            const unsigned k2 = order_keys2<NANADD>(u.z), k3 = order_keys2<NANADD>(u.w);
+            const unsigned inv = 0xFFFFu - (unsigned)(8 * v - mis);   // element 8v sits at offset 8v - mis
+            const uint4 lo = make_uint4(__byte_perm(k0, inv, 0x1054), __byte_perm(k0, inv - 1, 0x3254),
+                                        __byte_perm(k1, inv - 2, 0x1054), __byte_perm(k1, inv - 3, 0x3254));
+            const uint4 hi = make_uint4(__byte_perm(k2, inv - 4, 0x1054), __byte_perm(k2, inv - 5, 0x3254),
+                                        __byte_perm(k3, inv - 6, 0x1054), __byte_perm(k3, inv - 7, 0x3254));
+            // lanes 4-7 of each quarter-warp store their upper 16 bytes first, so a
+            // quarter-warp's stores meet all eight 16-byte bank groups once
+            uint4* dst = reinterpret_cast<uint4*>(wb + 8 * v);
+            dst[fh] = fh ? hi : lo;
+            dst[fh ^ 1] = fh ? lo : hi;
+        }
+        __syncthreads();
+        // 3. this slice's winner of the (h, w) window, folded into depth windows
+        if (owner) {
+            const unsigned* base = wb + mis + woff;
+            unsigned best = 0u;
+            if constexpr (KH > 0 && KW > 0) {
+#pragma unroll
+                for (int h = 0; h < KH; ++h)
+#pragma unroll
+                    for (int w = 0; w < KW; ++w) best = max(best, base[h * g.W + w]);
+            } else {
+                for (int h = 0; h < he - hs; ++h)
+                    for (int w = 0; w < we - ws; ++w) best = max(best, base[h * g.W + w]);
+            }
+            const int d = d_first + i;
+            if (d >= a_start && d < a_end && (best >> 16) > (acc0 >> 16)) { acc0 = best; dd0 = d; }
+            if (d >= b_start && (best >> 16) > (acc1 >> 16)) { acc1 = best; dd1 = d; }
+            // windows whose last slice this is (two adjacent windows may end together)
+            while (d == a_end - 1) {
+                const int off = dd0 * HW + (int)(0xFFFFu - (acc0 & 0xFFFFu));
+                const long long o = ((p * g.OD + a) * (long long)g.OH) * g.OW + mine;
+                y[o] = x[p * g.vol + off];
+                if (idx) idx[o] = off;
+                acc0 = acc1; dd0 = dd1;
+                acc1 = 0u;
+                ++a;
+                a_start = b_start;
+                a_end = a < od1 ? win_end(a, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+                b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+namespace {
+
+template <typename T> int rf_es() { return (int)sizeof(T); }
+
+// Depth windows: at most two over any slice.
+bool depth_two_cover(const Geo& g) {
+    if (!g.adaptive) return g.kd <= 2 * g.sd;
+    for (int i = 0; i + 2 < g.OD; ++i) {
+        const long long e = ((long long)(i + 1) * g.D + g.OD - 1) / g.OD;
+        const long long s2 = (long long)(i + 2) * g.D / g.OD;
+        if (e > s2) return false;
+    }
+    return true;
+}
+
+int uniform_len_rf(int I, int O, int K, bool adaptive) {
+    if (!adaptive) return K;
+    int len = -1;
+    for (int i = 0; i < O; ++i) {
+        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
+        if (len >= 0 && l != len) return 0;
+        len = l;
+    }
+    return len;
+}
+
+bool plan_rf(const Geo& g, int sms, RollFwdGeo* rg, size_t* smem) {
+    const long long HW = (long long)g.H * g.W;
+    if (HW > 65536 || (long long)g.OH * g.OW > RF_NT) return false;
+    if (g.pd || g.ph || g.pw || g.dd != 1 || g.dh != 1 || g.dw != 1) return false;
+    if (!depth_two_cover(g)) return false;
+    // a slice spans up to 7 elements before it and up to 7 after it
+    rg->wstr = (int)((HW + 16 + 31) / 32 * 32);
+    rg->rstr = (int)((HW * 2 + 32 + 127) / 128 * 128);
+    *smem = 2 * (size_t)rg->wstr * 4 + (size_t)RF_NS * rg->rstr;
+    if (*smem > 96 * 1024) return false;
+    // groups of output depths: enough CTAs for several waves
+    const long long want = 4LL * sms * 4;
+    int odg = g.OD;
+    while (odg > 1 && g.P * ((g.OD + odg - 1) / odg) < want) odg = (odg + 1) / 2;
+    rg->odg = odg;
+    rg->ngrp = (g.OD + odg - 1) / odg;
+    return true;
+}
+
+// Deal the outputs to threads: warp by warp, at most one output per bank of
+// its window's first word (offset hs * W + ws modulo 32 words); outputs left
+// over take any free thread.
+void deal_outputs(const Geo& g, OutMap* om) {
+    const int nout = g.OH * g.OW;
+    std::vector<std::vector<int>> by_bank(32);
+    for (int o = nout - 1; o >= 0; --o) {   // reversed: popped from the back in ascending order
+        const int oh = o / g.OW, ow = o - (o / g.OW) * g.OW;
+        const long long hs = g.adaptive ? (long long)oh * g.H / g.OH : (long long)oh * g.sh;
+        const long long ws = g.adaptive ? (long long)ow * g.W / g.OW : (long long)ow * g.sw;
+        by_bank[(int)((hs * g.W + ws) % 32)].push_back(o);
+    }
+    for (int i = 0; i < RF_NT; ++i) om->t[i] = 0xFFFF;
+    std::vector<int> spare;
+    for (int w = 0; w < RF_NT / 32; ++w) {
+        int lane = 0;
+        for (int b = 0; b < 32; ++b)
+            if (!by_bank[b].empty()) {
+                om->t[w * 32 + lane++] = (uint16_t)by_bank[b].back();
+                by_bank[b].pop_back();
+            }
+    }
+    for (auto& v : by_bank)
+        for (int o : v) spare.push_back(o);
+    size_t k = 0;
+    for (int i = 0; i < RF_NT && k < spare.size(); ++i)
+        if (om->t[i] == 0xFFFF) om->t[i] = (uint16_t)spare[k++];
+}
+
+template <typename T, bool AD>
+auto rf_kernel(int kh, int kw) {
+    if (kh == kw) {
+        switch (kh) {
+        case 2: return k_fwd_roll<T, AD, 2, 2>;
+        case 3: return k_fwd_roll<T, AD, 3, 3>;
+        case 4: return k_fwd_roll<T, AD, 4, 4>;
+        case 5: return k_fwd_roll<T, AD, 5, 5>;
+        default: break;
+        }
+    }
+    return k_fwd_roll<T, AD, 0, 0>;
+}
+
+template <typename T>
+cudaError_t rf_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms, cudaStream_t s) {
+    RollFwdGeo rg;
+    size_t smem = 0;
+    if (!plan_rf(g, sms, &rg, &smem)) return cudaErrorNotSupported;
+    const int kh = uniform_len_rf(g.H, g.OH, g.kh, g.adaptive);
+    const int kw = uniform_len_rf(g.W, g.OW, g.kw, g.adaptive);
+    auto kern = g.adaptive ? rf_kernel<T, true>(kh, kw) : rf_kernel<T, false>(kh, kw);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = g.P * rg.ngrp;
+    if (ctas > INT_MAX) return cudaErrorNotSupported;
+    const unsigned char* x_end = static_cast<const unsigned char*>(x) + (size_t)g.P * g.vol * sizeof(T);
+    OutMap om;
+    deal_outputs(g, &om);
+    kern<<<(unsigned)ctas, RF_NT, smem, s>>>((const T*)x, (T*)y, idx, g, rg, x_end, om);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
+    RollFwdGeo rg;
+    size_t smem = 0;
+    return dtype != F32 && aligned16 && g.P * (long long)g.OD <= INT_MAX &&
+           plan_rf(g, 1, &rg, &smem);
+}
+
+cudaError_t launch_fwd_roll(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,
+                            cudaStream_t s) {
+    switch (dtype) {
+    case F16: return rf_t<__half>(x, y, idx, g, sms, s);
+    case BF16: return rf_t<__nv_bfloat16>(x, y, idx, g, sms, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace mp3d

@@ -27,6 +27,12 @@ bool fwd_slab_supported(const Geo& g, int dtype);
 // Whether the stride-2 kernel handles this geometry and type (it needs the
 // input on a 16-byte boundary; plan queries assume an aligned buffer).
 bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16);
+// 16-bit types, walking the depth slices of a plane in order (fwd_roll.cu):
+// at most two windows over any slice along d, no padding or dilation, small
+// planes of outputs, and the input on a 16-byte boundary.
+bool fwd_roll_supported(const Geo& g, int dtype, bool aligned16);
+cudaError_t launch_fwd_roll(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,
+                            cudaStream_t s);
 
 // Channels-last layout (ndhwc.cu): g.P is the batch N, C the channel count.
 cudaError_t launch_fwd_ndhwc(const void* x, void* y, int64_t* idx, const Geo& g, int C, int dtype,

@@ -95,7 +95,10 @@ typedef enum {
     MP3D_PATH_BWD_PADDED = 15,       /* padded / dilated windows, direct gather */
     MP3D_PATH_BWD_RECOMPUTE_TILES = 16, /* no stored index, 2x2x2 tiling, fused */
     MP3D_PATH_BWD_RECOMPUTE = 17,    /* no stored index, direct form          */
-    MP3D_PATH_BWD_NDHWC = 18         /* channels-last layout                  */
+    MP3D_PATH_BWD_NDHWC = 18,        /* channels-last layout                  */
+    MP3D_PATH_FWD_ROLL = 19          /* 16-bit, depth slices streamed in order,
+                                        windows as unsigned maxima of order
+                                        words                                 */
 } mp3d_path;
 
 /*

@@ -125,7 +125,7 @@ def test_stated_output_sizes():
 
 
 def test_plans_per_workload(L):
-    expect_fwd = {0: {"fwd_slab"}, 1: {"fwd_slab"}, 2: {"fwd_s2"}, 3: {"fwd_s2"},
+    expect_fwd = {0: {"fwd_slab"}, 1: {"fwd_roll"}, 2: {"fwd_s2"}, 3: {"fwd_s2"},
                   4: {"fwd_global"}}
     expect_bwd = {0: {"bwd_disjoint"}, 1: {"bwd_overlap_roll"}, 2: {"bwd_disjoint"},
                   3: {"bwd_overlap_roll"}, 4: {"bwd_disjoint"}}

@@ -452,8 +452,9 @@ VALUES_ONLY = [
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 8, 6, 32), torch.bfloat16),    # 2x2x2 tiling
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 9, 7, 32), torch.float16),
     ("fwd_slab", None, None, (5, 4, 8), (2, 2, 9, 7, 13), torch.float32),
-    ("fwd_slab", None, None, (8, 12, 12), (1, 3, 30, 50, 50), torch.float16),     # keyed slab
-    ("fwd_slab", None, None, (3, 4, 5), (2, 3, 7, 9, 13), torch.bfloat16),
+    ("fwd_roll", None, None, (8, 12, 12), (1, 3, 30, 50, 50), torch.float16),
+    ("fwd_roll", None, None, (3, 4, 5), (2, 3, 7, 9, 13), torch.bfloat16),
+    ("fwd_slab", None, None, (4, 20, 20), (1, 2, 9, 40, 40), torch.float16),      # keyed slab
     ("fwd_generic", (5, 5, 5), (3, 3, 3), None, (1, 1, 8, 120, 120), torch.float32),
     ("fwd_global", None, None, (1, 1, 1), (1, 3, 8, 14, 14), torch.float32),
 ]
@@ -633,8 +634,8 @@ def test_channels_last(case, dtype, offset):
     assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(), "grad_in (channels last)")
 
 
-# The slab forward for 16-bit types ranks elements by one unsigned word
-# (value order key, then earliest offset). Arbitrary bit patterns pin that
+# The slab and rolling forwards for 16-bit types rank elements by one
+# unsigned word (value order key, then earliest offset). Arbitrary bit patterns pin that
 # order against the scan's rule: NaNs of either sign and any payload (the
 # first NaN wins), +0 against -0 (the first wins), subnormals, +-inf. Slab
 # starts off a 16-byte boundary take the element-wise head and tail.
@@ -643,6 +644,8 @@ ANY_BITS_CASES = [
     ((2, 3, 7, 9, 13), (3, 4, 5)),
     ((1, 2, 5, 3, 3), (5, 3, 3)),       # one-element windows
     ((3, 1, 6, 6, 6), (1, 1, 1)),       # one window over a whole plane
+    ((1, 2, 9, 40, 40), (4, 20, 20)),   # more outputs per depth than one CTA's threads
+    ((2, 2, 7, 5, 9), (8, 6, 4)),       # more depth windows than slices
 ]
 
 
@@ -666,7 +669,7 @@ def _any_bits(gen, shape, dtype, nan_share):
 @pytest.mark.parametrize("case", range(len(ANY_BITS_CASES)))
 def test_slab_forward_any_bits(case, nan_share, dtype):
     shape, out = ANY_BITS_CASES[case]
-    assert mp.adaptive_maxpool3d_fwd_plan(shape, out, dtype) in ("fwd_slab", "fwd_global")
+    assert mp.adaptive_maxpool3d_fwd_plan(shape, out, dtype) in ("fwd_roll", "fwd_slab", "fwd_global")
     gen = torch.Generator().manual_seed(9700 + 10 * case + int(100 * nan_share))
     x = _any_bits(gen, shape, dtype, nan_share)
     y_ref, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
