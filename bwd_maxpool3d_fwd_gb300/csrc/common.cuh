@@ -177,4 +177,70 @@ template <typename T> struct KeyConst;
 template <> struct KeyConst<__half> { static constexpr unsigned nanadd = 0x7FFFu - 0x7C00u; };
 template <> struct KeyConst<__nv_bfloat16> { static constexpr unsigned nanadd = 0x7FFFu - 0x7F80u; };
 
+// ------------------------------------------------ packed pairs (16-bit)
+// Two 16-bit values in one 32-bit word, compared lane by lane with set.gt on
+// f16x2 / bf16x2 (a mask of 0xFFFF per lane where the first is greater).
+// NaN never compares greater, so packed scans track NaN and infinities with
+// a running x*0 + acc, which turns NaN once either was seen; the caller then
+// recomputes with the exact scalar rule.
+template <typename T> struct Pair;
+template <> struct Pair<__half> {
+    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("set.gt.u32.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
+        uint32_t r;
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
+        return r;
+    }
+    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
+        return ((acc & 0x7FFFu) > 0x7C00u) || (((acc >> 16) & 0x7FFFu) > 0x7C00u);
+    }
+};
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
+        uint32_t r;
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
+        return r;
+    }
+    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
+        return ((acc & 0x7FFFu) > 0x7F80u) || (((acc >> 16) & 0x7FFFu) > 0x7F80u);
+    }
+};
+
+// Replace (mv, mc) lane by lane where v is strictly greater.
+template <typename T>
+__device__ __forceinline__ void merge2(uint32_t& mv, uint32_t& mc, uint32_t v, uint32_t c) {
+    const uint32_t m = Pair<T>::gt(v, mv);
+    mv = (v & m) | (mv & ~m);
+    mc = (c & m) | (mc & ~m);
+}
+
+// Exact scalar max/argmax over a fixed window (the fallback).
+template <typename T>
+__device__ __noinline__ void exact_window(const T* __restrict__ xp, int ds, int de, int hs, int he,
+                                          int ws, int we, int W, int HW, T* yo, int64_t* io) {
+    int best = ds * HW + hs * W + ws;
+    float m = Elem<T>::to_f(xp[best]);
+    for (int d = ds; d < de; ++d)
+        for (int h = hs; h < he; ++h)
+            for (int w = ws; w < we; ++w) {
+                const int off = d * HW + h * W + w;
+                const float v = Elem<T>::to_f(xp[off]);
+                if (beats(v, m)) {
+                    m = v;
+                    best = off;
+                }
+            }
+    *yo = xp[best];
+    *io = best;
+}
+
 }  // namespace mp3d

@@ -535,66 +535,6 @@ cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g
 // NaN or infinity was seen, and then the thread recomputes the affected
 // outputs with the exact scalar scan (same rule as the generic kernel).
 
-template <typename T> struct Pair;
-template <> struct Pair<__half> {
-    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
-        uint32_t r;
-        asm("set.gt.u32.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-        return r;
-    }
-    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
-        uint32_t r;
-        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
-        return r;
-    }
-    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
-        return ((acc & 0x7FFFu) > 0x7C00u) || (((acc >> 16) & 0x7FFFu) > 0x7C00u);
-    }
-};
-template <> struct Pair<__nv_bfloat16> {
-    static __device__ __forceinline__ uint32_t gt(uint32_t a, uint32_t b) {
-        uint32_t r;
-        asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-        return r;
-    }
-    static __device__ __forceinline__ uint32_t poison(uint32_t acc, uint32_t v) {
-        uint32_t r;
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0u), "r"(acc));
-        return r;
-    }
-    static __device__ __forceinline__ bool is_poisoned(uint32_t acc) {
-        return ((acc & 0x7FFFu) > 0x7F80u) || (((acc >> 16) & 0x7FFFu) > 0x7F80u);
-    }
-};
-
-// Replace (mv, mc) lane by lane where v is strictly greater.
-template <typename T>
-__device__ __forceinline__ void merge2(uint32_t& mv, uint32_t& mc, uint32_t v, uint32_t c) {
-    const uint32_t m = Pair<T>::gt(v, mv);
-    mv = (v & m) | (mv & ~m);
-    mc = (c & m) | (mc & ~m);
-}
-
-// Exact scalar max/argmax over a fixed window (the fallback).
-template <typename T>
-__device__ __noinline__ void exact_window(const T* __restrict__ xp, int ds, int de, int hs, int he,
-                                          int ws, int we, int W, int HW, T* yo, int64_t* io) {
-    int best = ds * HW + hs * W + ws;
-    float m = Elem<T>::to_f(xp[best]);
-    for (int d = ds; d < de; ++d)
-        for (int h = hs; h < he; ++h)
-            for (int w = ws; w < we; ++w) {
-                const int off = d * HW + h * W + w;
-                const float v = Elem<T>::to_f(xp[off]);
-                if (beats(v, m)) {
-                    m = v;
-                    best = off;
-                }
-            }
-    *yo = xp[best];
-    *io = best;
-}
-
 constexpr uint32_t kLanes = 0x00010001u;   // a constant in both 16-bit lanes
 
 // ---- bulk-copy pipeline helpers (mbarrier + cp.async.bulk, sm_90+) ----

@@ -29,6 +29,7 @@
 // H * W <= 65536 (in-slice offsets fit 16 bits), OH * OW <= threads, x on a
 // 16-byte boundary.
 #include <climits>
+#include <cstring>
 #include <vector>
 
 #include "internal.h"
@@ -188,9 +189,222 @@ k_fwd_roll(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     cp_async_wait<0>();
 }
 
+// ------------------------------------------------------------ plane pairs
+// The same walk with two planes per CTA, carried as the two 16-bit lanes of
+// every word: a slice of each plane is staged, the two are interleaved into
+// pair words, and each owner scans its (h, w) window once for both planes
+// with packed compares (set.gt on f16x2 / bf16x2: strictly greater replaces,
+// so the first occurrence in (h, w) order is kept, and +0 / -0 tie). The
+// winner's step in the window travels in the lanes of a second word. Slices
+// fold into the depth windows lane by lane with the same strict compare (an
+// earlier slice keeps a tie). NaN and infinities: a running x*0 + acc turns
+// NaN once either was seen in a window; those outputs are recomputed with
+// the exact scalar scan. Needs both planes' slices at the same offset
+// modulo 16 bytes (plane volume a multiple of 8 elements).
+constexpr int PF_NS = 3;
+
+template <typename T>
+__device__ __noinline__ void exact_output(const T* __restrict__ xp, int ds, int de, int hs, int he,
+                                          int ws, int we, int W, int HW, T* yo, int64_t* io) {
+    int best = ds * HW + hs * W + ws;
+    float m = Elem<T>::to_f(xp[best]);
+    for (int d = ds; d < de; ++d)
+        for (int h = hs; h < he; ++h)
+            for (int w = ws; w < we; ++w) {
+                const int off = d * HW + h * W + w;
+                const float v = Elem<T>::to_f(xp[off]);
+                if (beats(v, m)) {
+                    m = v;
+                    best = off;
+                }
+            }
+    *yo = xp[best];
+    if (io) *io = best;
+}
+
+template <typename T>
+__device__ __forceinline__ T lane_value(uint32_t word, int lane) {
+    const unsigned short b = (unsigned short)(lane ? word >> 16 : word & 0xFFFFu);
+    T v;
+    memcpy(&v, &b, sizeof(T));
+    return v;
+}
+
+template <typename T, bool AD, int KH, int KW>
+__global__ void __launch_bounds__(RF_NT, 4)
+k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
+           RollFwdGeo rg, const unsigned char* __restrict__ x_end, const __grid_constant__ OutMap om) {
+    extern __shared__ __align__(128) unsigned char smem_rf[];
+    uint32_t* words = reinterpret_cast<uint32_t*>(smem_rf);                 // [2][wstr] pair words
+    unsigned char* raw = smem_rf + 2 * rg.wstr * sizeof(uint32_t);         // [NS][2][rstr]
+    const int tid = threadIdx.x;
+    const int fh = (tid >> 2) & 1;          // half order of this thread's 32-byte word stores
+    const int HW = g.H * g.W;
+    const long long pp = blockIdx.x / rg.ngrp;
+    const int grp = (int)(blockIdx.x - pp * rg.ngrp);
+    const long long p0 = 2 * pp;
+    const bool has1 = p0 + 1 < g.P;
+    const long long p1 = has1 ? p0 + 1 : p0;   // a lone last plane runs in both lanes
+    const int od0 = grp * rg.odg;
+    const int od1 = min(od0 + rg.odg, g.OD);
+    const int d_first = win_start(od0, g.D, g.OD, g.kd, g.sd, AD);
+    const int d_last = win_end(od1 - 1, g.D, g.OD, g.kd, g.sd, AD);
+    const int ns = d_last - d_first;
+
+    const int mine = om.t[tid];
+    const bool owner = mine != 0xFFFF;
+    const int oh = owner ? mine / g.OW : 0;
+    const int ow = owner ? mine - oh * g.OW : 0;
+    const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, AD);
+    const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, AD);
+    const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, AD);
+    const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, AD);
+    const int woff = hs * g.W + ws;
+
+    const unsigned char* xb0 = reinterpret_cast<const unsigned char*>(x + p0 * g.vol);
+    const unsigned char* xb1 = reinterpret_cast<const unsigned char*>(x + p1 * g.vol);
+    auto issue = [&](int i) {
+        if (i < ns) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const unsigned char* sa = (q ? xb1 : xb0) + (size_t)(d_first + i) * HW * sizeof(T);
+                const unsigned char* a0 = reinterpret_cast<const unsigned char*>((uintptr_t)sa & ~(uintptr_t)15);
+                const int nvec = (int)((sa + HW * sizeof(T) - a0 + 15) / 16);
+                unsigned char* st = raw + ((i % PF_NS) * 2 + q) * rg.rstr;
+                for (int v = tid; v < nvec; v += RF_NT) {
+                    const unsigned char* src = a0 + 16 * v;
+                    if (src + 16 <= x_end) {
+                        cp_async16((uint32_t)__cvta_generic_to_shared(st + 16 * v), src);
+                    } else {
+                        for (int b = 0; b < 16; b += 2)
+                            *reinterpret_cast<unsigned short*>(st + 16 * v + b) =
+                                src + b < x_end ? *reinterpret_cast<const unsigned short*>(src + b) : 0;
+                    }
+                }
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < PF_NS - 1; ++i) issue(i);
+
+    // depth windows a (lowest not yet written) and a + 1: best pair word,
+    // the in-plane offsets of its two lanes, whether anything was folded in,
+    // whether a NaN or infinity was seen
+    uint32_t av0 = 0u, av1 = 0u;
+    int ao0[2] = {0, 0}, ao1[2] = {0, 0};
+    bool fresh0 = true, fresh1 = true, bad0 = false, bad1 = false;
+    unsigned redo = 0u;                        // depth windows (bit a - od0) seen with NaN or inf
+    int a = od0;
+    int a_start = d_first;
+    int a_end = win_end(a, g.D, g.OD, g.kd, g.sd, AD);
+    int b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+    for (int i = 0; i < ns; ++i) {
+        cp_async_wait<PF_NS - 2>();
+        __syncthreads();
+        issue(i + PF_NS - 1);
+        const unsigned char* sa = xb0 + (size_t)(d_first + i) * HW * sizeof(T);
+        const int mis = (int)(((uintptr_t)sa & 15) / sizeof(T));
+        const int nvec = (int)((mis * sizeof(T) + HW * sizeof(T) + 15) / 16);
+        const uint4* s0 = reinterpret_cast<const uint4*>(raw + ((i % PF_NS) * 2) * rg.rstr);
+        const uint4* s1 = reinterpret_cast<const uint4*>(raw + ((i % PF_NS) * 2 + 1) * rg.rstr);
+        uint32_t* wb = words + (i & 1) * rg.wstr;
+        for (int v = tid; v < nvec; v += RF_NT) {
+            const uint4 A = s0[v], B = s1[v];
+            // word j: element j of plane p0 in the low lane, of plane p1 in the high lane
+            const uint4 lo = make_uint4(__byte_perm(A.x, B.x, 0x5410), __byte_perm(A.x, B.x, 0x7632),
+                                        __byte_perm(A.y, B.y, 0x5410), __byte_perm(A.y, B.y, 0x7632));
+            const uint4 hi = make_uint4(__byte_perm(A.z, B.z, 0x5410), __byte_perm(A.z, B.z, 0x7632),
+                                        __byte_perm(A.w, B.w, 0x5410), __byte_perm(A.w, B.w, 0x7632));
+            uint4* dst = reinterpret_cast<uint4*>(wb + 8 * v);
+            dst[fh] = fh ? hi : lo;
+            dst[fh ^ 1] = fh ? lo : hi;
+        }
+        __syncthreads();
+        if (owner) {
+            const uint32_t* base = wb + mis + woff;
+            uint32_t mv = base[0], mk = 0u;
+            uint32_t pz = Pair<T>::poison(0u, mv);
+            int o_lane[2];
+            if constexpr (KH > 0 && KW > 0) {
+#pragma unroll
+                for (int k = 1; k < KH * KW; ++k) {
+                    const uint32_t v = base[(k / KW) * g.W + (k % KW)];
+                    merge2<T>(mv, mk, v, (uint32_t)k * 0x00010001u);
+                    pz = Pair<T>::poison(pz, v);
+                }
+#pragma unroll
+                for (int l = 0; l < 2; ++l) {
+                    const int k = (int)(l ? mk >> 16 : mk & 0xFFFFu);
+                    o_lane[l] = woff + (k / KW) * g.W + k % KW;
+                }
+            } else {
+                // runtime lengths: the lanes carry the winner's offset h * W + w
+                // inside the window box (below H * W <= 65536)
+                for (int h = 0; h < he - hs; ++h)
+                    for (int w = 0; w < we - ws; ++w) {
+                        if ((h | w) == 0) continue;
+                        const uint32_t v = base[h * g.W + w];
+                        merge2<T>(mv, mk, v, (uint32_t)(h * g.W + w) * 0x00010001u);
+                        pz = Pair<T>::poison(pz, v);
+                    }
+#pragma unroll
+                for (int l = 0; l < 2; ++l) o_lane[l] = woff + (int)(l ? mk >> 16 : mk & 0xFFFFu);
+            }
+            const bool bad = Pair<T>::is_poisoned(pz);
+            const int d = d_first + i;
+            const int dHW = d * HW;
+            if (d >= a_start && d < a_end) {
+                const uint32_t m = fresh0 ? 0xFFFFFFFFu : Pair<T>::gt(mv, av0);
+                av0 = (mv & m) | (av0 & ~m);
+                if (m & 0xFFFFu) ao0[0] = dHW + o_lane[0];
+                if (m >> 16) ao0[1] = dHW + o_lane[1];
+                fresh0 = false;
+                bad0 |= bad;
+            }
+            if (d >= b_start) {
+                const uint32_t m = fresh1 ? 0xFFFFFFFFu : Pair<T>::gt(mv, av1);
+                av1 = (mv & m) | (av1 & ~m);
+                if (m & 0xFFFFu) ao1[0] = dHW + o_lane[0];
+                if (m >> 16) ao1[1] = dHW + o_lane[1];
+                fresh1 = false;
+                bad1 |= bad;
+            }
+            while (d == a_end - 1) {
+#pragma unroll
+                for (int l = 0; l < 2; ++l) {
+                    if (l == 1 && !has1) break;
+                    const long long o = (((l ? p1 : p0) * g.OD + a) * (long long)g.OH) * g.OW + mine;
+                    y[o] = lane_value<T>(av0, l);
+                    if (idx) idx[o] = ao0[l];
+                }
+                if (bad0) redo |= 1u << (a - od0);      // recomputed after the walk
+                av0 = av1; ao0[0] = ao1[0]; ao0[1] = ao1[1];
+                fresh0 = fresh1; bad0 = bad1;
+                fresh1 = true; bad1 = false;
+                ++a;
+                a_start = b_start;
+                a_end = a < od1 ? win_end(a, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+                b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+            }
+        }
+    }
+    cp_async_wait<0>();
+    // outputs whose windows held a NaN or an infinity: the exact scalar scan
+    while (redo) {
+        const int r = od0 + __ffs(redo) - 1;
+        redo &= redo - 1;
+        const int ds = win_start(r, g.D, g.OD, g.kd, g.sd, AD), de = win_end(r, g.D, g.OD, g.kd, g.sd, AD);
+        for (int l = 0; l < (has1 ? 2 : 1); ++l) {
+            const long long pl = l ? p1 : p0;
+            const long long o = ((pl * g.OD + r) * (long long)g.OH) * g.OW + mine;
+            exact_output<T>(x + pl * g.vol, ds, de, hs, he, ws, we, g.W, HW, y + o, idx ? idx + o : nullptr);
+        }
+    }
+}
+
 namespace {
 
-template <typename T> int rf_es() { return (int)sizeof(T); }
 
 // Depth windows: at most two over any slice.
 bool depth_two_cover(const Geo& g) {
@@ -214,20 +428,24 @@ int uniform_len_rf(int I, int O, int K, bool adaptive) {
     return len;
 }
 
-bool plan_rf(const Geo& g, int sms, RollFwdGeo* rg, size_t* smem) {
+// pair: two planes per CTA (the packed form); else one plane (order words).
+bool plan_rf(const Geo& g, int sms, bool pair, RollFwdGeo* rg, size_t* smem) {
     const long long HW = (long long)g.H * g.W;
     if (HW > 65536 || (long long)g.OH * g.OW > RF_NT) return false;
     if (g.pd || g.ph || g.pw || g.dd != 1 || g.dh != 1 || g.dw != 1) return false;
     if (!depth_two_cover(g)) return false;
+    if (pair && g.vol % 8 != 0) return false;
     // a slice spans up to 7 elements before it and up to 7 after it
     rg->wstr = (int)((HW + 16 + 31) / 32 * 32);
     rg->rstr = (int)((HW * 2 + 32 + 127) / 128 * 128);
-    *smem = 2 * (size_t)rg->wstr * 4 + (size_t)RF_NS * rg->rstr;
+    *smem = 2 * (size_t)rg->wstr * 4 + (size_t)(pair ? 2 * PF_NS : RF_NS) * rg->rstr;
     if (*smem > 96 * 1024) return false;
-    // groups of output depths: enough CTAs for several waves
-    const long long want = 4LL * sms * 4;
+    // groups of output depths: enough CTAs for a few waves
+    const long long units = pair ? (g.P + 1) / 2 : g.P;
+    const long long want = (pair ? 3LL : 4LL) * sms * 4;
     int odg = g.OD;
-    while (odg > 1 && g.P * ((g.OD + odg - 1) / odg) < want) odg = (odg + 1) / 2;
+    while (odg > 1 && (units * ((g.OD + odg - 1) / odg) < want || (pair && odg > 32)))
+        odg = (odg + 1) / 2;
     rg->odg = odg;
     rg->ngrp = (g.OD + odg - 1) / odg;
     return true;
@@ -276,17 +494,33 @@ auto rf_kernel(int kh, int kw) {
     return k_fwd_roll<T, AD, 0, 0>;
 }
 
+template <typename T, bool AD>
+auto pf_kernel(int kh, int kw) {
+    if (kh == kw) {
+        switch (kh) {
+        case 2: return k_fwd_pair<T, AD, 2, 2>;
+        case 3: return k_fwd_pair<T, AD, 3, 3>;
+        case 4: return k_fwd_pair<T, AD, 4, 4>;
+        case 5: return k_fwd_pair<T, AD, 5, 5>;
+        default: break;
+        }
+    }
+    return k_fwd_pair<T, AD, 0, 0>;
+}
+
 template <typename T>
 cudaError_t rf_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms, cudaStream_t s) {
     RollFwdGeo rg;
     size_t smem = 0;
-    if (!plan_rf(g, sms, &rg, &smem)) return cudaErrorNotSupported;
+    const bool pair = plan_rf(g, sms, true, &rg, &smem);
+    if (!pair && !plan_rf(g, sms, false, &rg, &smem)) return cudaErrorNotSupported;
     const int kh = uniform_len_rf(g.H, g.OH, g.kh, g.adaptive);
     const int kw = uniform_len_rf(g.W, g.OW, g.kw, g.adaptive);
-    auto kern = g.adaptive ? rf_kernel<T, true>(kh, kw) : rf_kernel<T, false>(kh, kw);
+    auto kern = pair ? (g.adaptive ? pf_kernel<T, true>(kh, kw) : pf_kernel<T, false>(kh, kw))
+                     : (g.adaptive ? rf_kernel<T, true>(kh, kw) : rf_kernel<T, false>(kh, kw));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = g.P * rg.ngrp;
+    const long long ctas = (pair ? (g.P + 1) / 2 : g.P) * rg.ngrp;
     if (ctas > INT_MAX) return cudaErrorNotSupported;
     const unsigned char* x_end = static_cast<const unsigned char*>(x) + (size_t)g.P * g.vol * sizeof(T);
     OutMap om;
@@ -301,7 +535,7 @@ bool fwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
     RollFwdGeo rg;
     size_t smem = 0;
     return dtype != F32 && aligned16 && g.P * (long long)g.OD <= INT_MAX &&
-           plan_rf(g, 1, &rg, &smem);
+           plan_rf(g, 1, false, &rg, &smem);
 }
 
 cudaError_t launch_fwd_roll(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,

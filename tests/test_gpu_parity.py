@@ -646,6 +646,8 @@ ANY_BITS_CASES = [
     ((3, 1, 6, 6, 6), (1, 1, 1)),       # one window over a whole plane
     ((1, 2, 9, 40, 40), (4, 20, 20)),   # more outputs per depth than one CTA's threads
     ((2, 2, 7, 5, 9), (8, 6, 4)),       # more depth windows than slices
+    ((1, 3, 8, 10, 12), (3, 4, 5)),     # plane pairs (volume a multiple of 8), a lone last plane
+    ((1, 5, 16, 8, 8), (6, 3, 3)),
 ]
 
 
