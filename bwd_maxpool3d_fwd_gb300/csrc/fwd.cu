@@ -537,45 +537,9 @@ cudaError_t launch_fwd_global(const void* x, void* y, int64_t* idx, const Geo& g
 
 constexpr uint32_t kLanes = 0x00010001u;   // a constant in both 16-bit lanes
 
-// ---- bulk-copy pipeline helpers (mbarrier + cp.async.bulk, sm_90+) ----
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    return done != 0;
-}
-// Bounded wait: gives up after `limit` polls (each poll may itself suspend
-// for a short, hardware-defined time) and reports failure.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit) {
-    for (int i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
 // Set when a pipeline wait gave up (never expected); read and cleared by
 // mp3d_device_error_flags().
 __device__ unsigned int g_mp3d_device_error = 0;
-constexpr unsigned int kErrPipelineTimeout = 1u;
-constexpr int kWaitLimit = 1 << 22;
 
 // One CTA = (plane p, output-depth group, band of G oh-tiles of TOH rows).
 // Threads = nc chunks x G tiles. Each depth slice's band of input rows is
@@ -975,7 +939,12 @@ namespace mp3d {
 
 cudaError_t read_device_error(unsigned int* flags, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_mp3d_device_error, sizeof(unsigned int));
-    if (e != cudaSuccess || !clear) return e;
+    if (e != cudaSuccess) return e;
+    unsigned int more = 0;
+    e = read_roll_fwd_error(&more, clear);      // the flag of the kernels in fwd_roll.cu
+    if (e != cudaSuccess) return e;
+    *flags |= more;
+    if (!clear) return cudaSuccess;
     const unsigned int zero = 0;
     return cudaMemcpyToSymbol(g_mp3d_device_error, &zero, sizeof(unsigned int));
 }

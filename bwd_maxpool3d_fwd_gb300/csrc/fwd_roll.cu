@@ -203,6 +203,10 @@ k_fwd_roll(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
 // modulo 16 bytes (plane volume a multiple of 8 elements).
 constexpr int PF_NS = 3;
 
+// Set when a pipeline wait of the kernels in this file gave up (never
+// expected); folded into mp3d_device_error_flags().
+__device__ unsigned int g_mp3d_roll_error = 0;
+
 template <typename T>
 __device__ __noinline__ void exact_output(const T* __restrict__ xp, int ds, int de, int hs, int he,
                                           int ws, int we, int W, int HW, T* yo, int64_t* io) {
@@ -263,30 +267,43 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
 
     const unsigned char* xb0 = reinterpret_cast<const unsigned char*>(x + p0 * g.vol);
     const unsigned char* xb1 = reinterpret_cast<const unsigned char*>(x + p1 * g.vol);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + PF_NS * 2 * rg.rstr);   // one per stage
+    const unsigned char* x_last = reinterpret_cast<const unsigned char*>((uintptr_t)x_end & ~(uintptr_t)15);
+    // (thread 0) slice i of both planes into stage i % NS: one bulk copy per
+    // plane from the 16-byte boundary at or below the slice up to the one
+    // at or above its end (bytes of x past its last 16-byte boundary, if
+    // any, by plain loads), completion counted by the stage's mbarrier
     auto issue = [&](int i) {
-        if (i < ns) {
+        uint32_t total = 0;
+        const unsigned char* src[2];
+        uint32_t bytes[2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const unsigned char* sa = (q ? xb1 : xb0) + (size_t)(d_first + i) * HW * sizeof(T);
-                const unsigned char* a0 = reinterpret_cast<const unsigned char*>((uintptr_t)sa & ~(uintptr_t)15);
-                const int nvec = (int)((sa + HW * sizeof(T) - a0 + 15) / 16);
-                unsigned char* st = raw + ((i % PF_NS) * 2 + q) * rg.rstr;
-                for (int v = tid; v < nvec; v += RF_NT) {
-                    const unsigned char* src = a0 + 16 * v;
-                    if (src + 16 <= x_end) {
-                        cp_async16((uint32_t)__cvta_generic_to_shared(st + 16 * v), src);
-                    } else {
-                        for (int b = 0; b < 16; b += 2)
-                            *reinterpret_cast<unsigned short*>(st + 16 * v + b) =
-                                src + b < x_end ? *reinterpret_cast<const unsigned short*>(src + b) : 0;
-                    }
-                }
-            }
+        for (int q = 0; q < 2; ++q) {
+            const unsigned char* sa = (q ? xb1 : xb0) + (size_t)(d_first + i) * HW * sizeof(T);
+            const unsigned char* a0 = reinterpret_cast<const unsigned char*>((uintptr_t)sa & ~(uintptr_t)15);
+            const unsigned char* a1 = reinterpret_cast<const unsigned char*>(
+                ((uintptr_t)(sa + HW * sizeof(T)) + 15) & ~(uintptr_t)15);
+            const unsigned char* bend = a1 < x_last ? a1 : x_last;
+            unsigned char* st = raw + ((i % PF_NS) * 2 + q) * rg.rstr;
+            for (const unsigned char* t = bend; t < a1 && t < x_end; t += 2)
+                *reinterpret_cast<unsigned short*>(st + (t - a0)) = *reinterpret_cast<const unsigned short*>(t);
+            src[q] = a0;
+            bytes[q] = bend > a0 ? (uint32_t)(bend - a0) : 0u;
+            total += bytes[q];
         }
-        cp_async_commit();
-    };
+        const uint32_t bar = smem_addr(&bars[i % PF_NS]);
+        mbar_expect_tx(bar, total);
 #pragma unroll
-    for (int i = 0; i < PF_NS - 1; ++i) issue(i);
+        for (int q = 0; q < 2; ++q)
+            if (bytes[q]) bulk_g2s(smem_addr(raw + ((i % PF_NS) * 2 + q) * rg.rstr), src[q], bytes[q], bar);
+    };
+    if (tid == 0) {
+        for (int st = 0; st < PF_NS; ++st) mbar_init(smem_addr(&bars[st]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int i = 0; i < PF_NS && i < ns; ++i) issue(i);
 
     // depth windows a (lowest not yet written) and a + 1: best pair word,
     // the in-plane offsets of its two lanes, whether anything was folded in,
@@ -294,15 +311,17 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     uint32_t av0 = 0u, av1 = 0u;
     int ao0[2] = {0, 0}, ao1[2] = {0, 0};
     bool fresh0 = true, fresh1 = true, bad0 = false, bad1 = false;
+    bool failed = false;
     unsigned redo = 0u;                        // depth windows (bit a - od0) seen with NaN or inf
     int a = od0;
     int a_start = d_first;
     int a_end = win_end(a, g.D, g.OD, g.kd, g.sd, AD);
     int b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
     for (int i = 0; i < ns; ++i) {
-        cp_async_wait<PF_NS - 2>();
-        __syncthreads();
-        issue(i + PF_NS - 1);
+        if (!failed && !mbar_wait(smem_addr(&bars[i % PF_NS]), (uint32_t)((i / PF_NS) & 1), kWaitLimit)) {
+            failed = true;
+            atomicOr(&g_mp3d_roll_error, kErrPipelineTimeout);
+        }
         const unsigned char* sa = xb0 + (size_t)(d_first + i) * HW * sizeof(T);
         const int mis = (int)(((uintptr_t)sa & 15) / sizeof(T));
         const int nvec = (int)((mis * sizeof(T) + HW * sizeof(T) + 15) / 16);
@@ -320,7 +339,13 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             dst[fh] = fh ? hi : lo;
             dst[fh ^ 1] = fh ? lo : hi;
         }
+        // every thread is done with stage i % NS (refilled below) and with
+        // the words of slice i - 1 (overwritten next iteration)
         __syncthreads();
+        if (tid == 0 && i + PF_NS < ns && !failed) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(i + PF_NS);
+        }
         if (owner) {
             const uint32_t* base = wb + mis + woff;
             uint32_t mv = base[0], mk = 0u;
@@ -389,7 +414,6 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             }
         }
     }
-    cp_async_wait<0>();
     // outputs whose windows held a NaN or an infinity: the exact scalar scan
     while (redo) {
         const int r = od0 + __ffs(redo) - 1;
@@ -438,7 +462,8 @@ bool plan_rf(const Geo& g, int sms, bool pair, RollFwdGeo* rg, size_t* smem) {
     // a slice spans up to 7 elements before it and up to 7 after it
     rg->wstr = (int)((HW + 16 + 31) / 32 * 32);
     rg->rstr = (int)((HW * 2 + 32 + 127) / 128 * 128);
-    *smem = 2 * (size_t)rg->wstr * 4 + (size_t)(pair ? 2 * PF_NS : RF_NS) * rg->rstr;
+    *smem = 2 * (size_t)rg->wstr * 4 + (size_t)(pair ? 2 * PF_NS : RF_NS) * rg->rstr +
+            (pair ? PF_NS * sizeof(uint64_t) : 0);
     if (*smem > 96 * 1024) return false;
     // groups of output depths: enough CTAs for a few waves
     const long long units = pair ? (g.P + 1) / 2 : g.P;
@@ -530,6 +555,13 @@ cudaError_t rf_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms, cu
 }
 
 }  // namespace
+
+cudaError_t read_roll_fwd_error(unsigned int* flags, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_mp3d_roll_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_mp3d_roll_error, &zero, sizeof(unsigned int));
+}
 
 bool fwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
     RollFwdGeo rg;

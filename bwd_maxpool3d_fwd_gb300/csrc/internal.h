@@ -40,8 +40,10 @@ cudaError_t launch_fwd_ndhwc(const void* x, void* y, int64_t* idx, const Geo& g,
 cudaError_t launch_bwd_ndhwc(const void* go, const int64_t* idx, void* gi, const Geo& g, int C,
                              int dtype, int sms, cudaStream_t s);
 
-// Error flags set by kernels whose bounded waits gave up (fwd.cu).
+// Error flags set by kernels whose bounded waits gave up (fwd.cu, with the
+// flag of fwd_roll.cu folded in).
 cudaError_t read_device_error(unsigned int* flags, bool clear);
+cudaError_t read_roll_fwd_error(unsigned int* flags, bool clear);
 
 // Backward paths (bwd.cu). For the disjoint gather, g.kd..g.sw hold the
 // fixed window (adaptive divisible shapes are passed as kernel = stride =
