@@ -242,7 +242,6 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     uint32_t* words = reinterpret_cast<uint32_t*>(smem_rf);                 // [2][wstr] pair words
     unsigned char* raw = smem_rf + 2 * rg.wstr * sizeof(uint32_t);         // [NS][2][rstr]
     const int tid = threadIdx.x;
-    const int fh = (tid >> 2) & 1;          // half order of this thread's 32-byte word stores
     const int HW = g.H * g.W;
     const long long pp = blockIdx.x / rg.ngrp;
     const int grp = (int)(blockIdx.x - pp * rg.ngrp);
@@ -336,8 +335,8 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             const uint4 hi = make_uint4(__byte_perm(A.z, B.z, 0x5410), __byte_perm(A.z, B.z, 0x7632),
                                         __byte_perm(A.w, B.w, 0x5410), __byte_perm(A.w, B.w, 0x7632));
             uint4* dst = reinterpret_cast<uint4*>(wb + 8 * v);
-            dst[fh] = fh ? hi : lo;
-            dst[fh ^ 1] = fh ? lo : hi;
+            dst[0] = lo;
+            dst[1] = hi;
         }
         // every thread is done with stage i % NS (refilled below) and with
         // the words of slice i - 1 (overwritten next iteration)
@@ -352,11 +351,29 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             uint32_t pz = Pair<T>::poison(0u, mv);
             int o_lane[2];
             if constexpr (KH > 0 && KW > 0) {
+                // each row along w on its own (independent chains), then the
+                // rows in ascending order; a later candidate replaces only
+                // when strictly greater, so ties keep the earlier element
+                uint32_t rv[KH], rk[KH], rp[KH];
 #pragma unroll
-                for (int k = 1; k < KH * KW; ++k) {
-                    const uint32_t v = base[(k / KW) * g.W + (k % KW)];
-                    merge2<T>(mv, mk, v, (uint32_t)k * 0x00010001u);
-                    pz = Pair<T>::poison(pz, v);
+                for (int h = 0; h < KH; ++h) {
+                    rv[h] = base[h * g.W];
+                    rk[h] = (uint32_t)(h * KW) * 0x00010001u;
+                    rp[h] = Pair<T>::poison(0u, rv[h]);
+#pragma unroll
+                    for (int w = 1; w < KW; ++w) {
+                        const uint32_t v = base[h * g.W + w];
+                        merge2<T>(rv[h], rk[h], v, (uint32_t)(h * KW + w) * 0x00010001u);
+                        rp[h] = Pair<T>::poison(rp[h], v);
+                    }
+                }
+                mv = rv[0];
+                mk = rk[0];
+                pz = rp[0];
+#pragma unroll
+                for (int h = 1; h < KH; ++h) {
+                    merge2<T>(mv, mk, rv[h], rk[h]);
+                    pz = Pair<T>::poison(pz, rp[h]);
                 }
 #pragma unroll
                 for (int l = 0; l < 2; ++l) {
