@@ -345,6 +345,14 @@ int run_bwd(const void* grad_out, const int64_t* idx, void* grad_in, void* works
 // Path of a padded / dilated backward: ATOMIC on request; the rolling
 // ordered scatter when it takes the geometry (no dilation, at most two
 // windows over any position); else the direct gather.
+// Padded / dilated / ceil-mode forward: the depth walk for 16-bit types
+// (dilation 1), else the thread-per-output kernel.
+int ex_fwd_path(const Geo& g, int dtype, bool aligned16 = true) {
+    if (g.P == 0) return MP3D_PATH_NOOP;
+    if (fwd_roll_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_ROLL;
+    return MP3D_PATH_FWD_PADDED;
+}
+
 int bwd_ex_path(const Geo& g, int dtype, int algo, bool aligned16 = true) {
     if (g.P == 0) return MP3D_PATH_NOOP;
     if (algo == MP3D_BWD_ATOMIC) return MP3D_PATH_BWD_ATOMIC;
@@ -452,12 +460,14 @@ int maxpool3d_fwd_ex(const void* x, void* y, int64_t* idx, int64_t N, int64_t C,
     if (!st) st = check_fwd_buffers(x, y, idx, g, dtype);
     if (st) return st;
     if (ex_is_plain(g)) return run_fwd(x, y, idx, g, dtype, stream);
-    const int path = g.P == 0 ? MP3D_PATH_NOOP : MP3D_PATH_FWD_PADDED;
+    const int path = ex_fwd_path(g, dtype, (uintptr_t)x % 16 == 0);
     log_path("fwd", path, g, dtype);
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
     int sms = 0;
     if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
-    return launch_fwd_ex(x, y, idx, g, dtype, sms, stream) == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
+    const cudaError_t e = path == MP3D_PATH_FWD_ROLL ? launch_fwd_roll(x, y, idx, g, dtype, sms, stream)
+                                                     : launch_fwd_ex(x, y, idx, g, dtype, sms, stream);
+    return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
 }
 
 int maxpool3d_fwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int kd, int kh,
@@ -468,7 +478,7 @@ int maxpool3d_fwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
     if (!st) st = ex_geo(&g, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw, ceil_mode);
     if (!st && elem_size(dtype) == 0) st = MP3D_ERR_DTYPE;
     if (!st && path)
-        *path = ex_is_plain(g) ? fwd_path(g, dtype) : g.P == 0 ? MP3D_PATH_NOOP : MP3D_PATH_FWD_PADDED;
+        *path = ex_is_plain(g) ? fwd_path(g, dtype) : ex_fwd_path(g, dtype);
     return st;
 }
 

@@ -126,17 +126,25 @@ k_fwd_global(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ i
         float m = -INFINITY;
         int best = INT_MAX;
         if (VEC > 1) {
+            // U loads per lane in flight together, then their elements in order
+            constexpr int U = 8;
             const uint4* xv = reinterpret_cast<const uint4*>(xp);
-#pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) {
-                Vec16<T> c;
-                c.u = __ldg(xv + v);
+            for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+                Vec16<T> c[U];
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const float f = Elem<T>::to_f(c.e[j]);
-                    if (beats(f, m) || best == INT_MAX) {
-                        m = f;
-                        best = v * VEC + j;
+                for (int i = 0; i < U; ++i)
+                    if (v0 + 32 * i < nvec) c[i].u = __ldg(xv + v0 + 32 * i);
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    const int v = v0 + 32 * i;
+                    if (v >= nvec) break;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const float f = Elem<T>::to_f(c[i].e[j]);
+                        if (beats(f, m) || best == INT_MAX) {
+                            m = f;
+                            best = v * VEC + j;
+                        }
                     }
                 }
             }

@@ -52,6 +52,7 @@ __device__ __forceinline__ void cp_async_wait() {
 
 struct RollFwdGeo {
     int odg, ngrp;      // output depths per CTA, groups per plane
+    int bh, nband;      // output rows per band, bands per plane (the pair form)
     int wstr;           // words per slice buffer (multiple of 32)
     int rstr;           // bytes per raw stage (multiple of 128)
 };
@@ -201,11 +202,31 @@ k_fwd_roll(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
 // NaN once either was seen in a window; those outputs are recomputed with
 // the exact scalar scan. Needs both planes' slices at the same offset
 // modulo 16 bytes (plane volume a multiple of 8 elements).
+//
+// A CTA covers a band of output rows [oh0, oh1) (at most RF_NT outputs);
+// its input rows [r0, r1) are one contiguous span of each slice. Fixed
+// windows may be padded (dilation 1): window o covers [o*S - p, o*S - p + K)
+// clipped to the input; padding is never chosen. Windows of full size take
+// the unrolled scan, clipped ones the general loop.
 constexpr int PF_NS = 3;
 
 // Set when a pipeline wait of the kernels in this file gave up (never
 // expected); folded into mp3d_device_error_flags().
 __device__ unsigned int g_mp3d_roll_error = 0;
+
+// Clipped window bounds along one axis (fixed windows with padding p, or
+// adaptive windows; the planner keeps (O + 1) * I below 2^31, so 32-bit
+// division is exact).
+template <bool AD>
+__device__ __forceinline__ int cw_start(int o, int I, int O, int K, int S, int p) {
+    if constexpr (AD) return (o * I) / O;
+    else return max(o * S - p, 0);
+}
+template <bool AD>
+__device__ __forceinline__ int cw_end(int o, int I, int O, int K, int S, int p) {
+    if constexpr (AD) return ((o + 1) * I + O - 1) / O;
+    else return min(o * S - p + K, I);
+}
 
 template <typename T>
 __device__ __noinline__ void exact_output(const T* __restrict__ xp, int ds, int de, int hs, int he,
@@ -234,7 +255,10 @@ __device__ __forceinline__ T lane_value(uint32_t word, int lane) {
     return v;
 }
 
-template <typename T, bool AD, int KH, int KW>
+// KH, KW > 0: windows are KH x KW where not clipped; CLIP: some windows are
+// clipped by the input's edges (padding or ceil mode) and take the general
+// scan; KH = KW = 0: every window takes the general scan.
+template <typename T, bool AD, int KH, int KW, bool CLIP>
 __global__ void __launch_bounds__(RF_NT, 4)
 k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
            RollFwdGeo rg, const unsigned char* __restrict__ x_end, const __grid_constant__ OutMap om) {
@@ -243,35 +267,44 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     unsigned char* raw = smem_rf + 2 * rg.wstr * sizeof(uint32_t);         // [NS][2][rstr]
     const int tid = threadIdx.x;
     const int HW = g.H * g.W;
-    const long long pp = blockIdx.x / rg.ngrp;
-    const int grp = (int)(blockIdx.x - pp * rg.ngrp);
+    const int band = (int)(blockIdx.x % rg.nband);
+    const long long rest = blockIdx.x / rg.nband;
+    const long long pp = rest / rg.ngrp;
+    const int grp = (int)(rest - pp * rg.ngrp);
     const long long p0 = 2 * pp;
     const bool has1 = p0 + 1 < g.P;
     const long long p1 = has1 ? p0 + 1 : p0;   // a lone last plane runs in both lanes
     const int od0 = grp * rg.odg;
     const int od1 = min(od0 + rg.odg, g.OD);
-    const int d_first = win_start(od0, g.D, g.OD, g.kd, g.sd, AD);
-    const int d_last = win_end(od1 - 1, g.D, g.OD, g.kd, g.sd, AD);
+    const int d_first = cw_start<AD>(od0, g.D, g.OD, g.kd, g.sd, g.pd);
+    const int d_last = cw_end<AD>(od1 - 1, g.D, g.OD, g.kd, g.sd, g.pd);
     const int ns = d_last - d_first;
+    const int oh0 = band * rg.bh;
+    const int oh1 = min(oh0 + rg.bh, g.OH);
+    const int r0 = cw_start<AD>(oh0, g.H, g.OH, g.kh, g.sh, g.ph);     // input rows of the band
+    const int r1 = cw_end<AD>(oh1 - 1, g.H, g.OH, g.kh, g.sh, g.ph);
+    const int span = (r1 - r0) * g.W;                                  // elements per slice
 
-    const int mine = om.t[tid];
-    const bool owner = mine != 0xFFFF;
-    const int oh = owner ? mine / g.OW : 0;
-    const int ow = owner ? mine - oh * g.OW : 0;
-    const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, AD);
-    const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, AD);
-    const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, AD);
-    const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, AD);
-    const int woff = hs * g.W + ws;
+    const int mine = om.t[tid];                   // output of the band, (oh - oh0) * OW + ow
+    const bool owner = mine < (oh1 - oh0) * g.OW;   // 0xFFFF: none
+    const int oh = owner ? oh0 + mine / g.OW : oh0;
+    const int ow = owner ? mine % g.OW : 0;
+    const int hs = cw_start<AD>(oh, g.H, g.OH, g.kh, g.sh, g.ph);
+    const int he = cw_end<AD>(oh, g.H, g.OH, g.kh, g.sh, g.ph);
+    const int ws = cw_start<AD>(ow, g.W, g.OW, g.kw, g.sw, g.pw);
+    const int we = cw_end<AD>(ow, g.W, g.OW, g.kw, g.sw, g.pw);
+    const int wabs = hs * g.W + ws;              // in-slice offset of the window's first element
+    const int woff = (hs - r0) * g.W + ws;       // the same inside the band's span
+    const bool full = KH > 0 && KW > 0 && (!CLIP || (he - hs == KH && we - ws == KW));
 
-    const unsigned char* xb0 = reinterpret_cast<const unsigned char*>(x + p0 * g.vol);
-    const unsigned char* xb1 = reinterpret_cast<const unsigned char*>(x + p1 * g.vol);
+    const unsigned char* xb0 = reinterpret_cast<const unsigned char*>(x + p0 * g.vol + (long long)r0 * g.W);
+    const unsigned char* xb1 = reinterpret_cast<const unsigned char*>(x + p1 * g.vol + (long long)r0 * g.W);
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + PF_NS * 2 * rg.rstr);   // one per stage
     const unsigned char* x_last = reinterpret_cast<const unsigned char*>((uintptr_t)x_end & ~(uintptr_t)15);
-    // (thread 0) slice i of both planes into stage i % NS: one bulk copy per
-    // plane from the 16-byte boundary at or below the slice up to the one
-    // at or above its end (bytes of x past its last 16-byte boundary, if
-    // any, by plain loads), completion counted by the stage's mbarrier
+    // (thread 0) slice i's band span of both planes into stage i % NS: one
+    // bulk copy per plane from the 16-byte boundary at or below the span up
+    // to the one at or above its end (bytes of x past its last 16-byte
+    // boundary, if any, by plain loads), counted by the stage's mbarrier
     auto issue = [&](int i) {
         uint32_t total = 0;
         const unsigned char* src[2];
@@ -281,7 +314,7 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             const unsigned char* sa = (q ? xb1 : xb0) + (size_t)(d_first + i) * HW * sizeof(T);
             const unsigned char* a0 = reinterpret_cast<const unsigned char*>((uintptr_t)sa & ~(uintptr_t)15);
             const unsigned char* a1 = reinterpret_cast<const unsigned char*>(
-                ((uintptr_t)(sa + HW * sizeof(T)) + 15) & ~(uintptr_t)15);
+                ((uintptr_t)(sa + span * sizeof(T)) + 15) & ~(uintptr_t)15);
             const unsigned char* bend = a1 < x_last ? a1 : x_last;
             unsigned char* st = raw + ((i % PF_NS) * 2 + q) * rg.rstr;
             for (const unsigned char* t = bend; t < a1 && t < x_end; t += 2)
@@ -314,8 +347,8 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     unsigned redo = 0u;                        // depth windows (bit a - od0) seen with NaN or inf
     int a = od0;
     int a_start = d_first;
-    int a_end = win_end(a, g.D, g.OD, g.kd, g.sd, AD);
-    int b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+    int a_end = cw_end<AD>(a, g.D, g.OD, g.kd, g.sd, g.pd);
+    int b_start = a + 1 < od1 ? cw_start<AD>(a + 1, g.D, g.OD, g.kd, g.sd, g.pd) : INT_MAX;
     for (int i = 0; i < ns; ++i) {
         if (!failed && !mbar_wait(smem_addr(&bars[i % PF_NS]), (uint32_t)((i / PF_NS) & 1), kWaitLimit)) {
             failed = true;
@@ -323,7 +356,7 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
         }
         const unsigned char* sa = xb0 + (size_t)(d_first + i) * HW * sizeof(T);
         const int mis = (int)(((uintptr_t)sa & 15) / sizeof(T));
-        const int nvec = (int)((mis * sizeof(T) + HW * sizeof(T) + 15) / 16);
+        const int nvec = (int)((mis * sizeof(T) + span * sizeof(T) + 15) / 16);
         const uint4* s0 = reinterpret_cast<const uint4*>(raw + ((i % PF_NS) * 2) * rg.rstr);
         const uint4* s1 = reinterpret_cast<const uint4*>(raw + ((i % PF_NS) * 2 + 1) * rg.rstr);
         uint32_t* wb = words + (i & 1) * rg.wstr;
@@ -350,20 +383,21 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             uint32_t mv = base[0], mk = 0u;
             uint32_t pz = Pair<T>::poison(0u, mv);
             int o_lane[2];
-            if constexpr (KH > 0 && KW > 0) {
+            if (full) {
                 // each row along w on its own (independent chains), then the
                 // rows in ascending order; a later candidate replaces only
                 // when strictly greater, so ties keep the earlier element
-                uint32_t rv[KH], rk[KH], rp[KH];
+                constexpr int KH1 = KH > 0 ? KH : 1, KW1 = KW > 0 ? KW : 1;
+                uint32_t rv[KH1], rk[KH1], rp[KH1];
 #pragma unroll
-                for (int h = 0; h < KH; ++h) {
+                for (int h = 0; h < KH1; ++h) {
                     rv[h] = base[h * g.W];
-                    rk[h] = (uint32_t)(h * KW) * 0x00010001u;
+                    rk[h] = (uint32_t)(h * KW1) * 0x00010001u;
                     rp[h] = Pair<T>::poison(0u, rv[h]);
 #pragma unroll
-                    for (int w = 1; w < KW; ++w) {
+                    for (int w = 1; w < KW1; ++w) {
                         const uint32_t v = base[h * g.W + w];
-                        merge2<T>(rv[h], rk[h], v, (uint32_t)(h * KW + w) * 0x00010001u);
+                        merge2<T>(rv[h], rk[h], v, (uint32_t)(h * KW1 + w) * 0x00010001u);
                         rp[h] = Pair<T>::poison(rp[h], v);
                     }
                 }
@@ -371,17 +405,17 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 mk = rk[0];
                 pz = rp[0];
 #pragma unroll
-                for (int h = 1; h < KH; ++h) {
+                for (int h = 1; h < KH1; ++h) {
                     merge2<T>(mv, mk, rv[h], rk[h]);
                     pz = Pair<T>::poison(pz, rp[h]);
                 }
 #pragma unroll
                 for (int l = 0; l < 2; ++l) {
                     const int k = (int)(l ? mk >> 16 : mk & 0xFFFFu);
-                    o_lane[l] = woff + (k / KW) * g.W + k % KW;
+                    o_lane[l] = wabs + (k / KW1) * g.W + k % KW1;
                 }
-            } else {
-                // runtime lengths: the lanes carry the winner's offset h * W + w
+            } else if constexpr (KH == 0 || CLIP) {
+                // general lengths: the lanes carry the winner's offset h * W + w
                 // inside the window box (below H * W <= 65536)
                 for (int h = 0; h < he - hs; ++h)
                     for (int w = 0; w < we - ws; ++w) {
@@ -391,7 +425,7 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                         pz = Pair<T>::poison(pz, v);
                     }
 #pragma unroll
-                for (int l = 0; l < 2; ++l) o_lane[l] = woff + (int)(l ? mk >> 16 : mk & 0xFFFFu);
+                for (int l = 0; l < 2; ++l) o_lane[l] = wabs + (int)(l ? mk >> 16 : mk & 0xFFFFu);
             }
             const bool bad = Pair<T>::is_poisoned(pz);
             const int d = d_first + i;
@@ -412,11 +446,12 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 fresh1 = false;
                 bad1 |= bad;
             }
+            // windows whose last slice this is (two adjacent windows may end together)
             while (d == a_end - 1) {
 #pragma unroll
                 for (int l = 0; l < 2; ++l) {
                     if (l == 1 && !has1) break;
-                    const long long o = (((l ? p1 : p0) * g.OD + a) * (long long)g.OH) * g.OW + mine;
+                    const long long o = (((l ? p1 : p0) * g.OD + a) * (long long)g.OH + oh) * g.OW + ow;
                     y[o] = lane_value<T>(av0, l);
                     if (idx) idx[o] = ao0[l];
                 }
@@ -426,8 +461,8 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 fresh1 = true; bad1 = false;
                 ++a;
                 a_start = b_start;
-                a_end = a < od1 ? win_end(a, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
-                b_start = a + 1 < od1 ? win_start(a + 1, g.D, g.OD, g.kd, g.sd, AD) : INT_MAX;
+                a_end = a < od1 ? cw_end<AD>(a, g.D, g.OD, g.kd, g.sd, g.pd) : INT_MAX;
+                b_start = a + 1 < od1 ? cw_start<AD>(a + 1, g.D, g.OD, g.kd, g.sd, g.pd) : INT_MAX;
             }
         }
     }
@@ -435,10 +470,11 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     while (redo) {
         const int r = od0 + __ffs(redo) - 1;
         redo &= redo - 1;
-        const int ds = win_start(r, g.D, g.OD, g.kd, g.sd, AD), de = win_end(r, g.D, g.OD, g.kd, g.sd, AD);
+        const int ds = cw_start<AD>(r, g.D, g.OD, g.kd, g.sd, g.pd);
+        const int de = cw_end<AD>(r, g.D, g.OD, g.kd, g.sd, g.pd);
         for (int l = 0; l < (has1 ? 2 : 1); ++l) {
             const long long pl = l ? p1 : p0;
-            const long long o = ((pl * g.OD + r) * (long long)g.OH) * g.OW + mine;
+            const long long o = ((pl * g.OD + r) * (long long)g.OH + oh) * g.OW + ow;
             exact_output<T>(x + pl * g.vol, ds, de, hs, he, ws, we, g.W, HW, y + o, idx ? idx + o : nullptr);
         }
     }
@@ -469,41 +505,86 @@ int uniform_len_rf(int I, int O, int K, bool adaptive) {
     return len;
 }
 
-// pair: two planes per CTA (the packed form); else one plane (order words).
+// Clipped window bounds along one axis, as the kernels compute them.
+long long h_start(int o, int I, int O, int K, int S, int p, bool ad) {
+    if (ad) return (long long)o * I / O;
+    const long long v = (long long)o * S - p;
+    return v > 0 ? v : 0;
+}
+long long h_end(int o, int I, int O, int K, int S, int p, bool ad) {
+    if (ad) return ((long long)(o + 1) * I + O - 1) / O;
+    const long long v = (long long)o * S - p + K;
+    return v < I ? v : I;
+}
+
+// pair: two planes per CTA (the packed form, bands of output rows, padded
+// windows allowed); else one plane per CTA (order words, no padding, one
+// band).
 bool plan_rf(const Geo& g, int sms, bool pair, RollFwdGeo* rg, size_t* smem) {
+    const bool ad = g.adaptive != 0;
     const long long HW = (long long)g.H * g.W;
-    if (HW > 65536 || (long long)g.OH * g.OW > RF_NT) return false;
-    if (g.pd || g.ph || g.pw || g.dd != 1 || g.dh != 1 || g.dw != 1) return false;
+    if (HW > 65536 || g.OW > RF_NT) return false;
+    if (g.dd != 1 || g.dh != 1 || g.dw != 1) return false;
+    if (ad && ((long long)(g.OD + 1) * g.D >= (1LL << 31) || (long long)(g.OH + 1) * g.H >= (1LL << 31) ||
+               (long long)(g.OW + 1) * g.W >= (1LL << 31)))
+        return false;     // adaptive window arithmetic in 32 bits
+    if (!pair && (g.pd || g.ph || g.pw || (long long)g.OH * g.OW > RF_NT)) return false;
+    // the order-word form does not clip windows: every fixed window must lie
+    // inside the input (ceil mode can place the last one partly outside)
+    if (!pair && !ad &&
+        ((long long)(g.OD - 1) * g.sd + g.kd > g.D || (long long)(g.OH - 1) * g.sh + g.kh > g.H ||
+         (long long)(g.OW - 1) * g.sw + g.kw > g.W))
+        return false;
     if (!depth_two_cover(g)) return false;
     if (pair && g.vol % 8 != 0) return false;
-    // a slice spans up to 7 elements before it and up to 7 after it
-    rg->wstr = (int)((HW + 16 + 31) / 32 * 32);
-    rg->rstr = (int)((HW * 2 + 32 + 127) / 128 * 128);
+    int bh = g.OH, nband = 1;
+    if (pair) {
+        const long long nb = ((long long)g.OH * g.OW + RF_NT - 1) / RF_NT;
+        bh = (int)((g.OH + nb - 1) / nb);
+        if (bh * g.OW > RF_NT) bh = RF_NT / g.OW;
+        nband = (g.OH + bh - 1) / bh;
+    }
+    long long rows = 0;      // input rows of the widest band
+    for (int b = 0; b < nband; ++b) {
+        const int o0 = b * bh, o1 = o0 + bh < g.OH ? o0 + bh : g.OH;
+        const long long r = h_end(o1 - 1, g.H, g.OH, g.kh, g.sh, g.ph, ad) -
+                            h_start(o0, g.H, g.OH, g.kh, g.sh, g.ph, ad);
+        rows = r > rows ? r : rows;
+    }
+    if (!pair) rows = g.H;   // the order-word form stages whole slices
+    rg->bh = bh;
+    rg->nband = nband;
+    // a span reaches up to 7 elements before and after it
+    rg->wstr = (int)((rows * g.W + 16 + 31) / 32 * 32);
+    rg->rstr = (int)((rows * g.W * 2 + 32 + 127) / 128 * 128);
     *smem = 2 * (size_t)rg->wstr * 4 + (size_t)(pair ? 2 * PF_NS : RF_NS) * rg->rstr +
             (pair ? PF_NS * sizeof(uint64_t) : 0);
     if (*smem > 96 * 1024) return false;
     // groups of output depths: enough CTAs for a few waves
-    const long long units = pair ? (g.P + 1) / 2 : g.P;
+    const long long units = (pair ? (g.P + 1) / 2 : g.P) * nband;
     const long long want = (pair ? 3LL : 4LL) * sms * 4;
     int odg = g.OD;
     while (odg > 1 && (units * ((g.OD + odg - 1) / odg) < want || (pair && odg > 32)))
         odg = (odg + 1) / 2;
     rg->odg = odg;
     rg->ngrp = (g.OD + odg - 1) / odg;
-    return true;
+    return units * rg->ngrp <= INT_MAX;
 }
 
-// Deal the outputs to threads: warp by warp, at most one output per bank of
-// its window's first word (offset hs * W + ws modulo 32 words); outputs left
-// over take any free thread.
-void deal_outputs(const Geo& g, OutMap* om) {
-    const int nout = g.OH * g.OW;
+// Deal the outputs of one band (local index (oh - oh0) * OW + ow, for the
+// first band's geometry) to threads: warp by warp, at most one output per
+// bank of its window's first word (offset in the band's span modulo 32
+// words); outputs left over take any free thread.
+void deal_outputs(const Geo& g, int bh, OutMap* om) {
+    const bool ad = g.adaptive != 0;
+    const int nloc = bh * g.OW;
+    const long long r0 = h_start(0, g.H, g.OH, g.kh, g.sh, g.ph, ad);
     std::vector<std::vector<int>> by_bank(32);
-    for (int o = nout - 1; o >= 0; --o) {   // reversed: popped from the back in ascending order
+    for (int o = nloc - 1; o >= 0; --o) {   // reversed: popped from the back in ascending order
         const int oh = o / g.OW, ow = o - (o / g.OW) * g.OW;
-        const long long hs = g.adaptive ? (long long)oh * g.H / g.OH : (long long)oh * g.sh;
-        const long long ws = g.adaptive ? (long long)ow * g.W / g.OW : (long long)ow * g.sw;
-        by_bank[(int)((hs * g.W + ws) % 32)].push_back(o);
+        const long long hs = h_start(oh < g.OH ? oh : g.OH - 1, g.H, g.OH, g.kh, g.sh, g.ph, ad);
+        const long long ws = h_start(ow, g.W, g.OW, g.kw, g.sw, g.pw, ad);
+        by_bank[(int)(((hs - r0) * g.W + ws) % 32)].push_back(o);
     }
     for (int i = 0; i < RF_NT; ++i) om->t[i] = 0xFFFF;
     std::vector<int> spare;
@@ -536,18 +617,26 @@ auto rf_kernel(int kh, int kw) {
     return k_fwd_roll<T, AD, 0, 0>;
 }
 
-template <typename T, bool AD>
+template <typename T, bool AD, bool CLIP>
 auto pf_kernel(int kh, int kw) {
     if (kh == kw) {
         switch (kh) {
-        case 2: return k_fwd_pair<T, AD, 2, 2>;
-        case 3: return k_fwd_pair<T, AD, 3, 3>;
-        case 4: return k_fwd_pair<T, AD, 4, 4>;
-        case 5: return k_fwd_pair<T, AD, 5, 5>;
+        case 2: return k_fwd_pair<T, AD, 2, 2, CLIP>;
+        case 3: return k_fwd_pair<T, AD, 3, 3, CLIP>;
+        case 4: return k_fwd_pair<T, AD, 4, 4, CLIP>;
+        case 5: return k_fwd_pair<T, AD, 5, 5, CLIP>;
         default: break;
         }
     }
-    return k_fwd_pair<T, AD, 0, 0>;
+    return k_fwd_pair<T, AD, 0, 0, false>;
+}
+
+// Whether a fixed-window geometry clips any window at the input's edges
+// (padding, or ceil mode placing the last window partly outside).
+bool clips(const Geo& g) {
+    if (g.adaptive) return false;
+    return g.pd || g.ph || g.pw || (long long)(g.OD - 1) * g.sd + g.kd > g.D ||
+           (long long)(g.OH - 1) * g.sh + g.kh > g.H || (long long)(g.OW - 1) * g.sw + g.kw > g.W;
 }
 
 template <typename T>
@@ -558,15 +647,17 @@ cudaError_t rf_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms, cu
     if (!pair && !plan_rf(g, sms, false, &rg, &smem)) return cudaErrorNotSupported;
     const int kh = uniform_len_rf(g.H, g.OH, g.kh, g.adaptive);
     const int kw = uniform_len_rf(g.W, g.OW, g.kw, g.adaptive);
-    auto kern = pair ? (g.adaptive ? pf_kernel<T, true>(kh, kw) : pf_kernel<T, false>(kh, kw))
+    auto kern = pair ? (g.adaptive ? pf_kernel<T, true, false>(kh, kw)
+                                   : clips(g) ? pf_kernel<T, false, true>(kh, kw)
+                                              : pf_kernel<T, false, false>(kh, kw))
                      : (g.adaptive ? rf_kernel<T, true>(kh, kw) : rf_kernel<T, false>(kh, kw));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = (pair ? (g.P + 1) / 2 : g.P) * rg.ngrp;
+    const long long ctas = (pair ? (g.P + 1) / 2 : g.P) * rg.ngrp * rg.nband;
     if (ctas > INT_MAX) return cudaErrorNotSupported;
     const unsigned char* x_end = static_cast<const unsigned char*>(x) + (size_t)g.P * g.vol * sizeof(T);
     OutMap om;
-    deal_outputs(g, &om);
+    deal_outputs(g, rg.bh, &om);
     kern<<<(unsigned)ctas, RF_NT, smem, s>>>((const T*)x, (T*)y, idx, g, rg, x_end, om);
     return cudaGetLastError();
 }
@@ -583,8 +674,8 @@ cudaError_t read_roll_fwd_error(unsigned int* flags, bool clear) {
 bool fwd_roll_supported(const Geo& g, int dtype, bool aligned16) {
     RollFwdGeo rg;
     size_t smem = 0;
-    return dtype != F32 && aligned16 && g.P * (long long)g.OD <= INT_MAX &&
-           plan_rf(g, 1, false, &rg, &smem);
+    return dtype != F32 && aligned16 &&
+           (plan_rf(g, 1, true, &rg, &smem) || plan_rf(g, 1, false, &rg, &smem));
 }
 
 cudaError_t launch_fwd_roll(const void* x, void* y, int64_t* idx, const Geo& g, int dtype, int sms,

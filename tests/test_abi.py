@@ -204,8 +204,13 @@ def test_padded_argument_errors(L, bufs):
 
 def test_padded_plans(L):
     f32, f16 = torch.float32, torch.float16
-    # padded or dilated: the padded kernels
+    # padded or dilated: the depth walk for 16-bit types (clipped windows,
+    # plane volume a multiple of 8), else the thread-per-output kernel
     assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                    False, f16) == "fwd_roll"
+    assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                    False, f32) == "fwd_padded"
+    assert mp.maxpool3d_fwd_ex_plan((2, 3, 7, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
                                     False, f16) == "fwd_padded"
     assert mp.maxpool3d_fwd_ex_plan((2, 3, 8, 9, 10), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1),
                                     False, f32) == "fwd_padded"

@@ -454,7 +454,8 @@ VALUES_ONLY = [
     ("fwd_slab", None, None, (5, 4, 8), (2, 2, 9, 7, 13), torch.float32),
     ("fwd_roll", None, None, (8, 12, 12), (1, 3, 30, 50, 50), torch.float16),
     ("fwd_roll", None, None, (3, 4, 5), (2, 3, 7, 9, 13), torch.bfloat16),
-    ("fwd_slab", None, None, (4, 20, 20), (1, 2, 9, 40, 40), torch.float16),      # keyed slab
+    ("fwd_roll", None, None, (4, 20, 20), (1, 2, 9, 40, 40), torch.float16),      # bands of rows
+    ("fwd_slab", None, None, (4, 20, 20), (1, 2, 9, 39, 41), torch.float16),      # keyed slab
     ("fwd_generic", (5, 5, 5), (3, 3, 3), None, (1, 1, 8, 120, 120), torch.float32),
     ("fwd_global", None, None, (1, 1, 1), (1, 3, 8, 14, 14), torch.float32),
 ]
@@ -491,6 +492,9 @@ PADDED_CASES = [
     ((2, 2, 2), (2, 2, 2), (0, 0, 0), (1, 1, 1), True, (1, 2, 9, 9, 9)),       # ceil adds a window
     ((4, 4, 4), (3, 3, 3), (2, 2, 2), (1, 1, 1), True, (1, 2, 11, 14, 19)),
     ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (1, 2, 6, 112, 112)),  # wide planes
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), False, (1, 3, 8, 56, 56)),    # bands of output rows
+    ((2, 2, 2), (2, 2, 2), (0, 0, 0), (1, 1, 1), True, (1, 3, 8, 9, 10)),      # ceil mode, clipped
+    ((3, 3, 3), (1, 2, 2), (1, 1, 1), (1, 1, 1), True, (2, 1, 8, 40, 24)),     # depth stride 1 (3 covers)
 ]
 
 
@@ -518,7 +522,11 @@ def _gpu_bwd_ex(g_cpu, idx_cpu, in_shape, k, s, p, dl, cm, algo=mp.BWD_AUTO):
 @pytest.mark.parametrize("case", range(len(PADDED_CASES)))
 def test_padded_fwd_bwd(case, dtype):
     k, s, p, dl, cm, shape = PADDED_CASES[case]
-    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, dl, cm, dtype) == "fwd_padded"
+    # 16-bit types with dilation 1 and plane volumes a multiple of 8 take the
+    # depth walk (clipped windows); the rest the thread-per-output kernel
+    walk = (dtype != torch.float32 and dl == (1, 1, 1) and k[0] <= 2 * s[0] and
+            (shape[2] * shape[3] * shape[4]) % 8 == 0)
+    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, dl, cm, dtype) == ("fwd_roll" if walk else "fwd_padded")
     gen = torch.Generator().manual_seed(9500 + case)
     x = random_input(gen, shape, dtype, KINDS[case % 3])
     y_ref, i_ref = oracle.maxpool3d_fwd_ex(x, k, s, p, dl, cm)
@@ -529,7 +537,8 @@ def test_padded_fwd_bwd(case, dtype):
     gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
     # undilated windows take the rolling ordered scatter, dilated ones the
     # direct gather; both are bit-exact
-    want = "bwd_overlap_roll" if dl == (1, 1, 1) else "bwd_padded"
+    two_cover = all(kk <= 2 * ss for kk, ss in zip(k, s))
+    want = "bwd_overlap_roll" if dl == (1, 1, 1) and two_cover else "bwd_padded"
     assert mp.maxpool3d_bwd_ex_plan(shape, y_ref.shape[2:], k, s, p, dl, cm, dtype) == want
     assert_bits_equal(_gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm), gin_ref, "grad_in (padded)")
     gin_a = _gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm, algo=mp.BWD_ATOMIC)
@@ -644,7 +653,8 @@ ANY_BITS_CASES = [
     ((2, 3, 7, 9, 13), (3, 4, 5)),
     ((1, 2, 5, 3, 3), (5, 3, 3)),       # one-element windows
     ((3, 1, 6, 6, 6), (1, 1, 1)),       # one window over a whole plane
-    ((1, 2, 9, 40, 40), (4, 20, 20)),   # more outputs per depth than one CTA's threads
+    ((1, 2, 9, 40, 40), (4, 20, 20)),   # more outputs per depth than one CTA's threads (bands)
+    ((1, 2, 9, 39, 41), (4, 20, 20)),   # the same, odd plane volume (keyed slab)
     ((2, 2, 7, 5, 9), (8, 6, 4)),       # more depth windows than slices
     ((1, 3, 8, 10, 12), (3, 4, 5)),     # plane pairs (volume a multiple of 8), a lone last plane
     ((1, 5, 16, 8, 8), (6, 3, 3)),
