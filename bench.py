@@ -246,9 +246,14 @@ def time_one(fn, dev, iters, flush):
     return statistics.median(ts)
 
 
+# Sources of the two kernels the traffic record covers (the stride-2 forward
+# and the rolling backward) and the headers they include.
+TRAFFIC_SOURCES = ("bwd_roll.cu", "common.cuh", "fwd.cu", "internal.h")
+
+
 def kernel_hash():
     h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "csrc"))):
+    for name in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "csrc", name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:12]

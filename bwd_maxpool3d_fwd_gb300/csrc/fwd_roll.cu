@@ -295,7 +295,20 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     const int we = cw_end<AD>(ow, g.W, g.OW, g.kw, g.sw, g.pw);
     const int wabs = hs * g.W + ws;              // in-slice offset of the window's first element
     const int woff = (hs - r0) * g.W + ws;       // the same inside the band's span
-    const bool full = KH > 0 && KW > 0 && (!CLIP || (he - hs == KH && we - ws == KW));
+    // clipped windows scan the full KH x KW box with rows and columns clamped
+    // into the window: a clamped position repeats an element already seen
+    // earlier in the scan, which never replaces the running best (strictly
+    // greater only), so the first occurrence is kept
+    constexpr int KH1 = KH > 0 ? KH : 1, KW1 = KW > 0 ? KW : 1;
+    int crow[KH1], ccol[KW1];                    // CLIP: clamped row (span-relative, times W) and column
+    if constexpr (CLIP) {
+        const int nh = oh * g.sh - g.ph, nw = ow * g.sw - g.pw;   // nominal window origin
+#pragma unroll
+        for (int h = 0; h < KH1; ++h) crow[h] = (min(max(nh + h, hs), he - 1) - r0) * g.W;
+#pragma unroll
+        for (int w = 0; w < KW1; ++w) ccol[w] = min(max(nw + w, ws), we - 1);
+    }
+    const bool full = KH > 0 && KW > 0;
 
     const unsigned char* xb0 = reinterpret_cast<const unsigned char*>(x + p0 * g.vol + (long long)r0 * g.W);
     const unsigned char* xb1 = reinterpret_cast<const unsigned char*>(x + p1 * g.vol + (long long)r0 * g.W);
@@ -387,16 +400,20 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 // each row along w on its own (independent chains), then the
                 // rows in ascending order; a later candidate replaces only
                 // when strictly greater, so ties keep the earlier element
-                constexpr int KH1 = KH > 0 ? KH : 1, KW1 = KW > 0 ? KW : 1;
+                const uint32_t* cbase = wb + mis;
+                auto at = [&](int h, int w) {
+                    if constexpr (CLIP) return cbase[crow[h] + ccol[w]];
+                    else return base[h * g.W + w];
+                };
                 uint32_t rv[KH1], rk[KH1], rp[KH1];
 #pragma unroll
                 for (int h = 0; h < KH1; ++h) {
-                    rv[h] = base[h * g.W];
+                    rv[h] = at(h, 0);
                     rk[h] = (uint32_t)(h * KW1) * 0x00010001u;
                     rp[h] = Pair<T>::poison(0u, rv[h]);
 #pragma unroll
                     for (int w = 1; w < KW1; ++w) {
-                        const uint32_t v = base[h * g.W + w];
+                        const uint32_t v = at(h, w);
                         merge2<T>(rv[h], rk[h], v, (uint32_t)(h * KW1 + w) * 0x00010001u);
                         rp[h] = Pair<T>::poison(rp[h], v);
                     }
@@ -412,9 +429,14 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
 #pragma unroll
                 for (int l = 0; l < 2; ++l) {
                     const int k = (int)(l ? mk >> 16 : mk & 0xFFFFu);
-                    o_lane[l] = wabs + (k / KW1) * g.W + k % KW1;
+                    if constexpr (CLIP) {
+                        const int nh = oh * g.sh - g.ph, nw = ow * g.sw - g.pw;
+                        o_lane[l] = min(max(nh + k / KW1, hs), he - 1) * g.W + min(max(nw + k % KW1, ws), we - 1);
+                    } else {
+                        o_lane[l] = wabs + (k / KW1) * g.W + k % KW1;
+                    }
                 }
-            } else if constexpr (KH == 0 || CLIP) {
+            } else {
                 // general lengths: the lanes carry the winner's offset h * W + w
                 // inside the window box (below H * W <= 65536)
                 for (int h = 0; h < he - hs; ++h)
@@ -571,17 +593,20 @@ bool plan_rf(const Geo& g, int sms, bool pair, RollFwdGeo* rg, size_t* smem) {
     return units * rg->ngrp <= INT_MAX;
 }
 
-// Deal the outputs of one band (local index (oh - oh0) * OW + ow, for the
-// first band's geometry) to threads: warp by warp, at most one output per
-// bank of its window's first word (offset in the band's span modulo 32
-// words); outputs left over take any free thread.
+// Deal the outputs of one band (local index (oh - oh0) * OW + ow, with the
+// window pattern of a band inside the plane, where padding clips nothing)
+// to threads: warp by warp, at most one output per bank of its window's
+// first word (offset in the band's span modulo 32 words); outputs left over
+// take any free thread.
 void deal_outputs(const Geo& g, int bh, OutMap* om) {
     const bool ad = g.adaptive != 0;
     const int nloc = bh * g.OW;
-    const long long r0 = h_start(0, g.H, g.OH, g.kh, g.sh, g.ph, ad);
+    const int nband = (g.OH + bh - 1) / bh;
+    const int oh0 = (nband > 2 ? 1 : 0) * bh;      // a band inside the plane, where windows are whole
+    const long long r0 = h_start(oh0, g.H, g.OH, g.kh, g.sh, g.ph, ad);
     std::vector<std::vector<int>> by_bank(32);
     for (int o = nloc - 1; o >= 0; --o) {   // reversed: popped from the back in ascending order
-        const int oh = o / g.OW, ow = o - (o / g.OW) * g.OW;
+        const int oh = oh0 + o / g.OW, ow = o - (o / g.OW) * g.OW;
         const long long hs = h_start(oh < g.OH ? oh : g.OH - 1, g.H, g.OH, g.kh, g.sh, g.ph, ad);
         const long long ws = h_start(ow, g.W, g.OW, g.kw, g.sw, g.pw, ad);
         by_bank[(int)(((hs - r0) * g.W + ws) % 32)].push_back(o);
