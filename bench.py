@@ -259,10 +259,16 @@ def kernel_hash():
     return h.hexdigest()[:12]
 
 
-def recorded_traffic(kernel_kind):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic_fixed_k3s2_f16_32x128x16x112x112.txt")
+TRAFFIC_WORKLOAD = "fixed_k3s2_f16_32x128x16x112x112"
+
+
+def recorded_traffic(kernel_kind, workload_name, full):
+    """DRAM bytes per launch from the committed ncu summary, if this run is
+    the whole workload the summary was taken on and the kernel sources are
+    the ones it was taken on; else None."""
+    if workload_name != TRAFFIC_WORKLOAD or not full:
+        return None
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{TRAFFIC_WORKLOAD}.txt")
     try:
         with open(path) as f:
             kv = dict(ln.split(":", 1) for ln in f if ":" in ln and not ln.startswith("#"))
@@ -596,7 +602,8 @@ def our_arm(args):
     pf, pb = r.paths()
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kind),
+                "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(kind, w.name, not args.planes),
                 "kernel": pb if kind == "bwd" else pf, "peak_source": peak_kind,
                 "bytes_per_launch": kbytes,
                 "fwd": {"path": pf, "us": round(fwd_ms * 1e3, 2), "bytes": fb,
