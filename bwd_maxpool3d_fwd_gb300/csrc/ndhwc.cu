@@ -92,6 +92,93 @@ k_fwd_ndhwc(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ id
     }
 }
 
+// Forward for 16-bit types, packed: one thread per (n, od, oh, ow, 16-byte
+// chunk of 8 channels). The chunk is four words of two channels each; the
+// window is scanned in (d, h, w) order and each word is merged with set.gt on
+// f16x2 / bf16x2 (a later element replaces only when strictly greater, so
+// the first occurrence is kept and +0 / -0 tie). Each lane carries the
+// winner's offset from the window's first element, d_l*H*W + h_l*W + w_l
+// (below 65536, checked by the launcher). NaN and infinities: a running
+// x*0 + acc turns NaN once either was seen, and the chunk is then recomputed
+// with the exact scalar scan.
+template <typename T, bool ADAPTIVE>
+__global__ void __launch_bounds__(256)
+k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C) {
+    constexpr int VEC = 8;
+    const int nch = C / VEC;
+    const long long total = (long long)g.P * g.ovol * nch;
+    const int HW = g.H * g.W;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int ch = (int)(t % nch);
+        long long r = t / nch;
+        const int ow = (int)(r % g.OW);
+        r /= g.OW;
+        const int oh = (int)(r % g.OH);
+        r /= g.OH;
+        const int od = (int)(r % g.OD);
+        const long long n = r / g.OD;
+        const int ds = win_start(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+        const int de = win_end(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
+        const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+        const int he = win_end(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
+        const int ws = win_start(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+        const int we = win_end(ow, g.W, g.OW, g.kw, g.sw, ADAPTIVE);
+        const T* xn = x + n * (long long)g.vol * C + ch * VEC;
+        const int origin = ds * HW + hs * g.W + ws;
+        uint32_t mv[4], mc[4] = {0u, 0u, 0u, 0u}, pz = 0u;
+        {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(xn + (long long)origin * C));
+            mv[0] = u.x; mv[1] = u.y; mv[2] = u.z; mv[3] = u.w;
+        }
+        for (int d = ds; d < de; ++d)
+            for (int h = hs; h < he; ++h) {
+                const int rowoff = (d - ds) * HW + (h - hs) * g.W;
+                const T* row = xn + ((long long)d * HW + h * g.W) * C;
+                for (int w = ws; w < we; ++w) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + (long long)w * C));
+                    const uint32_t code = (uint32_t)(rowoff + w - ws) * 0x00010001u;
+                    merge2<T>(mv[0], mc[0], u.x, code);
+                    merge2<T>(mv[1], mc[1], u.y, code);
+                    merge2<T>(mv[2], mc[2], u.z, code);
+                    merge2<T>(mv[3], mc[3], u.w, code);
+                    pz = Pair<T>::poison(pz, u.x);
+                    pz = Pair<T>::poison(pz, u.y);
+                    pz = Pair<T>::poison(pz, u.z);
+                    pz = Pair<T>::poison(pz, u.w);
+                }
+            }
+        const long long o = (((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C + ch * VEC;
+        if (Pair<T>::is_poisoned(pz)) {
+            // exact scalar scan of the chunk's eight channels
+            for (int k = 0; k < VEC; ++k) {
+                int best = origin;
+                float m = Elem<T>::to_f(xn[(long long)origin * C + k]);
+                for (int d = ds; d < de; ++d)
+                    for (int h = hs; h < he; ++h)
+                        for (int w = ws; w < we; ++w) {
+                            const int sidx = d * HW + h * g.W + w;
+                            const float f = Elem<T>::to_f(xn[(long long)sidx * C + k]);
+                            if (beats(f, m)) {
+                                m = f;
+                                best = sidx;
+                            }
+                        }
+                y[o + k] = xn[(long long)best * C + k];
+                if (idx) idx[o + k] = best;
+            }
+            continue;
+        }
+        *reinterpret_cast<uint4*>(y + o) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+        if (idx) {
+            int4* id = reinterpret_cast<int4*>(idx + o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                id[q] = make_int4(origin + (int)(mc[q] & 0xFFFFu), 0, origin + (int)(mc[q] >> 16), 0);
+        }
+    }
+}
+
 // Backward: one thread per (n, d, h, w, channel chunk); walks the covering
 // windows in ascending (od, oh, ow) order and, per channel, sums the
 // gradients of the windows whose stored index is this position (first
@@ -209,11 +296,43 @@ cudaError_t bwd_t(const void* go, const int64_t* idx, void* gi, const Geo& g, in
     return cudaGetLastError();
 }
 
+// The winner's offset from its window's first element fits a 16-bit lane
+// for every window of the geometry.
+bool rel_fits(const Geo& g) {
+    long long kd = g.kd, kh = g.kh, kw = g.kw;
+    if (g.adaptive) {
+        auto longest = [](int I, int O) {
+            long long m = 0;
+            for (int i = 0; i < O; ++i) {
+                const long long l = ((long long)(i + 1) * I + O - 1) / O - (long long)i * I / O;
+                m = l > m ? l : m;
+            }
+            return m;
+        };
+        kd = longest(g.D, g.OD);
+        kh = longest(g.H, g.OH);
+        kw = longest(g.W, g.OW);
+    }
+    return (kd - 1) * g.H * g.W + (kh - 1) * g.W + (kw - 1) < 65536;
+}
+
 template <typename T>
 cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int C, int sms,
                          cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
-    if (chunked(C, sizeof(T), {x, y, idx})) return fwd_t<T, VEC>(x, y, idx, g, C, sms, s);
+    if (chunked(C, sizeof(T), {x, y, idx})) {
+        if constexpr (sizeof(T) == 2) {
+            if (rel_fits(g)) {
+                const long long work = (long long)g.P * g.ovol * (C / VEC);
+                if (g.adaptive)
+                    k_fwd_ndhwc_pk<T, true><<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
+                else
+                    k_fwd_ndhwc_pk<T, false><<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
+                return cudaGetLastError();
+            }
+        }
+        return fwd_t<T, VEC>(x, y, idx, g, C, sms, s);
+    }
     return fwd_t<T, 1>(x, y, idx, g, C, sms, s);
 }
 

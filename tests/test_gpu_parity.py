@@ -600,6 +600,10 @@ NDHWC_CASES = [
     ((2, 3, 2), (1, 2, 3), None, (2, 7, 9, 10, 5)),         # odd channel count
     (None, None, (4, 5, 3), (1, 10, 11, 9, 8)),             # adaptive, overlapping
     (None, None, (1, 1, 1), (2, 4, 6, 5, 32)),              # global
+    ((3, 3, 3), (2, 2, 2), None, (1, 7, 9, 11, 16)),        # packed 16-bit form, special values
+    ((2, 2, 2), (2, 2, 2), None, (2, 6, 8, 10, 24)),
+    ((3, 2, 3), (2, 2, 1), None, (1, 8, 7, 9, 32)),
+    (None, None, (3, 4, 5), (2, 6, 9, 10, 8)),              # adaptive, special values
 ]
 
 
