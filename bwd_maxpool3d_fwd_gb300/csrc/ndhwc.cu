@@ -10,6 +10,8 @@
 // 16-byte load across channels, and neighbouring threads read neighbouring
 // chunks (coalesced). Channel counts that are not a multiple of VEC, or
 // buffers off a 16-byte boundary, take the same kernels with VEC = 1.
+#include <cstring>
+
 #include "internal.h"
 
 namespace mp3d {
@@ -259,6 +261,138 @@ k_bwd_ndhwc(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __rest
     }
 }
 
+// Backward for fixed windows of stride 2 on every axis and length at most 4
+// (so at most two windows cover a position along each axis: windows a - 1
+// and a for the positions 2a, 2a + 1): one thread per (n, 2x2x2 block of
+// input positions, CH channels). The thread streams the covering windows of
+// its block, at most 8, in ascending (od, oh, ow) order, loading each
+// window's CH indices and CH gradients once for all 8 positions, and sums for
+// each position and channel the gradients of the windows whose index is
+// that position (binary32, first term as the initial value, one rounding;
+// +0 where none).
+// K > 0: every window is K long on every axis (the covering pairs of window
+// and position are then known at compile time); 0: lengths from g.
+template <typename T, int CH, int K>
+__global__ void __launch_bounds__(256, CH == 2 ? 4 : 2)
+k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
+                int C) {
+    static_assert(CH == 2 || CH == 4, "2 or 4 channels per thread");
+    const int nch = C / CH;
+    const int BD = (g.D + 1) / 2, BH = (g.H + 1) / 2, BW = (g.W + 1) / 2;
+    const long long total = (long long)g.P * BD * BH * BW * nch;
+    const int HW = g.H * g.W;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int ch = (int)(t % nch);
+        long long r = t / nch;
+        const int bw = (int)(r % BW);
+        r /= BW;
+        const int bh = (int)(r % BH);
+        r /= BH;
+        const int bd = (int)(r % BD);
+        const long long n = r / BD;
+        float acc[8][CH];
+        unsigned any = 0u;                       // bit p * CH + k: position p, channel k has a term
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+#pragma unroll
+            for (int k = 0; k < CH; ++k) acc[p][k] = 0.0f;
+        const int d0 = 2 * bd, h0 = 2 * bh, w0 = 2 * bw;
+        const int s0 = d0 * HW + h0 * g.W + w0;  // in-plane offset of position 0
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            const int od = bd - 1 + a;
+            if (od < 0 || od >= g.OD) continue;
+            // positions 2bd + i inside window od along d (window bd - 1 + a
+            // covers position i when 2 - 2a + i < K)
+            const int dm = K > 0 ? ((2 - 2 * a < K ? 1 : 0) | (3 - 2 * a < K && d0 + 1 < g.D ? 2 : 0))
+                                 : ((d0 >= od * 2 && d0 < od * 2 + g.kd ? 1 : 0) |
+                                    (d0 + 1 < g.D && d0 + 1 < od * 2 + g.kd ? 2 : 0));
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int oh = bh - 1 + b;
+                if (oh < 0 || oh >= g.OH) continue;
+                const int hm = K > 0 ? ((2 - 2 * b < K ? 1 : 0) | (3 - 2 * b < K && h0 + 1 < g.H ? 2 : 0))
+                                     : ((h0 >= oh * 2 && h0 < oh * 2 + g.kh ? 1 : 0) |
+                                        (h0 + 1 < g.H && h0 + 1 < oh * 2 + g.kh ? 2 : 0));
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int ow = bw - 1 + c;
+                    if (ow < 0 || ow >= g.OW) continue;
+                    const int wm = K > 0 ? ((2 - 2 * c < K ? 1 : 0) | (3 - 2 * c < K && w0 + 1 < g.W ? 2 : 0))
+                                         : ((w0 >= ow * 2 && w0 < ow * 2 + g.kw ? 1 : 0) |
+                                            (w0 + 1 < g.W && w0 + 1 < ow * 2 + g.kw ? 2 : 0));
+                    if (!dm || !hm || !wm) continue;
+                    const long long o = ((((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C) + ch * CH;
+                    unsigned lo[CH];
+                    bool hz[CH];
+#pragma unroll
+                    for (int q = 0; q < CH / 2; ++q) {
+                        const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + o + 2 * q));
+                        lo[2 * q] = iv.x;
+                        lo[2 * q + 1] = iv.z;
+                        hz[2 * q] = iv.y == 0u;
+                        hz[2 * q + 1] = iv.w == 0u;
+                    }
+                    float gv[CH];
+                    {
+                        T e[CH];
+                        if constexpr (sizeof(T) * CH == 4) {
+                            const unsigned u = *reinterpret_cast<const unsigned*>(go + o);
+                            memcpy(e, &u, sizeof(u));
+                        } else if constexpr (sizeof(T) * CH == 8) {
+                            const uint2 u = *reinterpret_cast<const uint2*>(go + o);
+                            memcpy(e, &u, sizeof(u));
+                        } else {
+                            const uint4 u = *reinterpret_cast<const uint4*>(go + o);
+                            memcpy(e, &u, sizeof(u));
+                        }
+#pragma unroll
+                        for (int k = 0; k < CH; ++k) gv[k] = Elem<T>::to_f(e[k]);
+                    }
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {
+                        const int i = p >> 2, j = (p >> 1) & 1, kk = p & 1;
+                        if (!((dm >> i) & (hm >> j) & (wm >> kk) & 1)) continue;
+                        const unsigned sp = (unsigned)(s0 + i * HW + j * g.W + kk);
+#pragma unroll
+                        for (int k = 0; k < CH; ++k) {
+                            if (lo[k] == sp && hz[k]) {
+                                const unsigned bit = 1u << (p * CH + k);
+                                acc[p][k] = (any & bit) ? acc[p][k] + gv[k] : gv[k];
+                                any |= bit;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int i = p >> 2, j = (p >> 1) & 1, kk = p & 1;
+            if (d0 + i >= g.D || h0 + j >= g.H || w0 + kk >= g.W) continue;
+            const long long e = (n * (long long)g.vol + s0 + i * HW + j * g.W + kk) * C + ch * CH;
+            T out[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+                out[k] = Elem<T>::from_f(((any >> (p * CH + k)) & 1u) ? acc[p][k] : 0.0f);
+            if constexpr (sizeof(T) * CH == 4) {
+                unsigned u;
+                memcpy(&u, out, sizeof(u));
+                *reinterpret_cast<unsigned*>(gi + e) = u;
+            } else if constexpr (sizeof(T) * CH == 8) {
+                uint2 u;
+                memcpy(&u, out, sizeof(u));
+                *reinterpret_cast<uint2*>(gi + e) = u;
+            } else {
+                uint4 u;
+                memcpy(&u, out, sizeof(u));
+                *reinterpret_cast<uint4*>(gi + e) = u;
+            }
+        }
+    }
+}
+
 namespace {
 
 int grid_of(long long work, int sms) {
@@ -336,10 +470,29 @@ cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int
     return fwd_t<T, 1>(x, y, idx, g, C, sms, s);
 }
 
+// The block form: fixed windows, stride 2 and length at most 4 on every
+// axis, BLK_CH channels per thread with aligned vector access.
+constexpr int BLK_CH = 4;
+bool blk_ok(const Geo& g, int C, int es, const void* go, const int64_t* idx, const void* gi) {
+    if (g.adaptive || g.sd != 2 || g.sh != 2 || g.sw != 2) return false;
+    if (g.kd > 4 || g.kh > 4 || g.kw > 4 || C % BLK_CH != 0) return false;
+    const uintptr_t a = BLK_CH * (uintptr_t)es;   // bytes of the thread's channels
+    return (uintptr_t)idx % 16 == 0 && (uintptr_t)go % a == 0 && (uintptr_t)gi % a == 0;
+}
+
 template <typename T>
 cudaError_t bwd_dispatch(const void* go, const int64_t* idx, void* gi, const Geo& g, int C, int sms,
                          cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
+    if (blk_ok(g, C, sizeof(T), go, idx, gi)) {
+        const long long work =
+            (long long)g.P * ((g.D + 1) / 2) * ((g.H + 1) / 2) * ((g.W + 1) / 2) * (C / BLK_CH);
+        const int k = g.kd == g.kh && g.kd == g.kw && (g.kd == 2 || g.kd == 3) ? g.kd : 0;
+        auto kern = k == 2 ? k_bwd_ndhwc_blk<T, BLK_CH, 2>
+                           : k == 3 ? k_bwd_ndhwc_blk<T, BLK_CH, 3> : k_bwd_ndhwc_blk<T, BLK_CH, 0>;
+        kern<<<grid_of(work, sms), 256, 0, s>>>((const T*)go, idx, (T*)gi, g, C);
+        return cudaGetLastError();
+    }
     if (chunked(C, sizeof(T), {go, idx, gi})) return bwd_t<T, VEC>(go, idx, gi, g, C, sms, s);
     return bwd_t<T, 1>(go, idx, gi, g, C, sms, s);
 }
