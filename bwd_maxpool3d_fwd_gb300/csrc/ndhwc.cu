@@ -279,18 +279,26 @@ k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __
     static_assert(CH == 2 || CH == 4, "2 or 4 channels per thread");
     const int nch = C / CH;
     const int BD = (g.D + 1) / 2, BH = (g.H + 1) / 2, BW = (g.W + 1) / 2;
-    const long long total = (long long)g.P * BD * BH * BW * nch;
+    // blocks are taken in groups of 2x2x2 (neighbours share most of their
+    // covering windows, so the group's loads of a window after the first
+    // are served by L1): work index = ((n, group) * 8 + block in group) * nch + chunk
+    const int GD = (BD + 1) / 2, GH = (BH + 1) / 2, GW = (BW + 1) / 2;
+    const long long total = (long long)g.P * GD * GH * GW * 8 * nch;
     const int HW = g.H * g.W;
     for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
          t += (long long)gridDim.x * blockDim.x) {
         const int ch = (int)(t % nch);
         long long r = t / nch;
-        const int bw = (int)(r % BW);
-        r /= BW;
-        const int bh = (int)(r % BH);
-        r /= BH;
-        const int bd = (int)(r % BD);
-        const long long n = r / BD;
+        const int sub = (int)(r % 8);
+        r /= 8;
+        const int gw = (int)(r % GW);
+        r /= GW;
+        const int gh = (int)(r % GH);
+        r /= GH;
+        const int gd = (int)(r % GD);
+        const long long n = r / GD;
+        const int bd = 2 * gd + (sub >> 2), bh = 2 * gh + ((sub >> 1) & 1), bw = 2 * gw + (sub & 1);
+        if (bd >= BD || bh >= BH || bw >= BW) continue;
         float acc[8][CH];
         unsigned any = 0u;                       // bit p * CH + k: position p, channel k has a term
 #pragma unroll
@@ -485,8 +493,8 @@ cudaError_t bwd_dispatch(const void* go, const int64_t* idx, void* gi, const Geo
                          cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     if (blk_ok(g, C, sizeof(T), go, idx, gi)) {
-        const long long work =
-            (long long)g.P * ((g.D + 1) / 2) * ((g.H + 1) / 2) * ((g.W + 1) / 2) * (C / BLK_CH);
+        const long long work = (long long)g.P * ((g.D + 3) / 4) * ((g.H + 3) / 4) * ((g.W + 3) / 4) * 8 *
+                               (C / BLK_CH);
         const int k = g.kd == g.kh && g.kd == g.kw && (g.kd == 2 || g.kd == 3) ? g.kd : 0;
         auto kern = k == 2 ? k_bwd_ndhwc_blk<T, BLK_CH, 2>
                            : k == 3 ? k_bwd_ndhwc_blk<T, BLK_CH, 3> : k_bwd_ndhwc_blk<T, BLK_CH, 0>;
