@@ -103,7 +103,9 @@ k_fwd_ndhwc(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ id
 // (below 65536, checked by the launcher). NaN and infinities: a running
 // x*0 + acc turns NaN once either was seen, and the chunk is then recomputed
 // with the exact scalar scan.
-template <typename T, bool ADAPTIVE>
+// KH, KW > 0: every window is KH x KW in (h, w); each depth's KH * KW loads
+// are issued together before they are merged (in order).
+template <typename T, bool ADAPTIVE, int KH, int KW>
 __global__ void __launch_bounds__(256)
 k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C) {
     constexpr int VEC = 8;
@@ -133,23 +135,39 @@ k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(xn + (long long)origin * C));
             mv[0] = u.x; mv[1] = u.y; mv[2] = u.z; mv[3] = u.w;
         }
-        for (int d = ds; d < de; ++d)
-            for (int h = hs; h < he; ++h) {
-                const int rowoff = (d - ds) * HW + (h - hs) * g.W;
-                const T* row = xn + ((long long)d * HW + h * g.W) * C;
-                for (int w = ws; w < we; ++w) {
-                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + (long long)w * C));
-                    const uint32_t code = (uint32_t)(rowoff + w - ws) * 0x00010001u;
-                    merge2<T>(mv[0], mc[0], u.x, code);
-                    merge2<T>(mv[1], mc[1], u.y, code);
-                    merge2<T>(mv[2], mc[2], u.z, code);
-                    merge2<T>(mv[3], mc[3], u.w, code);
-                    pz = Pair<T>::poison(pz, u.x);
-                    pz = Pair<T>::poison(pz, u.y);
-                    pz = Pair<T>::poison(pz, u.z);
-                    pz = Pair<T>::poison(pz, u.w);
-                }
+        auto take = [&](const uint4& u, uint32_t code) {
+            merge2<T>(mv[0], mc[0], u.x, code);
+            merge2<T>(mv[1], mc[1], u.y, code);
+            merge2<T>(mv[2], mc[2], u.z, code);
+            merge2<T>(mv[3], mc[3], u.w, code);
+            pz = Pair<T>::poison(pz, u.x);
+            pz = Pair<T>::poison(pz, u.y);
+            pz = Pair<T>::poison(pz, u.z);
+            pz = Pair<T>::poison(pz, u.w);
+        };
+        if constexpr (KH > 0 && KW > 0) {
+            for (int d = ds; d < de; ++d) {
+                const T* plane = xn + ((long long)d * HW + hs * g.W + ws) * C;
+                uint4 u[KH * KW];
+#pragma unroll
+                for (int k = 0; k < KH * KW; ++k)
+                    u[k] = __ldg(reinterpret_cast<const uint4*>(plane + ((long long)(k / KW) * g.W + k % KW) * C));
+                const int dofs = (d - ds) * HW;
+#pragma unroll
+                for (int k = 0; k < KH * KW; ++k)
+                    take(u[k], (uint32_t)(dofs + (k / KW) * g.W + k % KW) * 0x00010001u);
             }
+        } else {
+            for (int d = ds; d < de; ++d)
+                for (int h = hs; h < he; ++h) {
+                    const int rowoff = (d - ds) * HW + (h - hs) * g.W;
+                    const T* row = xn + ((long long)d * HW + h * g.W) * C;
+                    for (int w = ws; w < we; ++w) {
+                        const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + (long long)w * C));
+                        take(u, (uint32_t)(rowoff + w - ws) * 0x00010001u);
+                    }
+                }
+        }
         const long long o = (((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C + ch * VEC;
         if (Pair<T>::is_poisoned(pz)) {
             // exact scalar scan of the chunk's eight channels
@@ -438,6 +456,18 @@ cudaError_t bwd_t(const void* go, const int64_t* idx, void* gi, const Geo& g, in
     return cudaGetLastError();
 }
 
+// The one window length along an axis, or 0 when lengths differ.
+int uniform_len(int I, int O, int K, bool adaptive) {
+    if (!adaptive) return K;
+    int len = -1;
+    for (int i = 0; i < O; ++i) {
+        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
+        if (len >= 0 && l != len) return 0;
+        len = l;
+    }
+    return len;
+}
+
 // The winner's offset from its window's first element fits a 16-bit lane
 // for every window of the geometry.
 bool rel_fits(const Geo& g) {
@@ -466,10 +496,15 @@ cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int
         if constexpr (sizeof(T) == 2) {
             if (rel_fits(g)) {
                 const long long work = (long long)g.P * g.ovol * (C / VEC);
-                if (g.adaptive)
-                    k_fwd_ndhwc_pk<T, true><<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
-                else
-                    k_fwd_ndhwc_pk<T, false><<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
+                // uniform (h, w) window extents 2 or 3: the unrolled form
+                const int kh = uniform_len(g.H, g.OH, g.kh, g.adaptive);
+                const int kw = uniform_len(g.W, g.OW, g.kw, g.adaptive);
+                const int k = kh == kw && (kh == 2 || kh == 3) ? kh : 0;
+                auto kern = g.adaptive ? (k == 2 ? k_fwd_ndhwc_pk<T, true, 2, 2>
+                                          : k == 3 ? k_fwd_ndhwc_pk<T, true, 3, 3> : k_fwd_ndhwc_pk<T, true, 0, 0>)
+                                       : (k == 2 ? k_fwd_ndhwc_pk<T, false, 2, 2>
+                                          : k == 3 ? k_fwd_ndhwc_pk<T, false, 3, 3> : k_fwd_ndhwc_pk<T, false, 0, 0>);
+                kern<<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
                 return cudaGetLastError();
             }
         }
