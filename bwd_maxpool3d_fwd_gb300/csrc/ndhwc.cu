@@ -287,7 +287,10 @@ k_bwd_ndhwc(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __rest
 // window's CH indices and CH gradients once for all 8 positions, and sums for
 // each position and channel the gradients of the windows whose index is
 // that position (binary32, first term as the initial value, one rounding;
-// +0 where none).
+// +0 where none). Accumulators start at -0, the identity of binary32
+// addition (x + -0 is x for every x, +0 and -0 included), so adding the
+// first term to it gives the first term; a bit per position and channel
+// records whether any term arrived.
 // K > 0: every window is K long on every axis (the covering pairs of window
 // and position are then known at compile time); 0: lengths from g.
 template <typename T, int CH, int K>
@@ -322,7 +325,7 @@ k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __
 #pragma unroll
         for (int p = 0; p < 8; ++p)
 #pragma unroll
-            for (int k = 0; k < CH; ++k) acc[p][k] = 0.0f;
+            for (int k = 0; k < CH; ++k) acc[p][k] = -0.0f;
         const int d0 = 2 * bd, h0 = 2 * bh, w0 = 2 * bw;
         const int s0 = d0 * HW + h0 * g.W + w0;  // in-plane offset of position 0
 #pragma unroll
@@ -350,15 +353,14 @@ k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __
                                             (w0 + 1 < g.W && w0 + 1 < ow * 2 + g.kw ? 2 : 0));
                     if (!dm || !hm || !wm) continue;
                     const long long o = ((((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C) + ch * CH;
+                    // low words of the indices; an index with a nonzero high word
+                    // names no position (all ones never equals an in-plane offset)
                     unsigned lo[CH];
-                    bool hz[CH];
 #pragma unroll
                     for (int q = 0; q < CH / 2; ++q) {
                         const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + o + 2 * q));
-                        lo[2 * q] = iv.x;
-                        lo[2 * q + 1] = iv.z;
-                        hz[2 * q] = iv.y == 0u;
-                        hz[2 * q + 1] = iv.w == 0u;
+                        lo[2 * q] = iv.y == 0u ? iv.x : 0xFFFFFFFFu;
+                        lo[2 * q + 1] = iv.w == 0u ? iv.z : 0xFFFFFFFFu;
                     }
                     float gv[CH];
                     {
@@ -383,10 +385,9 @@ k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __
                         const unsigned sp = (unsigned)(s0 + i * HW + j * g.W + kk);
 #pragma unroll
                         for (int k = 0; k < CH; ++k) {
-                            if (lo[k] == sp && hz[k]) {
-                                const unsigned bit = 1u << (p * CH + k);
-                                acc[p][k] = (any & bit) ? acc[p][k] + gv[k] : gv[k];
-                                any |= bit;
+                            if (lo[k] == sp) {
+                                acc[p][k] += gv[k];
+                                any |= 1u << (p * CH + k);
                             }
                         }
                     }

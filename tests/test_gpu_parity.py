@@ -638,6 +638,11 @@ def test_channels_last(case, dtype, offset):
     assert torch.equal(idx.cpu(), i_ref.permute(0, 2, 3, 4, 1))
     assert_bits_equal(y.cpu(), y_ref.permute(0, 2, 3, 4, 1).contiguous(), "y (channels last)")
     g = torch.randn(y_ref.shape, generator=gen).to(dtype)         # (N, C, OD, OH, OW)
+    if case % 2:
+        # signed zeros and small integers: sums of lone -0 terms stay -0,
+        # -0 + +0 is +0, cancellations give +0
+        pick = torch.randint(0, 5, y_ref.shape, generator=gen)
+        g = torch.tensor([-0.0, 0.0, -0.0, 1.0, -1.0])[pick].to(dtype)
     gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[1:4])
     gd = buf(oshape, dtype)
     gd.copy_(g.permute(0, 2, 3, 4, 1).to(DEV))
