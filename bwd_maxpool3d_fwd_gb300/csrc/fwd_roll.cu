@@ -259,7 +259,7 @@ __device__ __forceinline__ T lane_value(uint32_t word, int lane) {
 // clipped by the input's edges (padding or ceil mode) and take the general
 // scan; KH = KW = 0: every window takes the general scan.
 template <typename T, bool AD, int KH, int KW, bool CLIP>
-__global__ void __launch_bounds__(RF_NT, 4)
+__global__ void __launch_bounds__(RF_NT, CLIP ? 3 : 4)
 k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
            RollFwdGeo rg, const unsigned char* __restrict__ x_end, const __grid_constant__ OutMap om) {
     extern __shared__ __align__(128) unsigned char smem_rf[];
