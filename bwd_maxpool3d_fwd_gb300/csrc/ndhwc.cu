@@ -106,7 +106,7 @@ k_fwd_ndhwc(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ id
 // KH, KW > 0: every window is KH x KW in (h, w); each depth's KH * KW loads
 // are issued together before they are merged (in order).
 template <typename T, bool ADAPTIVE, int KH, int KW>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C) {
     constexpr int VEC = 8;
     const int nch = C / VEC;
@@ -294,7 +294,7 @@ k_bwd_ndhwc(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __rest
 // K > 0: every window is K long on every axis (the covering pairs of window
 // and position are then known at compile time); 0: lengths from g.
 template <typename T, int CH, int K>
-__global__ void __launch_bounds__(256, CH == 2 ? 4 : 2)
+__global__ void __launch_bounds__(256, CH == 2 ? 4 : 3)
 k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
                 int C) {
     static_assert(CH == 2 || CH == 4, "2 or 4 channels per thread");
