@@ -403,12 +403,13 @@ struct RollCfg {
 // 256 threads holding up to 4 windows each (64 registers), at most 54 KB of
 // shared memory, so that four CTAs fit on an SM. A launch compiles for the
 // fewest windows per thread that its h-tiles need. The compiled 3x3x3
-// stride-2 form runs 224 threads: h-tiles of up to 896 windows then fill
-// their 4-per-thread slots more closely (on 112x112 planes, 825 windows in
-// 896 slots rather than 1024; measured 631 us against 658 us on the
-// 32x128x16x112x112 fp16 backward).
+// stride-2 form runs 128 threads at eight CTAs per SM: smaller h-tiles
+// (512 windows each) and more CTAs in flight hide the shared-memory latency
+// of the ordered passes better (on the 32x128x16x112x112 fp16 backward:
+// 224 threads x 4 CTAs 523 us, 192 x 5 514 us, 160 x 6 517 us, 128 x 8
+// 496 us, 96 x 10 558 us, 64 x 16 595 us).
 constexpr RollCfg kRollCfg = {256, 4, 4, 54 * 1024};
-constexpr RollCfg kRollCfgK3 = {192, 4, 5, 44 * 1024};
+constexpr RollCfg kRollCfgK3 = {128, 4, 8, 27 * 1024};
 
 size_t roll_smem(int RS, int SSTR) {
     const size_t nacc = (size_t)RS * SSTR;
