@@ -137,19 +137,30 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-class Runner:
-    """Device buffers and the two entry-point calls for one workload."""
+def channels_last(shape):
+    n, c, d, h, w = shape
+    return (n, d, h, w, c)
 
-    def __init__(self, w, x_cpu, g_cpu, dev, algo=None):
+
+class Runner:
+    """Device buffers and the two entry-point calls for one workload, in the
+    NCDHW layout or (layout "ndhwc") the channels-last one, where x_cpu and
+    g_cpu are given channels-last."""
+
+    def __init__(self, w, x_cpu, g_cpu, dev, algo=None, layout="ncdhw"):
         import bwd_maxpool3d_fwd_gb300 as mp
         self.mp = mp
         self.w = w
         self.dev = dev
+        self.layout = layout
+        cl = layout == "ndhwc"
         self.x = x_cpu.to(dev)
         self.g = g_cpu.to(dev)
-        self.y = torch.empty(w.out_shape, dtype=w.dtype, device=dev)
-        self.idx = torch.empty(w.out_shape, dtype=torch.int64, device=dev)
-        self.gin = torch.empty(w.in_shape, dtype=w.dtype, device=dev)
+        oshape = channels_last(w.out_shape) if cl else w.out_shape
+        self.y = torch.empty(oshape, dtype=w.dtype, device=dev)
+        self.idx = torch.empty(oshape, dtype=torch.int64, device=dev)
+        self.gin = torch.empty(channels_last(w.in_shape) if cl else w.in_shape, dtype=w.dtype,
+                               device=dev)
         self.algo = mp.BWD_AUTO if algo is None else algo
         self.k = w.kernel if w.mode == "fixed" else None
         self.s = w.stride if w.mode == "fixed" else None
@@ -158,6 +169,8 @@ class Runner:
 
     def paths(self):
         mp, w = self.mp, self.w
+        if self.layout == "ndhwc":
+            return "fwd_ndhwc", "bwd_ndhwc"
         if w.mode == "fixed":
             pf = mp.maxpool3d_fwd_plan(w.in_shape, w.kernel, w.stride, w.dtype)
         else:
@@ -187,6 +200,12 @@ class Runner:
         x = self.x if x is None else x
         y = self.y if y is None else y
         idx = self.idx if idx is None else idx
+        if self.layout == "ndhwc":
+            if self.w.mode == "fixed":
+                self.mp.maxpool3d_fwd_ndhwc(x, y, idx, self.w.kernel, self.w.stride)
+            else:
+                self.mp.adaptive_maxpool3d_fwd_ndhwc(x, y, idx, self.w.out)
+            return
         if self.w.mode == "fixed":
             self.mp.maxpool3d_fwd(x, y, idx, self.w.kernel, self.w.stride)
         else:
@@ -196,6 +215,9 @@ class Runner:
         g = self.g if g is None else g
         idx = self.idx if idx is None else idx
         gin = self.gin if gin is None else gin
+        if self.layout == "ndhwc":
+            self.mp.maxpool3d_bwd_ndhwc(g, idx, gin, self.k, self.s)
+            return
         self.mp.maxpool3d_bwd(g, idx, gin, self.k, self.s, algo=self.algo, workspace=self.ws)
 
 
@@ -409,9 +431,9 @@ def e2e(r, x_cpu, g_cpu, steps=5, warmup=2):
     every result (y, idx, grad_in) back to pinned host memory."""
     w = r.w
     xh, gh = x_cpu.pin_memory(), g_cpu.pin_memory()
-    yh = torch.empty(w.out_shape, dtype=w.dtype).pin_memory()
-    ih = torch.empty(w.out_shape, dtype=torch.int64).pin_memory()
-    ginh = torch.empty(w.in_shape, dtype=w.dtype).pin_memory()
+    yh = torch.empty(r.y.shape, dtype=w.dtype).pin_memory()
+    ih = torch.empty(r.idx.shape, dtype=torch.int64).pin_memory()
+    ginh = torch.empty(r.gin.shape, dtype=w.dtype).pin_memory()
     stream = torch.cuda.current_stream()
 
     def step():
@@ -557,12 +579,19 @@ def our_arm(args):
     import bwd_maxpool3d_fwd_gb300 as mp
     mp.lib()                                     # fail loudly if the library is missing
     base = workloads.WORKLOADS[args.workload]
+    cl = args.layout == "ndhwc"
     if args.planes:
         import dataclasses
-        base = dataclasses.replace(base, N=1, C=min(args.planes, base.planes))
+        if cl:   # whole samples: the channel axis stays whole
+            base = dataclasses.replace(base, N=max(1, min(base.N, args.planes // base.C)))
+        else:
+            base = dataclasses.replace(base, N=1, C=min(args.planes, base.planes))
     w = shard_seed(base, rank)
     x_cpu, g_cpu = workloads.make_x(w), workloads.make_grad_out(w)
-    r = Runner(w, x_cpu, g_cpu, dev)
+    if cl:
+        x_cpu = x_cpu.permute(0, 2, 3, 4, 1).contiguous()
+        g_cpu = g_cpu.permute(0, 2, 3, 4, 1).contiguous()
+    r = Runner(w, x_cpu, g_cpu, dev, layout=args.layout)
     peak, peak_kind = hbm_peak()
     fb, bb = algorithmic_bytes(w)
     nf, nb = r.launches_per_step()
@@ -603,7 +632,7 @@ def our_arm(args):
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(kind, w.name, not args.planes),
+                "traffic": recorded_traffic(kind, w.name, not args.planes and not cl),
                 "kernel": pb if kind == "bwd" else pf, "peak_source": peak_kind,
                 "bytes_per_launch": kbytes,
                 "fwd": {"path": pf, "us": round(fwd_ms * 1e3, 2), "bytes": fb,
@@ -630,7 +659,7 @@ def our_arm(args):
         "data": "synthetic (seeded generators; shapes and value recipes of the workload)",
         "config": {"workload": base.name, "input": list(base.in_shape),
                    "output": list(base.out_shape), "kernel": list(base.kernel),
-                   "stride": list(base.stride),
+                   "stride": list(base.stride), "layout": args.layout,
                    "l2": ("inputs larger than L2 (%d MB input); no flush between steps"
                           % (base.planes * base.D * base.H * base.W * base.elem_bytes // 10**6)),
                    "parallelism": f"independent shards x{world}"},
@@ -651,7 +680,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--planes", type=int, default=0,
                     help="run only the first N planes of the workload (same per-plane shape; "
-                         "for profiling small cases)")
+                         "for profiling small cases; whole samples with --layout ndhwc)")
+    ap.add_argument("--layout", choices=("ncdhw", "ndhwc"), default="ncdhw",
+                    help="tensor layout of the timed step (ndhwc: the channels-last entry points)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
