@@ -281,4 +281,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 constexpr unsigned int kErrPipelineTimeout = 1u;
 constexpr int kWaitLimit = 1 << 22;
 
+// The one window length along an axis (fixed windows: K; adaptive windows
+// [floor(i*I/O), ceil((i+1)*I/O)): their common length), or 0 when the
+// lengths differ. Host side, for choosing compiled window shapes.
+inline int uniform_window_len(int I, int O, int K, bool adaptive) {
+    if (!adaptive) return K;
+    int len = -1;
+    for (int i = 0; i < O; ++i) {
+        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
+        if (len >= 0 && l != len) return 0;
+        len = l;
+    }
+    return len;
+}
+
 }  // namespace mp3d

@@ -387,18 +387,6 @@ static bool keyslab_fits(const Geo& g) {
            keyslab_smem(g) <= (size_t)kKeySlabBytes;
 }
 
-// The one window length along an axis, or 0 when lengths differ.
-static int uniform_len(int I, int O, int K, bool adaptive) {
-    if (!adaptive) return K;
-    int len = -1;
-    for (int i = 0; i < O; ++i) {
-        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
-        if (len >= 0 && l != len) return 0;
-        len = l;
-    }
-    return len;
-}
-
 template <typename T, bool AD>
 static auto keyslab_kernel(int kh, int kw) {
     if (kh == kw) {
@@ -417,7 +405,7 @@ template <typename T>
 static cudaError_t keyslab_t(const void* x, void* y, int64_t* idx, const Geo& g, cudaStream_t s) {
     const size_t smem = keyslab_smem(g);
     dim3 grid((unsigned)g.OD, (unsigned)(g.P < 65535 ? g.P : 65535));
-    const int kh = uniform_len(g.H, g.OH, g.kh, g.adaptive), kw = uniform_len(g.W, g.OW, g.kw, g.adaptive);
+    const int kh = uniform_window_len(g.H, g.OH, g.kh, g.adaptive), kw = uniform_window_len(g.W, g.OW, g.kw, g.adaptive);
     auto kern = g.adaptive ? keyslab_kernel<T, true>(kh, kw) : keyslab_kernel<T, false>(kh, kw);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -516,17 +516,6 @@ bool depth_two_cover(const Geo& g) {
     return true;
 }
 
-int uniform_len_rf(int I, int O, int K, bool adaptive) {
-    if (!adaptive) return K;
-    int len = -1;
-    for (int i = 0; i < O; ++i) {
-        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
-        if (len >= 0 && l != len) return 0;
-        len = l;
-    }
-    return len;
-}
-
 // Clipped window bounds along one axis, as the kernels compute them.
 long long h_start(int o, int I, int O, int K, int S, int p, bool ad) {
     if (ad) return (long long)o * I / O;
@@ -672,8 +661,8 @@ cudaError_t rf_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms, cu
     size_t smem = 0;
     const bool pair = plan_rf(g, sms, true, &rg, &smem);
     if (!pair && !plan_rf(g, sms, false, &rg, &smem)) return cudaErrorNotSupported;
-    const int kh = uniform_len_rf(g.H, g.OH, g.kh, g.adaptive);
-    const int kw = uniform_len_rf(g.W, g.OW, g.kw, g.adaptive);
+    const int kh = uniform_window_len(g.H, g.OH, g.kh, g.adaptive);
+    const int kw = uniform_window_len(g.W, g.OW, g.kw, g.adaptive);
     auto kern = pair ? (g.adaptive ? pf_kernel<T, true, false>(kh, kw)
                                    : clips(g) ? pf_kernel<T, false, true>(kh, kw)
                                               : pf_kernel<T, false, false>(kh, kw))

@@ -457,18 +457,6 @@ cudaError_t bwd_t(const void* go, const int64_t* idx, void* gi, const Geo& g, in
     return cudaGetLastError();
 }
 
-// The one window length along an axis, or 0 when lengths differ.
-int uniform_len(int I, int O, int K, bool adaptive) {
-    if (!adaptive) return K;
-    int len = -1;
-    for (int i = 0; i < O; ++i) {
-        const int l = (int)((((long long)(i + 1) * I + O - 1) / O) - ((long long)i * I / O));
-        if (len >= 0 && l != len) return 0;
-        len = l;
-    }
-    return len;
-}
-
 // The winner's offset from its window's first element fits a 16-bit lane
 // for every window of the geometry.
 bool rel_fits(const Geo& g) {
@@ -498,8 +486,8 @@ cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int
             if (rel_fits(g)) {
                 const long long work = (long long)g.P * g.ovol * (C / VEC);
                 // uniform (h, w) window extents 2 or 3: the unrolled form
-                const int kh = uniform_len(g.H, g.OH, g.kh, g.adaptive);
-                const int kw = uniform_len(g.W, g.OW, g.kw, g.adaptive);
+                const int kh = uniform_window_len(g.H, g.OH, g.kh, g.adaptive);
+                const int kw = uniform_window_len(g.W, g.OW, g.kw, g.adaptive);
                 const int k = kh == kw && (kh == 2 || kh == 3) ? kh : 0;
                 auto kern = g.adaptive ? (k == 2 ? k_fwd_ndhwc_pk<T, true, 2, 2>
                                           : k == 3 ? k_fwd_ndhwc_pk<T, true, 3, 3> : k_fwd_ndhwc_pk<T, true, 0, 0>)
