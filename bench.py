@@ -425,36 +425,62 @@ def smi_id(dev):
 
 # ---------------------------------------------------------------- e2e
 
-def e2e(r, x_cpu, g_cpu, steps=5, warmup=2):
+def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
     """Same metric through the public API with host buffers: each step copies
-    the inputs from pinned host memory, runs forward + backward, and copies
-    every result (y, idx, grad_in) back to pinned host memory."""
+    its inputs from pinned host memory, runs forward + backward, and copies
+    every result (y, idx, grad_in) back to pinned host memory. Steps are
+    pipelined the way a data loader would run them: two sets of device
+    buffers, the copies in, the compute and the copies out on three streams
+    ordered by events, so step k + 1's inputs travel while step k computes
+    and step k - 1's results come back. The timed region runs from the first
+    copy in to the last copy out."""
     w = r.w
     xh, gh = x_cpu.pin_memory(), g_cpu.pin_memory()
     yh = torch.empty(r.y.shape, dtype=w.dtype).pin_memory()
     ih = torch.empty(r.idx.shape, dtype=torch.int64).pin_memory()
     ginh = torch.empty(r.gin.shape, dtype=w.dtype).pin_memory()
-    stream = torch.cuda.current_stream()
+    bufs = [(r.x, r.g, r.y, r.idx, r.gin),
+            tuple(torch.empty_like(t) for t in (r.x, r.g, r.y, r.idx, r.gin))]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    cmp_done = [ev(), ev()]   # compute of the set's last step (it read x, g)
+    out_done = [ev(), ev()]   # copies out of the set's last step (they read y, idx, grad_in)
+    for e in cmp_done + out_done:
+        e.record(torch.cuda.current_stream())
 
-    def step():
-        r.x.copy_(xh, non_blocking=True)
-        r.g.copy_(gh, non_blocking=True)
-        r.fwd()
-        r.bwd()
-        yh.copy_(r.y, non_blocking=True)
-        ih.copy_(r.idx, non_blocking=True)
-        ginh.copy_(r.gin, non_blocking=True)
+    def step(k):
+        x, g, y, idx, gin = bufs[k % 2]
+        in_done = ev()
+        s_in.wait_event(cmp_done[k % 2])
+        with torch.cuda.stream(s_in):
+            x.copy_(xh, non_blocking=True)
+            g.copy_(gh, non_blocking=True)
+            in_done.record(s_in)
+        s_cmp.wait_event(in_done)
+        s_cmp.wait_event(out_done[k % 2])
+        with torch.cuda.stream(s_cmp):
+            r.fwd(x, y, idx)
+            r.bwd(g, idx, gin)
+            cmp_done[k % 2].record(s_cmp)
+        s_out.wait_event(cmp_done[k % 2])
+        with torch.cuda.stream(s_out):
+            yh.copy_(y, non_blocking=True)
+            ih.copy_(idx, non_blocking=True)
+            ginh.copy_(gin, non_blocking=True)
+            out_done[k % 2].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for k in range(warmup):
+        step(k)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_in)
+    for k in range(steps):
+        step(warmup + k)
+    b.record(s_out)
     b.synchronize()
+    torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    del bufs
     fb, bb = algorithmic_bytes(w)
     h2d = xh.numel() * xh.element_size() + gh.numel() * gh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in (yh, ih, ginh))
