@@ -667,6 +667,8 @@ ANY_BITS_CASES = [
     ((2, 2, 7, 5, 9), (8, 6, 4)),       # more depth windows than slices
     ((1, 3, 8, 10, 12), (3, 4, 5)),     # plane pairs (volume a multiple of 8), a lone last plane
     ((1, 5, 16, 8, 8), (6, 3, 3)),
+    ((1, 3, 8, 4, 10), (9, 3, 5)),      # plane pairs, more depth windows than slices
+    ((1, 2, 6, 96, 64), (3, 40, 30)),   # plane pairs in bands of output rows (1200 outputs a depth)
 ]
 
 
@@ -697,3 +699,22 @@ def test_slab_forward_any_bits(case, nan_share, dtype):
     y, idx = gpu_fwd(x, out_size=out)
     assert torch.equal(idx, i_ref), f"idx differs ({shape} -> {out}, nan share {nan_share})"
     assert torch.equal(bits(y), bits(y_ref)), "y must be the chosen element's own bits"
+
+
+# The depth walk needs x on a 16-byte boundary; a view one element off takes
+# another forward path with the same results.
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=str)
+def test_depth_walk_unaligned_input_falls_back(dtype):
+    shape, out = (1, 4, 8, 10, 12), (3, 4, 5)
+    gen = torch.Generator().manual_seed(9990)
+    x = random_input(gen, shape, dtype, "special")
+    y_ref, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    n = x.numel()
+    xd = torch.empty(n + 1, dtype=dtype, device=DEV)[1:].view(shape)
+    xd.copy_(x.to(DEV))
+    y = torch.empty(y_ref.shape, dtype=dtype, device=DEV)
+    idx = torch.empty(y_ref.shape, dtype=torch.int64, device=DEV)
+    mp.adaptive_maxpool3d_fwd(xd, y, idx, out)
+    torch.cuda.synchronize()
+    assert torch.equal(idx.cpu(), i_ref)
+    assert_bits_equal(y.cpu(), y_ref, "y (unaligned x)")
