@@ -357,6 +357,7 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     int ao0[2] = {0, 0}, ao1[2] = {0, 0};
     bool fresh0 = true, fresh1 = true, bad0 = false, bad1 = false;
     bool failed = false;
+    __shared__ int fail_at;                    // (thread 0) the slice whose wait gave up
     unsigned redo = 0u;                        // depth windows (bit a - od0) seen with NaN or inf
     int a = od0;
     int a_start = d_first;
@@ -365,6 +366,7 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     for (int i = 0; i < ns; ++i) {
         if (!failed && !mbar_wait(smem_addr(&bars[i % PF_NS]), (uint32_t)((i / PF_NS) & 1), kWaitLimit)) {
             failed = true;
+            if (tid == 0) fail_at = i;
             atomicOr(&g_mp3d_roll_error, kErrPipelineTimeout);
         }
         const unsigned char* sa = xb0 + (size_t)(d_first + i) * HW * sizeof(T);
@@ -488,6 +490,12 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             }
         }
     }
+    // after thread 0's wait gave up at slice f, let the copies still in
+    // flight land before the CTA exits: thread 0 issued nothing after that
+    // wait, so they are among slices [f, f + NS)
+    if (failed && tid == 0)
+        for (int k = fail_at; k < fail_at + PF_NS && k < ns; ++k)
+            mbar_wait(smem_addr(&bars[k % PF_NS]), (uint32_t)((k / PF_NS) & 1), kWaitLimit);
     // outputs whose windows held a NaN or an infinity: the exact scalar scan
     while (redo) {
         const int r = od0 + __ffs(redo) - 1;
