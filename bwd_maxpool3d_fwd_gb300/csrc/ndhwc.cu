@@ -292,9 +292,12 @@ k_bwd_ndhwc(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __rest
 // first term to it gives the first term; a bit per position and channel
 // records whether any term arrived.
 // K > 0: every window is K long on every axis (the covering pairs of window
-// and position are then known at compile time); 0: lengths from g.
+// and position are then known at compile time); 0: lengths from g. Four
+// CTAs per SM for K = 3 (it spills a few registers there and is still
+// faster: 1124 -> 1055 us on the 32x128x16x112x112 fp16 backward), three
+// otherwise.
 template <typename T, int CH, int K>
-__global__ void __launch_bounds__(256, CH == 2 ? 4 : 3)
+__global__ void __launch_bounds__(256, K == 3 ? 4 : 3)
 k_bwd_ndhwc_blk(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
                 int C) {
     static_assert(CH == 2 || CH == 4, "2 or 4 channels per thread");
