@@ -293,9 +293,9 @@ int maxpool3d_bwd_noalloc(const void* grad_out, const int64_t* idx, void* grad_i
                           int dtype, cudaStream_t stream);
 
 /* Error flags raised on the device by a kernel whose bounded wait for an
- * asynchronous copy gave up (bit 0: the forward's copy pipeline timed out;
- * the kernel then leaves its outputs unwritten and exits). Not expected in
- * normal operation. Reads the current device's flags into *flags (clearing
+ * asynchronous copy gave up (bit 0: the copy pipeline of a forward kernel,
+ * the stride-2 one or the depth walk, timed out; that call's outputs are
+ * then incomplete and must not be used). Not expected in normal operation. Reads the current device's flags into *flags (clearing
  * them if clear != 0); this call waits for the device to finish prior work.
  * No counterpart on the pages: it exists because the library's kernels
  * never trap or spin without limit. */
