@@ -344,6 +344,16 @@ def cpu_baseline(w, target_s=12.0):
                       f"{dt:.1f} s on 1 host core (host has {os.cpu_count()} cores)"}
 
 
+def workload_config(base, layout, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": base.name, "input": list(base.in_shape),
+            "output": list(base.out_shape), "kernel": list(base.kernel),
+            "stride": list(base.stride), "layout": layout,
+            "l2": ("inputs larger than L2 (%d MB input); no flush between steps"
+                   % (base.planes * base.D * base.H * base.W * base.elem_bytes // 10**6)),
+            "parallelism": f"independent shards x{world}"}
+
+
 def reference_arm(args):
     """The oracle as the reference implementation, timed on the host cores."""
     w = workloads.WORKLOADS[args.workload]
@@ -369,7 +379,7 @@ def reference_arm(args):
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
             "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "planes_per_step": n},
+            "config": dict(workload_config(w, "ncdhw", 1), planes_per_step=n),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -683,12 +693,7 @@ def our_arm(args):
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
         "data": "synthetic (seeded generators; shapes and value recipes of the workload)",
-        "config": {"workload": base.name, "input": list(base.in_shape),
-                   "output": list(base.out_shape), "kernel": list(base.kernel),
-                   "stride": list(base.stride), "layout": args.layout,
-                   "l2": ("inputs larger than L2 (%d MB input); no flush between steps"
-                          % (base.planes * base.D * base.H * base.W * base.elem_bytes // 10**6)),
-                   "parallelism": f"independent shards x{world}"},
+        "config": workload_config(base, args.layout, world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e_res,
         "gpu_launches": (nf + nb) * args.steps, "clocks": clocks,
         "per_config": cfg,
