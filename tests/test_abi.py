@@ -264,3 +264,24 @@ def test_recompute_argument_errors_and_plans(L, bufs):
                                            bf) == "bwd_recompute_direct"
     assert mp.maxpool3d_bwd_recompute_plan((2, 3, 9, 9, 9), (4, 4, 4), None, None,
                                            bf) == "bwd_recompute_direct"
+
+
+def test_path_names_cover_the_header():
+    # every mp3d_path value the header declares has a name in the binding
+    src = open(os.path.join(ROOT, "include", "mp3d.h")).read()
+    values = {int(v) for v in re.findall(r"MP3D_PATH_\w+\s*=\s*(\d+)", src)}
+    assert values and values == set(mp.PATHS), sorted(values ^ set(mp.PATHS))
+
+
+def test_depth_walk_plans(L):
+    f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
+    # the adaptive workload shape, both 16-bit types; fp32 keeps the slab
+    for dt in (f16, bf16):
+        assert mp.adaptive_maxpool3d_fwd_plan((2, 3, 30, 50, 50), (8, 12, 12), dt) == "fwd_roll"
+    assert mp.adaptive_maxpool3d_fwd_plan((2, 3, 30, 50, 50), (8, 12, 12), f32) == "fwd_slab"
+    # three windows over a depth slice (kernel 3, stride 1 along d): not the walk
+    assert mp.maxpool3d_fwd_plan((1, 2, 8, 9, 10), (3, 2, 2), (1, 2, 2), f16) != "fwd_roll"
+    # more outputs per depth than a CTA has threads: bands of output rows
+    assert mp.adaptive_maxpool3d_fwd_plan((1, 2, 9, 40, 40), (4, 20, 20), f16) == "fwd_roll"
+    # more than 65536 elements per slice: not the walk
+    assert mp.adaptive_maxpool3d_fwd_plan((1, 1, 4, 300, 300), (2, 10, 10), f16) != "fwd_roll"
