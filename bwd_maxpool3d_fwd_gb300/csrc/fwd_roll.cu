@@ -1,6 +1,9 @@
-// Forward for 16-bit types as a walk along depth: one CTA takes one plane
-// and a group of consecutive output depths, and streams the depth slices
-// its windows cover, in ascending order, through shared memory.
+// Forward for 16-bit types as a walk along depth: a CTA takes one plane (or
+// two, in the plane-pair form further down, which the launcher prefers) and
+// a group of consecutive output depths, and streams the depth slices its
+// windows cover, in ascending order, through shared memory. This first form
+// (order words, one plane) serves plane volumes that are not a multiple of
+// 8 elements.
 //
 // Definition followed (teenygrad docs "Struct Maxpool3dForward",
 // description and Constraints; adaptive windows
@@ -24,10 +27,10 @@
 //     a tie. When the last slice of a depth window has been folded in, the
 //     output is written: idx from the slice and the in-slice offset, y
 //     re-read from x at that offset (the element's own bits).
-// Scope: 16-bit types, no padding or dilation, at most two windows over any
-// slice along d (fixed K <= 2 * S, or adaptive end(i) <= start(i + 2)),
-// H * W <= 65536 (in-slice offsets fit 16 bits), OH * OW <= threads, x on a
-// 16-byte boundary.
+// Scope of this form: 16-bit types, no padding or dilation, every window
+// inside the input, at most two windows over any slice along d (fixed
+// K <= 2 * S, or adaptive end(i) <= start(i + 2)), H * W <= 65536 (in-slice
+// offsets fit 16 bits), OH * OW <= threads, x on a 16-byte boundary.
 #include <climits>
 #include <cstring>
 #include <vector>
