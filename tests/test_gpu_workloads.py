@@ -1,7 +1,8 @@
 """The five workloads at full size, through the same entry points the
 benchmark times (needs a GPU). Workloads 0, 1, 2 and 4 are compared with
 the oracle in full; workload 3 (822M inputs) on a sample of planes, plus
-properties checked on every output."""
+properties checked on every output. The padded workload the benchmark also
+times is compared in full."""
 import pytest
 import torch
 
@@ -91,3 +92,24 @@ def test_workload3_sampled_and_properties():
         len(planes), *w.out, 27)
     repeats = (win == win.max(dim=-1, keepdim=True).values).sum(-1)
     assert int((repeats > 1).sum()) > 0.01 * repeats.numel()
+
+
+def test_padded_workload_full():
+    # the padded workload the benchmark times (3x3x3, stride 2, padding 1,
+    # fp16, 8x64x16x56x56), forward and backward in full against the oracle
+    shape, k, s, p, dl = (8, 64, 16, 56, 56), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1)
+    gen = torch.Generator().manual_seed(20261302)
+    x = torch.randn(shape, generator=gen).half()
+    y_ref, i_ref = oracle.maxpool3d_fwd_ex(x, k, s, p, dl, False)
+    g = torch.randn(y_ref.shape, generator=gen).half()
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    xd, gd = x.to(DEV), g.to(DEV)
+    y = torch.empty(y_ref.shape, dtype=x.dtype, device=DEV)
+    idx = torch.empty(y_ref.shape, dtype=torch.int64, device=DEV)
+    gin = torch.empty(shape, dtype=x.dtype, device=DEV)
+    mp.maxpool3d_fwd_ex(xd, y, idx, k, s, p, dl)
+    mp.maxpool3d_bwd_ex(gd, idx, gin, k, s, p, dl)
+    torch.cuda.synchronize()
+    assert torch.equal(idx.cpu(), i_ref)
+    assert_bits_equal(y.cpu(), y_ref, "y (padded workload)")
+    assert_bits_equal(gin.cpu(), gin_ref, "grad_in (padded workload)")
