@@ -372,6 +372,46 @@ def check_bwd_against_exact_sum(orc):
                     assert abs(gi[p, j] - exact) <= tol, (p, j, gi[p, j], exact, tol)
 
 
+def check_bwd_signed_zero(orc):
+    """Sums of signed zeros, with the sign IEEE 754 (section 6.3) fixes for
+    a sum in round-to-nearest: a lone contribution is the gradient itself
+    (the disjoint gather writes it bit for bit, [AMPB] Summary), so a lone
+    -0 stays -0; -0 + -0 is -0; zeros of opposite signs, in either order,
+    and an exact cancellation x + (-x) give +0; an input nobody selects is
+    +0. Expected values are written out per case, not computed."""
+    NEG, POS = -0.0, 0.0
+    # (contributions in ascending output order, expected result)
+    cases = [
+        ([NEG], NEG),
+        ([NEG, NEG], NEG),
+        ([NEG, POS], POS),
+        ([POS, NEG], POS),
+        ([NEG, NEG, NEG], NEG),
+        ([1.5, -1.5], POS),
+        ([-1.5, 1.5, NEG], POS),
+        ([NEG, 2.0, -2.0], POS),
+        ([], POS),
+    ]
+    targets, grads = [], []
+    # interleave the inputs' contributions so that each input's terms are
+    # spread over the output order
+    longest = max(len(c) for c, _ in cases)
+    for k in range(longest):
+        for j, (terms, _) in enumerate(cases):
+            if k < len(terms):
+                targets.append(j)
+                grads.append(terms[k])
+    n = len(grads)
+    idx = torch.tensor(targets, dtype=torch.int64).reshape(1, 1, 1, 1, n)
+    for dtype in DTYPES:
+        go = torch.tensor(grads, dtype=torch.float32).to(dtype).reshape(1, 1, 1, 1, n)
+        gin = orc.maxpool3d_bwd(go, idx, (1, 1, len(cases)))
+        got = gin.float().reshape(-1).tolist()
+        for j, (terms, want) in enumerate(cases):
+            assert got[j] == want and math.copysign(1.0, got[j]) == math.copysign(1.0, want), (
+                dtype, terms, got[j], want)
+
+
 # ----------------------------------------------------- padding and dilation
 # The forward with padding, dilation and ceil mode against torch's CPU
 # max_pool1d / max_pool3d (a library routine whose tie rule, for values
@@ -468,6 +508,6 @@ ALL_CHECKS = [
     check_fixed_windows, check_fwd_bruteforce_fixed, check_fwd_bruteforce_adaptive,
     check_fwd_hand_examples, check_fwd_identity, check_fixed_equals_divisible_adaptive,
     check_bwd_hand_examples, check_bwd_disjoint_bijection, check_bwd_integer_sum_conserved,
-    check_bwd_against_exact_sum, check_ex_out_size_vs_torch, check_fwd_ex_vs_torch,
+    check_bwd_against_exact_sum, check_bwd_signed_zero, check_ex_out_size_vs_torch, check_fwd_ex_vs_torch,
     check_fwd_ex_16bit_vs_torch, check_fwd_ex_reduces_to_plain,
 ]

@@ -29,6 +29,7 @@ MUTANTS = {
         "{ store_rounded(dtype, gin, p * in_vol, acc[target] + gv);"
         " acc[target] = load_f32(dtype, gin, p * in_vol); }"),
     "bwd_empty_is_negative_zero": ("seen[j] ? acc[j] : 0.0f", "seen[j] ? acc[j] : -0.0f"),
+    "bwd_sum_starts_at_positive_zero": ("acc[target] = gv;", "acc[target] = 0.0f + gv;"),
     "round_ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
     "f16_subnormal_scale": ("(float)frac * 0x1p-24f", "(float)frac * 0x1p-25f"),
     "f16_exponent_bias": ("((e - 15 + 127) << 23)", "((e - 14 + 127) << 23)"),
