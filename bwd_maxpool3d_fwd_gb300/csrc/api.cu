@@ -380,6 +380,29 @@ int bwd_ex_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, in
 
 extern "C" {
 
+int maxpool3d_out_size(int64_t D, int64_t H, int64_t W, int kd, int kh, int kw, int sd, int sh,
+                       int sw, int* od, int* oh, int* ow) {
+    if (!od || !oh || !ow) return MP3D_ERR_NULLPTR;
+    Geo g;
+    int st = check_dims(1, 1, D, H, W, &g);
+    if (!st) st = fixed_geo(&g, kd, kh, kw, sd, sh, sw);
+    if (st) return st;
+    *od = g.OD; *oh = g.OH; *ow = g.OW;
+    return MP3D_OK;
+}
+
+int maxpool3d_ex_out_size(int64_t D, int64_t H, int64_t W, int kd, int kh, int kw, int sd, int sh,
+                          int sw, int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                          int* od, int* oh, int* ow) {
+    if (!od || !oh || !ow) return MP3D_ERR_NULLPTR;
+    Geo g;
+    int st = check_dims(1, 1, D, H, W, &g);
+    if (!st) st = ex_geo(&g, kd, kh, kw, sd, sh, sw, pd, ph, pw, dd, dh, dw, ceil_mode);
+    if (st) return st;
+    *od = g.OD; *oh = g.OH; *ow = g.OW;
+    return MP3D_OK;
+}
+
 int maxpool3d_fwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int kd, int kh,
                        int kw, int sd, int sh, int sw, int dtype, int* path) {
     Geo g;

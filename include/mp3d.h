@@ -102,6 +102,19 @@ typedef enum {
 } mp3d_path;
 
 /*
+ * Output sizes of the fixed-window forward [MPF] (Constraints: no padding,
+ * OD = (D - KD)/STRIDE_D + 1, likewise OH and OW): the sizes maxpool3d_fwd
+ * writes and maxpool3d_bwd expects for this input and window. Checks the
+ * arguments as maxpool3d_fwd does (sizes >= 1 with D*H*W below 2^31;
+ * 1 <= k <= input size and s >= 1 on every axis). On MP3D_OK stores the
+ * sizes in *od, *oh, *ow; otherwise returns MP3D_ERR_SHAPE or
+ * MP3D_ERR_WINDOW (MP3D_ERR_NULLPTR for a NULL result pointer) and stores
+ * nothing. Host only: no CUDA call.
+ */
+int maxpool3d_out_size(int64_t D, int64_t H, int64_t W, int kd, int kh, int kw,
+                       int sd, int sh, int sw, int* od, int* oh, int* ow);
+
+/*
  * Fixed-window forward [MPF]. x: [N, C, D, H, W]; y: [N, C, OD, OH, OW] of
  * the same type; idx: int64 [N, C, OD, OH, OW], with
  * OD = (D - kd)/sd + 1, OH = (H - kh)/sh + 1, OW = (W - kw)/sw + 1
@@ -250,6 +263,14 @@ int maxpool3d_bwd_ex(const void* grad_out, const int64_t* idx, void* grad_in,
                      int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
                      int dtype, int algo, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+/* Output sizes of maxpool3d_fwd_ex (the rule above), with its checks: on
+ * MP3D_OK stores them in *od, *oh, *ow; an invalid geometry (including one
+ * with a window that holds no input position) returns MP3D_ERR_WINDOW, bad
+ * sizes MP3D_ERR_SHAPE, and nothing is stored. Host only: no CUDA call. */
+int maxpool3d_ex_out_size(int64_t D, int64_t H, int64_t W,
+                          int kd, int kh, int kw, int sd, int sh, int sw,
+                          int pd, int ph, int pw, int dd, int dh, int dw, int ceil_mode,
+                          int* od, int* oh, int* ow);
 /* Path the padded calls take (mp3d_path), with the same checks. */
 int maxpool3d_fwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                           int kd, int kh, int kw, int sd, int sh, int sw,

@@ -235,15 +235,107 @@ def test_padded_plans(L):
                                     True, f32) == "fwd_padded"
 
 
+def _has_empty_window(I, K, S, p, dl, O):
+    """Some window o < O has no position o*S - p + k*dl inside [0, I)."""
+    return any(all(not (0 <= o * S - p + k * dl < I) for k in range(K)) for o in range(O))
+
+
 def test_padded_out_size_matches_oracle(orc):
+    # the library's size query (one axis at a time, the others of size 1)
+    # against the oracle's; where the library refuses a geometry the oracle
+    # sizes, a window must hold no input position
     for I in range(1, 12):
         for K in range(1, 5):
             for S in range(1, 4):
                 for p in range(0, 3):
                     for dl in range(1, 4):
                         for cm in (False, True):
-                            (got,) = mp.pool_out_size_ex((I,), (K,), (S,), (p,), (dl,), cm)
-                            assert got == orc.ex_out_size(I, K, S, p, dl, cm), (I, K, S, p, dl, cm)
+                            want = orc.ex_out_size(I, K, S, p, dl, cm)
+                            try:
+                                got = mp.pool_out_size_ex((I, 1, 1), (K, 1, 1), (S, 1, 1), (p, 0, 0),
+                                                          (dl, 1, 1), cm)[0]
+                            except mp.MP3DError as e:
+                                assert e.status == WINDOW
+                                assert want == 0 or _has_empty_window(I, K, S, p, dl, want), (
+                                    I, K, S, p, dl, cm)
+                                continue
+                            assert got == want, (I, K, S, p, dl, cm)
+
+
+def test_out_size_queries(L):
+    od, oh, ow = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    r = (ctypes.byref(od), ctypes.byref(oh), ctypes.byref(ow))
+    assert L.maxpool3d_out_size(16, 112, 112, 3, 3, 3, 2, 2, 2, *r) == OK
+    assert (od.value, oh.value, ow.value) == (7, 55, 55)
+    assert L.maxpool3d_out_size(32, 64, 64, 2, 2, 2, 2, 2, 2, *r) == OK
+    assert (od.value, oh.value, ow.value) == (16, 32, 32)
+    od.value = -5
+    assert L.maxpool3d_out_size(4, 4, 4, 5, 2, 2, 1, 1, 1, *r) == WINDOW     # kernel > input
+    assert L.maxpool3d_out_size(4, 4, 4, 2, 2, 2, 0, 1, 1, *r) == WINDOW     # stride 0
+    assert L.maxpool3d_out_size(0, 4, 4, 2, 2, 2, 1, 1, 1, *r) == SHAPE
+    assert L.maxpool3d_out_size(1 << 20, 1 << 11, 2, 1, 1, 1, 1, 1, 1, *r) == SHAPE   # volume 2^32
+    assert od.value == -5                                                   # nothing stored
+    assert L.maxpool3d_out_size(4, 4, 4, 2, 2, 2, 2, 2, 2, None, r[1], r[2]) == NULLPTR
+    assert L.maxpool3d_ex_out_size(16, 56, 56, 3, 3, 3, 2, 2, 2, 1, 1, 1, 1, 1, 1, 0, *r) == OK
+    assert (od.value, oh.value, ow.value) == (8, 28, 28)
+    assert L.maxpool3d_ex_out_size(9, 9, 9, 2, 2, 2, 2, 2, 2, 0, 0, 0, 1, 1, 1, 1, *r) == OK
+    assert (od.value, oh.value, ow.value) == (5, 5, 5)                      # ceil mode
+    assert L.maxpool3d_ex_out_size(9, 9, 9, 2, 2, 2, 2, 2, 2, 2, 0, 0, 1, 1, 1, 0, *r) == WINDOW
+    # the binding's helpers are the library's answers
+    assert mp.pool_out_size((16, 112, 112), (3, 3, 3), (2, 2, 2)) == (7, 55, 55)
+    with pytest.raises(mp.MP3DError):
+        mp.pool_out_size((4, 4, 4), (5, 2, 2), (1, 1, 1))
+
+
+def test_binding_has_no_size_arithmetic():
+    # output sizes come from the library; the binding restates no formula
+    src = open(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "__init__.py")).read()
+    assert "//" not in src
+
+
+def test_binding_checks_buffers_before_any_call():
+    # wrong shapes and types raise before a pointer is handed over; these
+    # tensors live on the CPU (no GPU here), so reaching the device check
+    # would raise a different error
+    x = torch.empty((2, 3, 8, 8, 8), dtype=torch.float16)
+    y = torch.empty((2, 3, 4, 4, 4), dtype=torch.float16)
+    idx = torch.empty((2, 3, 4, 4, 4), dtype=torch.int64)
+    k = s = (2, 2, 2)
+    with pytest.raises(ValueError, match="y: shape"):
+        mp.maxpool3d_fwd(x, y[:, :, :3], idx, k, s)                      # short y
+    with pytest.raises(TypeError, match="idx: dtype"):
+        mp.maxpool3d_fwd(x, y, idx.int(), k, s)                          # int32 idx
+    with pytest.raises(TypeError, match="y: dtype"):
+        mp.maxpool3d_fwd(x, y.float(), idx, k, s)                        # y of another type
+    with pytest.raises(ValueError, match="y: shape"):
+        mp.adaptive_maxpool3d_fwd(x, y, idx, (4, 4, 3))
+    with pytest.raises(ValueError, match="y: shape"):
+        mp.maxpool3d_fwd_ex(x, y, idx, (3, 3, 3), (2, 2, 2))             # 3x3x3 outputs
+    with pytest.raises(ValueError, match="CUDA"):
+        mp.maxpool3d_fwd(x, y, idx, k, s)                                # all checks passed
+    gin = torch.empty_like(x)
+    with pytest.raises(TypeError, match="idx: dtype"):
+        mp.maxpool3d_bwd(y, idx.int(), gin, k, s)
+    with pytest.raises(ValueError, match="idx: shape"):
+        mp.maxpool3d_bwd(y, idx[:1], gin, k, s)
+    with pytest.raises(TypeError, match="grad_out: dtype"):
+        mp.maxpool3d_bwd(y.float(), idx, gin, k, s)
+    with pytest.raises(ValueError, match="the window gives"):
+        mp.maxpool3d_bwd(y, idx, gin, (3, 3, 3), (2, 2, 2))
+    with pytest.raises(ValueError, match="grad_out: shape"):
+        mp.maxpool3d_bwd(y[:1], idx[:1], gin, k, s)                      # batch mismatch
+    with pytest.raises(ValueError, match="x: shape"):
+        mp.maxpool3d_bwd_recompute(x[:1], y, gin, k, s)
+    with pytest.raises(ValueError, match="idx: shape"):
+        mp.maxpool3d_bwd_noalloc(y, idx[:, :1], gin, k, s)
+    xl = torch.empty((2, 8, 8, 8, 3), dtype=torch.float16)
+    yl = torch.empty((2, 4, 4, 4, 3), dtype=torch.float16)
+    with pytest.raises(ValueError, match="y: shape"):
+        mp.maxpool3d_fwd_ndhwc(xl, yl[..., :2], None, k, s)
+    with pytest.raises(ValueError, match="grad_out: shape"):
+        mp.maxpool3d_bwd_ndhwc(yl[..., :2], idx, xl, k, s)
+    with pytest.raises(ValueError, match="5-D"):
+        mp.maxpool3d_fwd(x[0], y, idx, k, s)
 
 
 def test_recompute_argument_errors_and_plans(L, bufs):
