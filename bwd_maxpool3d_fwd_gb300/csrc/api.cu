@@ -265,50 +265,9 @@ int check_fwd_buffers(const void* x, const void* y, const int64_t* idx, const Ge
     return MP3D_OK;
 }
 
-int bwd_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
-            int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype, int algo) {
-    int st = check_dims(N, C, D, H, W, g);
-    if (st) return st;
-    const bool all_zero = !kd && !kh && !kw && !sd && !sh && !sw;
-    if (all_zero) {
-        st = adaptive_geo(g, od, oh, ow);
-    } else {
-        st = fixed_geo(g, kd, kh, kw, sd, sh, sw);
-        if (!st && (g->OD != od || g->OH != oh || g->OW != ow)) st = MP3D_ERR_WINDOW;
-    }
-    if (st) return st;
-    if (elem_size(dtype) == 0) return MP3D_ERR_DTYPE;
-    if (algo < MP3D_BWD_AUTO || algo > MP3D_BWD_ATOMIC) return MP3D_ERR_ALGO;
-    return MP3D_OK;
-}
-
 size_t workspace_needed(const Geo& g, int dtype, int algo) {
     if (algo != MP3D_BWD_ATOMIC || dtype == MP3D_F32) return 0;
     return (size_t)(g.P * (long long)g.vol) * sizeof(float);
-}
-
-// Buffer checks of a backward call (before any CUDA call).
-int check_bwd_buffers(const void* grad_out, const int64_t* idx, const void* grad_in,
-                      const void* workspace, size_t workspace_bytes, const Geo& g, int dtype,
-                      int algo) {
-    const int es = elem_size(dtype);
-    const size_t need = workspace_needed(g, dtype, algo);
-    if (g.P == 0) return MP3D_OK;
-    if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
-    if (misaligned(grad_out, es) || misaligned(idx, 8) || misaligned(grad_in, es))
-        return MP3D_ERR_ALIGN;
-    const long long ng = g.P * g.ovol * es, ni = g.P * g.ovol * 8, nin = g.P * g.vol * es;
-    if (overlaps(grad_in, nin, grad_out, ng) || overlaps(grad_in, nin, idx, ni))
-        return MP3D_ERR_ALIAS;
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need || misaligned(workspace, 16))
-            return MP3D_ERR_WORKSPACE;
-        if (overlaps(workspace, (long long)need, grad_in, nin) ||
-            overlaps(workspace, (long long)need, grad_out, ng) ||
-            overlaps(workspace, (long long)need, idx, ni))
-            return MP3D_ERR_ALIAS;
-    }
-    return MP3D_OK;
 }
 
 // Path choice and launch of a checked backward call on the plain (unpadded)
@@ -375,6 +334,53 @@ int bwd_ex_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, in
 }
 
 }  // namespace
+
+namespace mp3d {
+
+// Geometry of a backward call (maxpool3d_bwd's checks of sizes, window,
+// dtype and algorithm).
+int bwd_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+            int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype, int algo) {
+    int st = check_dims(N, C, D, H, W, g);
+    if (st) return st;
+    const bool all_zero = !kd && !kh && !kw && !sd && !sh && !sw;
+    if (all_zero) {
+        st = adaptive_geo(g, od, oh, ow);
+    } else {
+        st = fixed_geo(g, kd, kh, kw, sd, sh, sw);
+        if (!st && (g->OD != od || g->OH != oh || g->OW != ow)) st = MP3D_ERR_WINDOW;
+    }
+    if (st) return st;
+    if (elem_size(dtype) == 0) return MP3D_ERR_DTYPE;
+    if (algo < MP3D_BWD_AUTO || algo > MP3D_BWD_ATOMIC) return MP3D_ERR_ALGO;
+    return MP3D_OK;
+}
+
+// Buffer checks of a backward call (before any CUDA call).
+int check_bwd_buffers(const void* grad_out, const int64_t* idx, const void* grad_in,
+                      const void* workspace, size_t workspace_bytes, const Geo& g, int dtype,
+                      int algo) {
+    const int es = elem_size(dtype);
+    const size_t need = workspace_needed(g, dtype, algo);
+    if (g.P == 0) return MP3D_OK;
+    if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
+    if (misaligned(grad_out, es) || misaligned(idx, 8) || misaligned(grad_in, es))
+        return MP3D_ERR_ALIGN;
+    const long long ng = g.P * g.ovol * es, ni = g.P * g.ovol * 8, nin = g.P * g.vol * es;
+    if (overlaps(grad_in, nin, grad_out, ng) || overlaps(grad_in, nin, idx, ni))
+        return MP3D_ERR_ALIAS;
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need || misaligned(workspace, 16))
+            return MP3D_ERR_WORKSPACE;
+        if (overlaps(workspace, (long long)need, grad_in, nin) ||
+            overlaps(workspace, (long long)need, grad_out, ng) ||
+            overlaps(workspace, (long long)need, idx, ni))
+            return MP3D_ERR_ALIAS;
+    }
+    return MP3D_OK;
+}
+
+}  // namespace mp3d
 
 // ==================================================================== C ABI
 
@@ -638,6 +644,8 @@ int mp3d_device_error_flags(unsigned int* flags, int clear) {
     if (!flags) return MP3D_ERR_NULLPTR;
     return read_device_error(flags, clear != 0) == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
 }
+
+int mp3d_set_pipeline_wait_limit(int polls) { return set_pipeline_wait_limit(polls); }
 
 const char* mp3d_status_string(int status) {
     switch (status) {

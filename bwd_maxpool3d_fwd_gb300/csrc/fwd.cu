@@ -5,6 +5,7 @@
 // window box of that output; no padding. The index written is the in-plane
 // flat offset d*H*W + h*W + w of the first element (in d, h, w row-major
 // order) that attains the maximum; a NaN beats every number.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
@@ -537,6 +538,16 @@ constexpr uint32_t kLanes = 0x00010001u;   // a constant in both 16-bit lanes
 // mp3d_device_error_flags().
 __device__ unsigned int g_mp3d_device_error = 0;
 
+// Polls the main pipeline waits make before giving up (host side; lowered
+// only by tests of the give-up path).
+static std::atomic<int> g_wait_limit{kWaitLimit};
+
+int pipeline_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+
+int set_pipeline_wait_limit(int polls) {
+    return g_wait_limit.exchange(polls < 0 ? kWaitLimit : polls, std::memory_order_relaxed);
+}
+
 // One CTA = (plane p, output-depth group, band of G oh-tiles of TOH rows).
 // Threads = nc chunks x G tiles. Each depth slice's band of input rows is
 // one contiguous span of memory; thread 0 streams slice after slice into a
@@ -547,7 +558,7 @@ __device__ unsigned int g_mp3d_device_error = 0;
 template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS>
 __global__ void __launch_bounds__(256)
 k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
-         int nq, int G, int nbands, int nc) {
+         int nq, int G, int nbands, int nc, int wait_limit) {
     static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
     extern __shared__ __align__(128) unsigned char smem[];
     const int band = (int)(blockIdx.x % nbands);
@@ -598,7 +609,10 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
     }
 
     uint32_t poison = 0;
+    // A wait that gives up fails the whole CTA: the threads agree on it at
+    // the block barrier after the slice (fail_at = that slice, -1: none).
     bool failed = false;
+    int fail_at = -1;
     uint32_t cv[TOH][2], cc[TOH][2], pv[TOH][2], pc[TOH][2];
 #pragma unroll
     for (int j = 0; j < TOH; ++j)
@@ -659,10 +673,7 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
             if (!role_cur && !role_prev) continue;
             const int stage = sl % NS;
             const uint32_t parity = (uint32_t)((sl / NS) & 1);
-            if (!failed && !mbar_wait(smem_addr(&bars[stage]), parity, kWaitLimit)) {
-                failed = true;
-                atomicOr(&g_mp3d_device_error, kErrPipelineTimeout);
-            }
+            if (!failed && !mbar_wait(smem_addr(&bars[stage]), parity, wait_limit)) failed = true;
             const unsigned char* buf = stages + stage * stage_stride;
             uint32_t hv[TOH][2], hc[TOH][2];
 #pragma unroll
@@ -709,8 +720,13 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                     }
                 }
             }
-            // Every thread is done reading this stage: refill it.
-            __syncthreads();
+            // Every thread is done reading this stage: refill it, unless a
+            // wait of any thread gave up.
+            if (__syncthreads_or(failed) && fail_at < 0) {
+                fail_at = sl;
+                if (tid == 0) atomicOr(&g_mp3d_device_error, kErrPipelineTimeout);
+            }
+            failed = fail_at >= 0;
             if (tid == 0 && sl + NS < nslices && !failed) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 const uint32_t bar = smem_addr(&bars[stage]);
@@ -751,9 +767,12 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                 pc[j][k] = cc[j][k];
             }
     }
-    // After a timeout, let copies still in flight land before the CTA exits.
-    if (failed && tid == 0) {
-        for (int k = (sl > NS ? sl - NS : 0); k < sl && k < nslices; ++k)
+    // After a timeout, let copies still in flight land before the CTA exits:
+    // nothing was issued after slice fail_at's barrier, and every slice before
+    // it was waited for, so they are among slices [fail_at, fail_at + NS).
+    // These waits keep the normal bound.
+    if (fail_at >= 0 && tid == 0) {
+        for (int k = fail_at; k < fail_at + NS && k < nslices; ++k)
             mbar_wait(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1), kWaitLimit);
     }
 }
@@ -899,7 +918,8 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long blocks = g.P * nq * nbands;
-    kern<<<(unsigned)blocks, nc * G, smem, s>>>((const T*)x, (T*)y, idx, g, odg, nq, G, nbands, nc);
+    kern<<<(unsigned)blocks, nc * G, smem, s>>>((const T*)x, (T*)y, idx, g, odg, nq, G, nbands, nc,
+                                                 pipeline_wait_limit());
     return cudaGetLastError();
 }
 

@@ -10,6 +10,15 @@
 
 namespace mp3d {
 
+// Argument checks of a backward call (api.cu), before any CUDA call:
+// sizes, window, dtype and algorithm into *g; then the buffers (NULL,
+// alignment, overlap, and the workspace when algo needs one).
+int bwd_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+            int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype, int algo);
+int check_bwd_buffers(const void* grad_out, const int64_t* idx, const void* grad_in,
+                      const void* workspace, size_t workspace_bytes, const Geo& g, int dtype,
+                      int algo);
+
 // Forward paths (fwd.cu).
 cudaError_t launch_fwd_generic(const void* x, void* y, int64_t* idx, const Geo& g,
                                int dtype, int sms, cudaStream_t s);
@@ -39,6 +48,12 @@ cudaError_t launch_fwd_ndhwc(const void* x, void* y, int64_t* idx, const Geo& g,
                              int sms, cudaStream_t s);
 cudaError_t launch_bwd_ndhwc(const void* go, const int64_t* idx, void* gi, const Geo& g, int C,
                              int dtype, int sms, cudaStream_t s);
+
+// Polls the main pipeline waits of the forward kernels make before giving
+// up (fwd.cu; kWaitLimit unless a test set another value), and its setter
+// (a negative value restores kWaitLimit; returns the previous value).
+int pipeline_wait_limit();
+int set_pipeline_wait_limit(int polls);
 
 // Error flags set by kernels whose bounded waits gave up (fwd.cu, with the
 // flag of fwd_roll.cu folded in).

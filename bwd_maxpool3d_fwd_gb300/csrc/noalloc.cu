@@ -23,7 +23,10 @@ std::mutex g_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up on
-// the first call per device (with that device current) and cached.
+// the first call per device (with that device current) and cached for the
+// life of the process. The cache is keyed by device ordinal: after
+// cudaDeviceReset, or under a context other than the device's primary one,
+// the cached address no longer names the array (documented in mp3d.h).
 int scratch_on_current_device(float** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MP3D_ERR_CUDA;
@@ -38,49 +41,34 @@ int scratch_on_current_device(float** out) {
     return MP3D_OK;
 }
 
-bool ranges_overlap(const void* a, long long na, const void* b, long long nb) {
-    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
-    return na > 0 && nb > 0 && pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
-}
-
 }  // namespace
 
 extern "C" int maxpool3d_bwd_noalloc(const void* grad_out, const int64_t* idx, void* grad_in,
                                      int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                                      int od, int oh, int ow, int kd, int kh, int kw, int sd,
                                      int sh, int sw, int dtype, cudaStream_t stream) {
-    // Shapes, window, dtype: checked exactly as maxpool3d_bwd checks them.
-    int path = MP3D_PATH_NOOP;
-    int st = maxpool3d_bwd_plan(N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype,
-                                MP3D_BWD_ATOMIC, &path);
+    // Sizes, window, dtype and buffers: maxpool3d_bwd's own checks, made
+    // before any CUDA call (the workspace is checked below, once its
+    // address is known).
+    mp3d::Geo g;
+    int st = mp3d::bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype,
+                           MP3D_BWD_ATOMIC);
+    if (st == MP3D_OK)
+        st = mp3d::check_bwd_buffers(grad_out, idx, grad_in, nullptr, 0, g, dtype, MP3D_BWD_AUTO);
     if (st != MP3D_OK) return st;
-    if (path == MP3D_PATH_NOOP) return MP3D_OK;
-
-    const int es = (dtype == MP3D_F32) ? 4 : 2;
-    const long long P = N * C, vol = D * H * W, ovol = (long long)od * oh * ow;
-    if (!grad_out || !idx || !grad_in) return MP3D_ERR_NULLPTR;
-    if ((uintptr_t)grad_out % es || (uintptr_t)idx % 8 || (uintptr_t)grad_in % es)
-        return MP3D_ERR_ALIGN;
-    if (ranges_overlap(grad_in, P * vol * es, grad_out, P * ovol * es) ||
-        ranges_overlap(grad_in, P * vol * es, idx, P * ovol * 8))
-        return MP3D_ERR_ALIAS;
+    if (g.P == 0) return MP3D_OK;
 
     float* scratch = nullptr;
     if (dtype != MP3D_F32) {
-        if (P * vol > kNoallocScratchFloats) return MP3D_ERR_SCRATCH;
+        if (g.P * (long long)g.vol > kNoallocScratchFloats) return MP3D_ERR_SCRATCH;
         st = scratch_on_current_device(&scratch);
         if (st != MP3D_OK) return st;
+        // the array as the atomic form's workspace: size, alignment, overlap
+        st = mp3d::check_bwd_buffers(grad_out, idx, grad_in, scratch,
+                                     (size_t)kNoallocScratchFloats * sizeof(float), g, dtype,
+                                     MP3D_BWD_ATOMIC);
+        if (st != MP3D_OK) return st;
     }
-
-    mp3d::Geo g{};
-    g.P = P;
-    g.D = (int)D; g.H = (int)H; g.W = (int)W;
-    g.OD = od; g.OH = oh; g.OW = ow;
-    g.kd = kd; g.kh = kh; g.kw = kw;
-    g.sd = sd; g.sh = sh; g.sw = sw;
-    g.adaptive = (kd == 0) ? 1 : 0;
-    g.vol = (int)vol;
-    g.ovol = (int)ovol;
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -298,8 +298,11 @@ int maxpool3d_bwd_ex_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
  *    return MP3D_ERR_SCRATCH before any launch. f32 accumulates in grad_in
  *    directly, uses no scratch and has no such limit.
  *  - The first call on each device looks up the array's device address
- *    (with that device current) and caches it; make that first call before
- *    any stream capture.
+ *    (with that device current) and caches it for the life of the
+ *    process; make that first call before any stream capture. The cached
+ *    address belongs to the device's primary context as it was at that
+ *    first call: do not use this entry point after cudaDeviceReset on that
+ *    device, or from a context created with the driver API.
  *  - Every call on a device shares the one array. Each call clears the part
  *    it uses before accumulating, so calls in sequence are independent, but
  *    calls that can overlap on the GPU (different streams without ordering,
@@ -321,6 +324,16 @@ int maxpool3d_bwd_noalloc(const void* grad_out, const int64_t* idx, void* grad_i
  * No counterpart on the pages: it exists because the library's kernels
  * never trap or spin without limit. */
 int mp3d_device_error_flags(unsigned int* flags, int clear);
+
+/* Sets how many times the forward kernels' copy pipelines poll a pending
+ * copy before their wait gives up (bit 0 of mp3d_device_error_flags), for
+ * launches made after the call, process-wide; returns the previous value.
+ * A negative value restores the default (2^22 polls). Only for tests of the
+ * give-up path: with 0 every pipeline wait gives up at once, the kernels
+ * still let their copies in flight land before they exit (those waits keep
+ * the default bound), and their outputs are incomplete. No counterpart on
+ * the pages. */
+int mp3d_set_pipeline_wait_limit(int polls);
 
 /* Static description of a status code (never NULL). */
 const char* mp3d_status_string(int status);

@@ -377,3 +377,23 @@ def test_depth_walk_plans(L):
     assert mp.adaptive_maxpool3d_fwd_plan((1, 2, 9, 40, 40), (4, 20, 20), f16) == "fwd_roll"
     # more than 65536 elements per slice: not the walk
     assert mp.adaptive_maxpool3d_fwd_plan((1, 1, 4, 300, 300), (2, 10, 10), f16) != "fwd_roll"
+
+
+def test_wait_limit_setter_restores_the_default(L):
+    f = L.mp3d_set_pipeline_wait_limit
+    f.argtypes = [ctypes.c_int]
+    f.restype = ctypes.c_int
+    prev = f(5)
+    try:
+        assert f(-1) == 5
+        assert f(-1) == 1 << 22
+    finally:
+        f(prev)
+
+
+def test_no_undefined_symbols_of_the_library():
+    # every function of the library's own namespace is defined in it
+    import subprocess
+    out = subprocess.run(["nm", "-DC", "--undefined-only", mp.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    assert "mp3d" not in out, out
