@@ -677,7 +677,7 @@ def our_arm(args):
                 "bwd": {"path": pb, "us": round(bwd_ms * 1e3, 2), "bytes": bb,
                         "gbs": round(bb / (bwd_ms * 1e-3) / 1e9, 1),
                         "frac": round(bb / (bwd_ms * 1e-3) / 1e9 / peak, 4)}}
-    e2e_res = e2e(r, x_cpu, g_cpu)
+    e2e_res = None if args.no_e2e else e2e(r, x_cpu, g_cpu)
     del r
     torch.cuda.empty_cache()
     cfg = per_config(dev, peak) if (rank == 0 and not args.no_per_config) else None
@@ -709,6 +709,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=HEADLINE)
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (its second set of device buffers); for profiling")
     ap.add_argument("--planes", type=int, default=0,
                     help="run only the first N planes of the workload (same per-plane shape; "
                          "for profiling small cases; whole samples with --layout ndhwc)")

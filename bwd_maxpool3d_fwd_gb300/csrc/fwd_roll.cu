@@ -360,18 +360,23 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
     uint32_t av0 = 0u, av1 = 0u;
     int ao0[2] = {0, 0}, ao1[2] = {0, 0};
     bool fresh0 = true, fresh1 = true, bad0 = false, bad1 = false;
-    // a wait that gives up fails the whole CTA: the threads agree on it at
-    // the block barrier after the slice (fail_at = that slice, -1: none)
+    // bounded waits: a thread whose wait gives up stops waiting (its outputs
+    // are then incomplete; the error flag says so); thread 0 alone issues
+    // copies, waits for every slice it issued until its own wait gives up
+    // (at fail_at) and refills nothing after that
     bool failed = false;
-    int fail_at = -1;
+    __shared__ int fail_at;                    // (thread 0) the slice whose wait gave up
     unsigned redo = 0u;                        // depth windows (bit a - od0) seen with NaN or inf
     int a = od0;
     int a_start = d_first;
     int a_end = cw_end<AD>(a, g.D, g.OD, g.kd, g.sd, g.pd);
     int b_start = a + 1 < od1 ? cw_start<AD>(a + 1, g.D, g.OD, g.kd, g.sd, g.pd) : INT_MAX;
     for (int i = 0; i < ns; ++i) {
-        if (!failed && !mbar_wait(smem_addr(&bars[i % PF_NS]), (uint32_t)((i / PF_NS) & 1), rg.wait_limit))
+        if (!failed && !mbar_wait(smem_addr(&bars[i % PF_NS]), (uint32_t)((i / PF_NS) & 1), rg.wait_limit)) {
             failed = true;
+            if (tid == 0) fail_at = i;
+            atomicOr(&g_mp3d_roll_error, kErrPipelineTimeout);
+        }
         const unsigned char* sa = xb0 + (size_t)(d_first + i) * HW * sizeof(T);
         const int mis = (int)(((uintptr_t)sa & 15) / sizeof(T));
         const int nvec = (int)((mis * sizeof(T) + span * sizeof(T) + 15) / 16);
@@ -389,14 +394,9 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             dst[0] = lo;
             dst[1] = hi;
         }
-        // every thread is done with stage i % NS (refilled below unless a
-        // wait gave up) and with the words of slice i - 1 (overwritten next
-        // iteration)
-        if (__syncthreads_or(failed) && fail_at < 0) {
-            fail_at = i;
-            if (tid == 0) atomicOr(&g_mp3d_roll_error, kErrPipelineTimeout);
-        }
-        failed = fail_at >= 0;
+        // every thread is done with stage i % NS (refilled below) and with
+        // the words of slice i - 1 (overwritten next iteration)
+        __syncthreads();
         if (tid == 0 && i + PF_NS < ns && !failed) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(i + PF_NS);
@@ -498,11 +498,10 @@ k_fwd_pair(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
             }
         }
     }
-    // after the CTA's waits gave up at slice fail_at, let the copies still in
-    // flight land before the CTA exits (with the normal bound): nothing was
-    // issued after that slice's barrier and every earlier slice was waited
-    // for, so they are among slices [fail_at, fail_at + NS)
-    if (fail_at >= 0 && tid == 0)
+    // after thread 0's wait gave up at slice f, let the copies still in
+    // flight land before the CTA exits: thread 0 issued nothing after that
+    // wait, so they are among slices [f, f + NS)
+    if (failed && tid == 0)
         for (int k = fail_at; k < fail_at + PF_NS && k < ns; ++k)
             mbar_wait(smem_addr(&bars[k % PF_NS]), (uint32_t)((k / PF_NS) & 1), kWaitLimit);
     // outputs whose windows held a NaN or an infinity: the exact scalar scan
