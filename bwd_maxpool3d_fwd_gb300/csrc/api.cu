@@ -308,6 +308,7 @@ int run_bwd(const void* grad_out, const int64_t* idx, void* grad_in, void* works
 // (dilation 1), else the thread-per-output kernel.
 int ex_fwd_path(const Geo& g, int dtype, bool aligned16 = true) {
     if (g.P == 0) return MP3D_PATH_NOOP;
+    if (fwd_s2_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_S2;
     if (fwd_roll_supported(g, dtype, aligned16)) return MP3D_PATH_FWD_ROLL;
     return MP3D_PATH_FWD_PADDED;
 }
@@ -494,8 +495,9 @@ int maxpool3d_fwd_ex(const void* x, void* y, int64_t* idx, int64_t N, int64_t C,
     if (path == MP3D_PATH_NOOP) return MP3D_OK;
     int sms = 0;
     if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
-    const cudaError_t e = path == MP3D_PATH_FWD_ROLL ? launch_fwd_roll(x, y, idx, g, dtype, sms, stream)
-                                                     : launch_fwd_ex(x, y, idx, g, dtype, sms, stream);
+    const cudaError_t e = path == MP3D_PATH_FWD_S2     ? launch_fwd_s2(x, y, idx, g, dtype, sms, stream)
+                          : path == MP3D_PATH_FWD_ROLL ? launch_fwd_roll(x, y, idx, g, dtype, sms, stream)
+                                                       : launch_fwd_ex(x, y, idx, g, dtype, sms, stream);
     return e == cudaSuccess ? MP3D_OK : MP3D_ERR_CUDA;
 }
 

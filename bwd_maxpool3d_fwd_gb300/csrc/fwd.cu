@@ -558,11 +558,21 @@ int set_pipeline_wait_limit(int polls) {
 // threads at five CTAs per SM: with the outputs no longer staged in shared
 // memory (and no barriers around their flush), 466 -> 412 us on the
 // 32x128x16x112x112 fp16 forward.
-template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS>
+//
+// PAD: windows padded by g.pd, g.ph, g.pw in {0, 1} (3x3x3 windows, stride
+// 2, floor output sizes): window o starts at 2o - p. A position outside the
+// input is read as its nearest position inside (the clamped slice, row or
+// column) carrying that position's own offset in the window as its code:
+// such a duplicate is either the same element as a candidate met earlier,
+// or comes first and bears the code of the real element that follows it,
+// so ties still go to the first real occurrence and padding is never chosen.
+template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS, bool PAD = false>
 __global__ void __launch_bounds__(128, 5)
 k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
          int nq, int G, int nbands, int nc, int wait_limit) {
     static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
+    static_assert(!PAD || (KD == 3 && SD == 2 && KH == 3 && SH == 2 && KW == 3), "padded shape");
+    const int pd = PAD ? g.pd : 0, ph = PAD ? g.ph : 0, pw = PAD ? g.pw : 0;
     extern __shared__ __align__(128) unsigned char smem[];
     const int band = (int)(blockIdx.x % nbands);
     long long rest = blockIdx.x / nbands;
@@ -581,7 +591,10 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
     const int nd = min(odg, g.OD - od0);
     const int HW = g.H * g.W;
     const bool has_extra = (KW > 2) && (w0 + 8 < g.W);
-    const int band_rows = (oh_band_end - oh_band - 1) * SH + KH;
+    // input rows of the band that exist: [r0, r1)
+    const int r0 = max(oh_band * SH - ph, 0);
+    const int r1 = min((oh_band_end - 1) * SH - ph + KH, g.H);
+    const int band_rows = r1 - r0;
     const uint32_t span_bytes = (uint32_t)band_rows * g.W * sizeof(T);
     const uint32_t stage_stride = (span_bytes + 127) / 128 * 128;
     // shared layout: [NS stages][NS mbarriers]
@@ -589,9 +602,12 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * stage_stride);
 
     const T* xp = x + p * g.vol;
-    const T* band_src = xp + (long long)oh_band * SH * g.W;
+    const T* band_src = xp + (long long)r0 * g.W;
     const int nslices = (KD >= SD) ? nd * SD + KD - SD : nd * KD;
-    auto slice_d = [&](int k) { return (KD >= SD) ? od0 * SD + k : (od0 + k / KD) * SD + k % KD; };
+    // nominal slice of step k (before the first or past the last slice when
+    // padded) and the slice it is read from
+    auto slice_nom = [&](int k) { return (KD >= SD) ? od0 * SD - pd + k : (od0 + k / KD) * SD + k % KD; };
+    auto slice_d = [&](int k) { return PAD ? min(max(slice_nom(k), 0), g.D - 1) : slice_nom(k); };
 
     // Bounded waits. Each thread waits for a slice itself and, once a wait
     // gives up, stops waiting (its outputs are then incomplete; the error
@@ -641,7 +657,7 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
             // in-plane offsets (below 2^31) of the four winners
             int off[4];
             uint32_t yw[2] = {v[j][0], v[j][1]};
-            const int base = od * SD * HW + oh * SH * g.W + ow0 * 2;
+            const int base = (od * SD - pd) * HW + (oh * SH - ph) * g.W + ow0 * 2 - pw;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint32_t code = (cd[j][e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
@@ -654,8 +670,13 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                     T yv;
                     int64_t iv;
                     const int ow = ow0 + e;
-                    exact_window<T>(xp, od * SD, od * SD + KD, oh * SH, oh * SH + KH, ow * 2,
-                                    ow * 2 + KW, g.W, HW, &yv, &iv);
+                    if constexpr (PAD)
+                        exact_window<T>(xp, max(od * SD - pd, 0), min(od * SD - pd + KD, g.D),
+                                        max(oh * SH - ph, 0), min(oh * SH - ph + KH, g.H),
+                                        max(ow * 2 - pw, 0), min(ow * 2 - pw + KW, g.W), g.W, HW, &yv, &iv);
+                    else
+                        exact_window<T>(xp, od * SD, od * SD + KD, oh * SH, oh * SH + KH, ow * 2,
+                                        ow * 2 + KW, g.W, HW, &yv, &iv);
                     yo[e] = *reinterpret_cast<uint16_t*>(&yv);
                     if (io) io[e] = iv;
                 }
@@ -709,6 +730,8 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                 atomicOr(&g_mp3d_device_error, kErrPipelineTimeout);
             }
             const unsigned char* buf = stages + stage * stage_stride;
+            // a clamped slice: its code offset from the nominal one
+            const int ddelta = PAD ? slice_d(sl) - slice_nom(sl) : 0;
             uint32_t hv[TOH][2], hc[TOH][2];
 #pragma unroll
             for (int j = 0; j < TOH; ++j) hv[j][0] = hv[j][1] = hc[j][0] = hc[j][1] = 0;
@@ -718,25 +741,55 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
 #pragma unroll
                 for (int r = 0; r < (TOH - 1) * SH + KH; ++r) {
                     if (r >= nrows) break;
-                    const unsigned char* row = buf + ((rbase + r) * g.W + w0) * sizeof(T);
+                    // nominal input row oh0*SH - ph + r, read from the nearest row that exists
+                    int srow = rbase + r, hdelta = 0;
+                    if constexpr (PAD) {
+                        const int hn = oh0 * SH - ph + r;
+                        const int hs = min(max(hn, 0), g.H - 1);
+                        hdelta = hs - hn;
+                        srow = hs - r0;
+                    }
+                    const unsigned char* row = buf + (srow * g.W + w0) * sizeof(T);
                     const uint4 raw = *reinterpret_cast<const uint4*>(row);
                     uint32_t e8 = 0;
-                    if (KW > 2 && has_extra) e8 = *reinterpret_cast<const unsigned short*>(row + 16);
+                    if (PAD && pw) {
+                        // the element before the chunk (window 4c starts at 8c - 1);
+                        // at the left edge, element 8c itself
+                        e8 = c > 0 ? *reinterpret_cast<const unsigned short*>(row - 2) : raw.x;
+                    } else if (KW > 2 && has_extra) {
+                        // the element after the chunk (with floor output sizes the
+                        // window that needs it past the last column is never written)
+                        e8 = *reinterpret_cast<const unsigned short*>(row + 16);
+                    }
                     poison = Pair<T>::poison(poison, raw.x);
                     poison = Pair<T>::poison(poison, raw.y);
                     poison = Pair<T>::poison(poison, raw.z);
                     poison = Pair<T>::poison(poison, raw.w);
                     if (KW > 2) poison = Pair<T>::poison(poison, e8);
                     uint32_t wv[2], wc[2];
-                    wv[0] = __byte_perm(raw.x, raw.y, 0x5410);
-                    wc[0] = 0;
-                    merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 1u * kLanes);
-                    wv[1] = __byte_perm(raw.z, raw.w, 0x5410);
-                    wc[1] = 0;
-                    merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 1u * kLanes);
-                    if (KW > 2) {
-                        merge2<T>(wv[0], wc[0], __byte_perm(raw.y, raw.z, 0x5410), 2u * kLanes);
-                        merge2<T>(wv[1], wc[1], __byte_perm(raw.w, e8, 0x5410), 2u * kLanes);
+                    if (PAD && pw) {
+                        // windows 4c..4c+3 over elements 8c-1..8c+7: lanes
+                        // (e-1, e1), (e0, e2), (e1, e3) and (e3, e5), (e4, e6), (e5, e7);
+                        // at the left edge e-1 is e0 with e0's code
+                        wv[0] = __byte_perm(e8, raw.x, 0x7610);
+                        wc[0] = c > 0 ? 0u : 1u;
+                        merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x5410), 1u * kLanes);
+                        merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 2u * kLanes);
+                        wv[1] = __byte_perm(raw.y, raw.z, 0x7632);
+                        wc[1] = 0;
+                        merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x5410), 1u * kLanes);
+                        merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 2u * kLanes);
+                    } else {
+                        wv[0] = __byte_perm(raw.x, raw.y, 0x5410);
+                        wc[0] = 0;
+                        merge2<T>(wv[0], wc[0], __byte_perm(raw.x, raw.y, 0x7632), 1u * kLanes);
+                        wv[1] = __byte_perm(raw.z, raw.w, 0x5410);
+                        wc[1] = 0;
+                        merge2<T>(wv[1], wc[1], __byte_perm(raw.z, raw.w, 0x7632), 1u * kLanes);
+                        if (KW > 2) {
+                            merge2<T>(wv[0], wc[0], __byte_perm(raw.y, raw.z, 0x5410), 2u * kLanes);
+                            merge2<T>(wv[1], wc[1], __byte_perm(raw.w, e8, 0x5410), 2u * kLanes);
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < TOH; ++j) {
@@ -746,9 +799,9 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
                         for (int k = 0; k < 2; ++k) {
                             if (hl == 0) {
                                 hv[j][k] = wv[k];
-                                hc[j][k] = wc[k];
+                                hc[j][k] = wc[k] | ((uint32_t)hdelta << 2) * kLanes;
                             } else {
-                                merge2<T>(hv[j][k], hc[j][k], wv[k], wc[k] | ((uint32_t)hl << 2) * kLanes);
+                                merge2<T>(hv[j][k], hc[j][k], wv[k], wc[k] | ((uint32_t)(hl + hdelta) << 2) * kLanes);
                             }
                         }
                     }
@@ -769,13 +822,13 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     if (role_prev)
-                        merge2<T>(pv[j][k], pc[j][k], hv[j][k], hc[j][k] | ((uint32_t)(SD + i) << 4) * kLanes);
+                        merge2<T>(pv[j][k], pc[j][k], hv[j][k], hc[j][k] | ((uint32_t)(SD + i + ddelta) << 4) * kLanes);
                     if (role_cur) {
                         if (i == 0) {
                             cv[j][k] = hv[j][k];
-                            cc[j][k] = hc[j][k];
+                            cc[j][k] = hc[j][k] | ((uint32_t)ddelta << 4) * kLanes;
                         } else {
-                            merge2<T>(cv[j][k], cc[j][k], hv[j][k], hc[j][k] | ((uint32_t)i << 4) * kLanes);
+                            merge2<T>(cv[j][k], cc[j][k], hv[j][k], hc[j][k] | ((uint32_t)(i + ddelta) << 4) * kLanes);
                         }
                     }
                 }
@@ -909,10 +962,19 @@ static int s2_variant(const Geo& g) {
 }
 
 bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
-    return (dtype == F16 || dtype == BF16) && s2_variant(g) >= 0 && g.W % 8 == 0 && g.W <= 1024 && aligned16;
+    if (!((dtype == F16 || dtype == BF16) && s2_variant(g) >= 0 && g.W % 8 == 0 && g.W <= 1024 && aligned16))
+        return false;
+    if (g.dd != 1 || g.dh != 1 || g.dw != 1) return false;
+    // floor output sizes (no ceil-mode window past the input)
+    if (g.OD != (g.D + 2 * g.pd - g.kd) / g.sd + 1 || g.OH != (g.H + 2 * g.ph - g.kh) / g.sh + 1 ||
+        g.OW != (g.W + 2 * g.pw - g.kw) / g.sw + 1)
+        return false;
+    // padding: 3x3x3 windows with stride 2, at most one position per side
+    if (g.pd || g.ph || g.pw) return s2_variant(g) == 1 && g.pd <= 1 && g.ph <= 1 && g.pw <= 1;
+    return true;
 }
 
-template <typename T, int KD, int SD, int KH, int SH, int KW>
+template <typename T, int KD, int SD, int KH, int SH, int KW, bool PAD = false>
 static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                             cudaStream_t s) {
     constexpr int TOH = 4, NS = 2;
@@ -934,7 +996,7 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
     const int band_rows = (G * TOH - 1) * SH + KH;
     const size_t stage = ((size_t)band_rows * g.W * sizeof(T) + 127) / 128 * 128;
     const size_t smem = NS * stage + NS * 8;
-    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS>;
+    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS, PAD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long blocks = g.P * nq * nbands;
@@ -946,6 +1008,7 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
 template <typename T>
 static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                                    cudaStream_t s) {
+    if (g.pd || g.ph || g.pw) return fwd_s2_t<T, 3, 2, 3, 2, 3, true>(x, y, idx, g, sms, s);
     // 2x2x2 windows tiling the input: direct loads, one thread per four windows
     if (s2_variant(g) == 0 && g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW &&
         g.OW % 4 == 0 && (uintptr_t)y % 8 == 0 && (uintptr_t)idx % 16 == 0) {

@@ -498,6 +498,23 @@ PADDED_CASES = [
 ]
 
 
+def _padded_fwd_path(shape, k, s, p, dl, cm, dtype):
+    """The forward path the library takes for a padded geometry: the stride-2
+    kernel for 16-bit 3x3x3 stride-2 windows with padding <= 1, rows a
+    multiple of 8 elements and floor sizes; else, for 16-bit types with
+    dilation 1 and plane volumes a multiple of 8, the depth walk (clipped
+    windows); else the thread-per-output kernel."""
+    floor = all(o == (i + 2 * pp - kk) // ss + 1 for o, i, kk, ss, pp in
+                zip(mp.pool_out_size_ex(shape[2:], k, s, p, dl, cm), shape[2:], k, s, p))
+    if (dtype != torch.float32 and tuple(k) == (3, 3, 3) and tuple(s) == (2, 2, 2) and
+            tuple(dl) == (1, 1, 1) and max(p) <= 1 and shape[4] % 8 == 0 and shape[4] <= 1024 and floor):
+        return "fwd_s2"
+    if (dtype != torch.float32 and tuple(dl) == (1, 1, 1) and k[0] <= 2 * s[0] and
+            (shape[2] * shape[3] * shape[4]) % 8 == 0):
+        return "fwd_roll"
+    return "fwd_padded"
+
+
 def _gpu_fwd_ex(x_cpu, k, s, p, dl, cm):
     x = x_cpu.to(DEV)
     out = mp.pool_out_size_ex(x.shape[2:], k, s, p, dl, cm)
@@ -524,9 +541,8 @@ def test_padded_fwd_bwd(case, dtype):
     k, s, p, dl, cm, shape = PADDED_CASES[case]
     # 16-bit types with dilation 1 and plane volumes a multiple of 8 take the
     # depth walk (clipped windows); the rest the thread-per-output kernel
-    walk = (dtype != torch.float32 and dl == (1, 1, 1) and k[0] <= 2 * s[0] and
-            (shape[2] * shape[3] * shape[4]) % 8 == 0)
-    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, dl, cm, dtype) == ("fwd_roll" if walk else "fwd_padded")
+    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, dl, cm, dtype) == _padded_fwd_path(shape, k, s, p, dl, cm,
+                                                                                     dtype)
     gen = torch.Generator().manual_seed(9500 + case)
     x = random_input(gen, shape, dtype, KINDS[case % 3])
     y_ref, i_ref = oracle.maxpool3d_fwd_ex(x, k, s, p, dl, cm)
@@ -543,6 +559,47 @@ def test_padded_fwd_bwd(case, dtype):
     assert_bits_equal(_gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm), gin_ref, "grad_in (padded)")
     gin_a = _gpu_bwd_ex(g, i_ref, shape, k, s, p, dl, cm, algo=mp.BWD_ATOMIC)
     assert _atomic_tolerance_ok(gin_a, gin_ref, g, i_ref, dtype)
+
+
+PADDED_S2_CASES = [
+    ((1, 1, 1), (2, 3, 16, 56, 56)),      # even sizes, the bench's padded geometry
+    ((1, 1, 1), (1, 2, 9, 23, 64)),       # odd D and H: the last windows clipped below
+    ((0, 1, 1), (1, 3, 8, 30, 16)),
+    ((1, 0, 1), (1, 2, 7, 17, 24)),
+    ((1, 1, 0), (2, 1, 10, 15, 40)),
+    ((0, 0, 1), (1, 2, 5, 9, 8)),         # one chunk per row: the left edge everywhere
+    ((1, 0, 0), (1, 2, 6, 11, 32)),
+    ((1, 1, 1), (1, 2, 5, 112, 112)),     # several bands of output rows
+]
+
+
+@pytest.mark.parametrize("dtype", (torch.float16, torch.bfloat16), ids=str)
+@pytest.mark.parametrize("case", range(len(PADDED_S2_CASES)))
+def test_padded_stride2_forward(case, dtype):
+    # 3x3x3 windows, stride 2, padding <= 1: the stride-2 kernel with clamped
+    # slices, rows and columns; ties, signed zeros, infinities and NaNs
+    p, shape = PADDED_S2_CASES[case]
+    k, s = (3, 3, 3), (2, 2, 2)
+    assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, (1, 1, 1), False, dtype) == "fwd_s2"
+    gen = torch.Generator().manual_seed(9700 + case)
+    for kind in ("ties", "special", "normal"):
+        x = random_input(gen, shape, dtype, kind)
+        y_ref, i_ref = oracle.maxpool3d_fwd_ex(x, k, s, p, (1, 1, 1), False)
+        y, idx = _gpu_fwd_ex(x, k, s, p, (1, 1, 1), False)
+        assert torch.equal(idx, i_ref), kind
+        assert_bits_equal(y, y_ref, f"y (padded stride 2, {kind})")
+    # values only, and outputs one element past a 16-byte boundary
+    xd = x.to(DEV)
+    yv = torch.empty(y_ref.shape, dtype=dtype, device=DEV)
+    mp.maxpool3d_fwd_ex(xd, yv, None, k, s, p)
+    yb = torch.empty(y_ref.numel() + 1, dtype=dtype, device=DEV)
+    ib = torch.empty(y_ref.numel() + 1, dtype=torch.int64, device=DEV)
+    yu, iu = yb[1:].view(y_ref.shape), ib[1:].view(y_ref.shape)
+    mp.maxpool3d_fwd_ex(xd, yu, iu, k, s, p)
+    torch.cuda.synchronize()
+    assert_bits_equal(yv.cpu(), y_ref, "y (padded stride 2, values only)")
+    assert_bits_equal(yu.cpu(), y_ref, "y (padded stride 2, unaligned)")
+    assert torch.equal(iu.cpu(), i_ref)
 
 
 def test_padded_plain_geometry_matches_plain_entry_points():

@@ -26,7 +26,8 @@ CASES = [
     # (name, input shape, forward kind, window args, expected path)
     ("stride2_k3s2", (2, 3, 9, 30, 64), "fixed", ((3, 3, 3), (2, 2, 2)), "fwd_s2"),
     ("pair_adaptive", (2, 4, 30, 50, 50), "adaptive", (8, 12, 12), "fwd_roll"),
-    ("pair_padded", (2, 4, 16, 56, 56), "padded", ((3, 3, 3), (2, 2, 2), (1, 1, 1)), "fwd_roll"),
+    ("pair_padded", (2, 4, 16, 50, 50), "padded", ((3, 3, 3), (2, 2, 2), (1, 1, 1)), "fwd_roll"),
+    ("stride2_padded", (2, 4, 16, 56, 56), "padded", ((3, 3, 3), (2, 2, 2), (1, 1, 1)), "fwd_s2"),
 ]
 
 
