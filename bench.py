@@ -553,18 +553,20 @@ def per_config(dev, peak):
 # inputs: x ~ N(0,1) and grad_out ~ N(0,1), drawn in binary32 then rounded.
 PADDED = {"name": "padded_k3s2p1_f16_8x64x16x56x56", "shape": (8, 64, 16, 56, 56),
           "k": (3, 3, 3), "s": (2, 2, 2), "p": (1, 1, 1), "dl": (1, 1, 1), "seed": 20261302}
+# the same padded window at the size of the k3s2 workload
+PADDED_LARGE = {"name": "padded_k3s2p1_f16_32x128x16x112x112", "shape": (32, 128, 16, 112, 112),
+                "k": (3, 3, 3), "s": (2, 2, 2), "p": (1, 1, 1), "dl": (1, 1, 1), "seed": 20261303}
 
 
-def padded_config(dev, peak):
-    """The padded workload's forward and backward timed alone (median of 20,
-    L2 flushed before every launch)."""
+def padded_config(dev, peak, c=PADDED):
+    """A padded workload's forward and backward timed alone (median of 20,
+    L2 flushed before every launch). Inputs are drawn on the device (seeded)."""
     import bwd_maxpool3d_fwd_gb300 as mp
-    c = PADDED
-    gen = torch.Generator().manual_seed(c["seed"])
-    x = torch.randn(c["shape"], generator=gen).half().to(dev)
+    gen = torch.Generator(device=dev).manual_seed(c["seed"])
+    x = torch.randn(c["shape"], generator=gen, device=dev).half()
     out = mp.pool_out_size_ex(c["shape"][2:], c["k"], c["s"], c["p"], c["dl"])
     oshape = c["shape"][:2] + out
-    g = torch.randn(oshape, generator=gen).half().to(dev)
+    g = torch.randn(oshape, generator=gen, device=dev).half()
     y = torch.empty(oshape, dtype=torch.float16, device=dev)
     idx = torch.empty(oshape, dtype=torch.int64, device=dev)
     gin = torch.empty(c["shape"], dtype=torch.float16, device=dev)
@@ -689,6 +691,8 @@ def our_arm(args):
     cfg = per_config(dev, peak) if (rank == 0 and not args.no_per_config) else None
     if cfg is not None:
         cfg[PADDED["name"]] = padded_config(dev, peak)
+        cfg[PADDED_LARGE["name"]] = padded_config(dev, peak, PADDED_LARGE)
+        torch.cuda.empty_cache()
         cfg.update(ndhwc_configs(dev, peak))
     cpu = cpu_baseline(base) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank != 0:

@@ -141,11 +141,16 @@ __device__ __forceinline__ uint4 roll_take(float* src, int f) {
 
 // K3 (a specialization): fixed 3x3x3 windows with stride 2, sizes known at
 // compile time; the stored index is decoded with compares instead of
-// divisions (496 -> 484 us on the 32x128x16x112x112 fp16 backward). AL:
+// divisions (496 -> 484 us on the 32x128x16x112x112 fp16 backward). KP:
+// K3 windows padded by at most one position per side (window o starts at
+// 2o - p); the decode also checks that the index lies in the plane and its
+// column inside the input, so an index outside its window still adds
+// nothing. AL:
 // every row span starts on a 16-byte boundary and holds a whole number of
 // 16-byte chunks (W and D*H*W multiples of the vector width), so the store
 // has no ragged ends.
-template <typename T, bool AD, int NT, int WPT, int MINB, bool K3 = false, bool AL = false>
+template <typename T, bool AD, int NT, int WPT, int MINB, bool K3 = false, bool AL = false,
+          bool KP = false>
 __global__ void __launch_bounds__(NT, MINB)
 k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
            RollGeo rg) {
@@ -181,6 +186,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
         // and (adaptive) its lengths and the distances to the next windows
         int wo[WPT];
         int wsh[WPT];    // adaptive: kh | kw << 8 | sh << 16 | sw << 24 (each < 256)
+        int wcol[WPT];   // KP: the window's first column (-1 when padded)
 #pragma unroll
         for (int k = 0; k < WPT; ++k) {
             const int me = tid + k * NT;
@@ -188,6 +194,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
             const int oh = min(ohl + row, g.OH - 1), ow = me - row * OW;   // slots past nw stay idle
             const int hs = ax_start<AD>(rg.ah, oh), ws = ax_start<AD>(rg.aw, ow);
             wo[k] = hs * W + ws;
+            wcol[k] = ws;
             if constexpr (AD) {
                 const int kh = ax_end<AD>(rg.ah, oh) - hs, kw = ax_end<AD>(rg.aw, ow) - ws;
                 const int sh = oh + 1 < g.OH ? ax_start<AD>(rg.ah, oh + 1) - hs : 255;
@@ -211,8 +218,9 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
         int cs = 0, sbc = 0;            // first slice the row completes and its ring slot
         __syncthreads();   // the ring is clear (first unit: initialised) before any pass
         for (int od = 0; od < OD; ++od) {
-            const int ods = K3 ? 2 * od : ax_start<AD>(rg.ad, od);   // window origin (before 0 when padded)
-            const int oe = K3 ? 2 * od + 3 : ax_end<AD>(rg.ad, od);
+            const int pdk = KP ? g.pd : 0;
+            const int ods = K3 ? 2 * od - pdk : ax_start<AD>(rg.ad, od);   // window origin (before 0 when padded)
+            const int oe = K3 ? ods + 3 : ax_end<AD>(rg.ad, od);
             const int kd = oe - ods;                   // window length along d
             const int de = min(oe, g.D);               // slices at or beyond de are in no window
             int sbo = ods % RS;                        // ring slot of the origin
@@ -247,9 +255,11 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                     const bool h1 = rem >= W, h2 = rem >= 2 * W;
                     const int offw = rem - (h1 ? W : 0) - (h2 ? W : 0);
                     const int loc = wo[k] + rem - h0W;        // place inside the h-tile's rows
-                    const bool ok = (int)(j >> 32) == 0 && (unsigned)rel < (unsigned)(3 * HW) &&
-                                    (unsigned)rem < (unsigned)(3 * W) && (unsigned)offw < 3u &&
-                                    (unsigned)loc < (unsigned)L;
+                    bool ok = (int)(j >> 32) == 0 && (unsigned)rel < (unsigned)(3 * HW) &&
+                              (unsigned)rem < (unsigned)(3 * W) && (unsigned)offw < 3u &&
+                              (unsigned)loc < (unsigned)L;
+                    if constexpr (KP)
+                        ok = ok && (unsigned)(int)j < (unsigned)g.vol && (unsigned)(wcol[k] + offw) < (unsigned)W;
                     off[k] = (d2 ? a3[2] : d1 ? a3[1] : a3[0]) + (wo[k] + rel) * (int)sizeof(float);
                     key[k] = ok ? ((h2 ? 0 : 2) | (offw >= 2 ? 0 : 1)) : 4;
                     if (ok && __float_as_uint(gv[k]) == 0x80000000u) {
@@ -311,7 +321,7 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 __syncthreads();
             }
             // 3. round and store the completed slices [cs, dn), clear their accumulators
-            const int dn = od + 1 < OD ? (K3 ? 2 * od + 2 : max(ax_start<AD>(rg.ad, od + 1), 0)) : g.D;
+            const int dn = od + 1 < OD ? (K3 ? max(2 * od + 2 - pdk, 0) : max(ax_start<AD>(rg.ad, od + 1), 0)) : g.D;
             const int nring = min(dn, de) - cs;        // completed slices held in the ring
             const int stored = ((1 << nring) - 1) << sbc | ((1 << nring) - 1) >> (RS - sbc);
             const int marked = *slotmask & stored;
@@ -518,11 +528,11 @@ bool roll_plan(const Geo& g, int es, long long min_units, const RollCfg& cfg, Ro
     return false;
 }
 
-template <typename T, bool AD, int WPT, bool K3 = false, bool AL = false>
+template <typename T, bool AD, int WPT, bool K3 = false, bool AL = false, bool KP = false>
 cudaError_t roll_launch(const void* go, const int64_t* idx, void* gi, const Geo& g,
                         const RollGeo& rg, size_t smem, cudaStream_t s) {
     constexpr RollCfg cfg = K3 ? kRollCfgK3 : kRollCfg;
-    auto kern = k_bwd_roll<T, AD, cfg.nt, WPT, cfg.minb, K3, AL>;
+    auto kern = k_bwd_roll<T, AD, cfg.nt, WPT, cfg.minb, K3, AL, KP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = g.P * rg.nht;
@@ -540,11 +550,15 @@ cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, i
     int wpt = 0;
     // one wave of CTAs at minb per SM
     const bool k3 = !g.adaptive && g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 &&
-                    g.sw == 2 && g.pd == 0 && g.ph == 0 && g.pw == 0 && g.W % VEC == 0 &&
+                    g.sw == 2 && g.pd <= 1 && g.ph <= 1 && g.pw <= 1 && g.W % VEC == 0 &&
                     g.vol % VEC == 0;
+    // padded, or ceil-mode sizes: windows reach past the input
+    const bool reach = g.pd || g.ph || g.pw || g.OD != (g.D - 3) / 2 + 1 || g.OH != (g.H - 3) / 2 + 1 ||
+                       g.OW != (g.W - 3) / 2 + 1;
     if (k3 && roll_plan(g, sizeof(T), 1LL * sms * kRollCfgK3.minb, kRollCfgK3, &rg, &smem, &wpt) &&
         wpt == 4)
-        return roll_launch<T, false, 4, true, true>(go, idx, gi, g, rg, smem, s);
+        return reach ? roll_launch<T, false, 4, true, true, true>(go, idx, gi, g, rg, smem, s)
+                     : roll_launch<T, false, 4, true, true, false>(go, idx, gi, g, rg, smem, s);
     if (!roll_plan(g, sizeof(T), 1LL * sms * kRollCfg.minb, kRollCfg, &rg, &smem, &wpt))
         return cudaErrorNotSupported;
     if (g.adaptive) {

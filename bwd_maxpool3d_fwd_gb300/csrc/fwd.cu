@@ -559,20 +559,24 @@ int set_pipeline_wait_limit(int polls) {
 // memory (and no barriers around their flush), 466 -> 412 us on the
 // 32x128x16x112x112 fp16 forward.
 //
-// PAD: windows padded by g.pd, g.ph, g.pw in {0, 1} (3x3x3 windows, stride
-// 2, floor output sizes): window o starts at 2o - p. A position outside the
+// PADC: windows padded by pd = bit 0, ph = bit 1, pw = bit 2 of PADC (one
+// position per side at most; 3x3x3 windows, stride 2, floor output sizes),
+// compiled per combination, at four CTAs per SM (the padded forms' extra
+// state spills at five: 788 -> 430 us on the 32x128x16x112x112 fp16
+// forward with padding 1): window o starts at 2o - p. A position outside the
 // input is read as its nearest position inside (the clamped slice, row or
 // column) carrying that position's own offset in the window as its code:
 // such a duplicate is either the same element as a candidate met earlier,
 // or comes first and bears the code of the real element that follows it,
 // so ties still go to the first real occurrence and padding is never chosen.
-template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS, bool PAD = false>
-__global__ void __launch_bounds__(128, 5)
+template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS, int PADC = 0>
+__global__ void __launch_bounds__(128, PADC ? 4 : 5)
 k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
          int nq, int G, int nbands, int nc, int wait_limit) {
     static_assert(KD <= 2 * SD && KD <= 4 && KH <= 4 && KW >= 2 && KW <= 3, "shape");
+    constexpr bool PAD = PADC != 0;
     static_assert(!PAD || (KD == 3 && SD == 2 && KH == 3 && SH == 2 && KW == 3), "padded shape");
-    const int pd = PAD ? g.pd : 0, ph = PAD ? g.ph : 0, pw = PAD ? g.pw : 0;
+    constexpr int pd = PADC & 1, ph = (PADC >> 1) & 1, pw = (PADC >> 2) & 1;
     extern __shared__ __align__(128) unsigned char smem[];
     const int band = (int)(blockIdx.x % nbands);
     long long rest = blockIdx.x / nbands;
@@ -974,7 +978,7 @@ bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
     return true;
 }
 
-template <typename T, int KD, int SD, int KH, int SH, int KW, bool PAD = false>
+template <typename T, int KD, int SD, int KH, int SH, int KW, int PADC = 0>
 static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                             cudaStream_t s) {
     constexpr int TOH = 4, NS = 2;
@@ -996,7 +1000,7 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
     const int band_rows = (G * TOH - 1) * SH + KH;
     const size_t stage = ((size_t)band_rows * g.W * sizeof(T) + 127) / 128 * 128;
     const size_t smem = NS * stage + NS * 8;
-    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS, PAD>;
+    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS, PADC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long blocks = g.P * nq * nbands;
@@ -1008,7 +1012,16 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
 template <typename T>
 static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                                    cudaStream_t s) {
-    if (g.pd || g.ph || g.pw) return fwd_s2_t<T, 3, 2, 3, 2, 3, true>(x, y, idx, g, sms, s);
+    switch (g.pd | g.ph << 1 | g.pw << 2) {
+    case 0: break;
+    case 1: return fwd_s2_t<T, 3, 2, 3, 2, 3, 1>(x, y, idx, g, sms, s);
+    case 2: return fwd_s2_t<T, 3, 2, 3, 2, 3, 2>(x, y, idx, g, sms, s);
+    case 3: return fwd_s2_t<T, 3, 2, 3, 2, 3, 3>(x, y, idx, g, sms, s);
+    case 4: return fwd_s2_t<T, 3, 2, 3, 2, 3, 4>(x, y, idx, g, sms, s);
+    case 5: return fwd_s2_t<T, 3, 2, 3, 2, 3, 5>(x, y, idx, g, sms, s);
+    case 6: return fwd_s2_t<T, 3, 2, 3, 2, 3, 6>(x, y, idx, g, sms, s);
+    default: return fwd_s2_t<T, 3, 2, 3, 2, 3, 7>(x, y, idx, g, sms, s);
+    }
     // 2x2x2 windows tiling the input: direct loads, one thread per four windows
     if (s2_variant(g) == 0 && g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW &&
         g.OW % 4 == 0 && (uintptr_t)y % 8 == 0 && (uintptr_t)idx % 16 == 0) {

@@ -116,3 +116,43 @@ def test_padded_workload_full():
     assert torch.equal(idx.cpu(), i_ref)
     assert_bits_equal(y.cpu(), y_ref, "y (padded workload)")
     assert_bits_equal(gin.cpu(), gin_ref, "grad_in (padded workload)")
+
+
+def test_padded_large_workload_full():
+    # 3x3x3 windows, stride 2, padding 1 at the size of the k3s2 workload
+    # (its input, ties included), forward and backward on every plane
+    # against the oracle, checked in chunks of planes on a thread pool
+    w = workloads.WORKLOADS[3]
+    k, s, p = (3, 3, 3), (2, 2, 2), (1, 1, 1)
+    x = workloads.make_x(w)
+    out = mp.pool_out_size_ex((w.D, w.H, w.W), k, s, p)
+    gen = torch.Generator().manual_seed(20261303)
+    g = torch.randn((w.N, w.C) + out, generator=gen).half()
+    xd, gd = x.to(DEV), g.to(DEV)
+    y = torch.empty(g.shape, dtype=torch.float16, device=DEV)
+    idx = torch.empty(g.shape, dtype=torch.int64, device=DEV)
+    gin = torch.empty(w.in_shape, dtype=torch.float16, device=DEV)
+    assert mp.maxpool3d_fwd_ex_plan(w.in_shape, k, s, p, (1, 1, 1), False, torch.float16) == "fwd_s2"
+    mp.maxpool3d_fwd_ex(xd, y, idx, k, s, p)
+    mp.maxpool3d_bwd_ex(gd, idx, gin, k, s, p)
+    torch.cuda.synchronize()
+    y, idx, gin = y.cpu(), idx.cpu(), gin.cpu()
+    del xd, gd
+    P = w.planes
+
+    def chunk(b):
+        p0, p1 = b
+        n = p1 - p0
+        xs = x.reshape(P, w.D, w.H, w.W)[p0:p1].reshape(1, n, w.D, w.H, w.W)
+        gs = g.reshape(P, *out)[p0:p1].reshape(1, n, *out)
+        y_ref, i_ref = oracle.maxpool3d_fwd_ex(xs, k, s, p, (1, 1, 1), False)
+        gin_ref = oracle.maxpool3d_bwd(gs, i_ref, (w.D, w.H, w.W))
+        return (p0, torch.equal(idx.reshape(P, -1)[p0:p1], i_ref.reshape(n, -1)),
+                torch.equal(bits(y.reshape(P, -1)[p0:p1]), bits(y_ref.reshape(n, -1))),
+                torch.equal(bits(gin.reshape(P, -1)[p0:p1]), bits(gin_ref.reshape(n, -1))))
+
+    bounds = [(q, min(q + 64, P)) for q in range(0, P, 64)]
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(chunk, bounds))
+    bad = [r for r in results if not all(r[1:])]
+    assert not bad, f"planes differing from the oracle (first plane of chunk, idx, y, grad_in): {bad[:4]}"
