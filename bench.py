@@ -42,8 +42,10 @@ DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"
 
 # ---------------------------------------------------------------- bytes
 
-def covered_extent(I, k, s, O):
-    return (O - 1) * s + k
+def covered_extent(I, k, s, O, p=0):
+    """Input positions along one axis that some window covers (windows start
+    at o*s - p and never read padding)."""
+    return min(I, (O - 1) * s - p + k) - max(0, -p)
 
 
 def algorithmic_bytes(w):
@@ -54,8 +56,8 @@ def algorithmic_bytes(w):
     ovol = w.out[0] * w.out[1] * w.out[2]
     if w.mode == "fixed":
         cov = 1
-        for I, k, s, O in zip((w.D, w.H, w.W), w.kernel, w.stride, w.out):
-            cov *= covered_extent(I, k, s, O)
+        for I, k, s, O, p in zip((w.D, w.H, w.W), w.kernel, w.stride, w.out, w.pad):
+            cov *= covered_extent(I, k, s, O, p)
     else:
         cov = w.D * w.H * w.W        # adaptive windows cover every input
     vol = w.D * w.H * w.W
@@ -171,6 +173,11 @@ class Runner:
         mp, w = self.mp, self.w
         if self.layout == "ndhwc":
             return "fwd_ndhwc", "bwd_ndhwc"
+        if any(w.pad):
+            return (mp.maxpool3d_fwd_ex_plan(w.in_shape, w.kernel, w.stride, w.pad, (1, 1, 1), False,
+                                             w.dtype),
+                    mp.maxpool3d_bwd_ex_plan(w.in_shape, w.out, w.kernel, w.stride, w.pad, (1, 1, 1),
+                                             False, w.dtype, self.algo))
         if w.mode == "fixed":
             pf = mp.maxpool3d_fwd_plan(w.in_shape, w.kernel, w.stride, w.dtype)
         else:
@@ -191,7 +198,9 @@ class Runner:
 
     def fwd_values(self):
         """Values-only forward (no index buffer)."""
-        if self.w.mode == "fixed":
+        if any(self.w.pad):
+            self.mp.maxpool3d_fwd_ex(self.x, self.y, None, self.w.kernel, self.w.stride, self.w.pad)
+        elif self.w.mode == "fixed":
             self.mp.maxpool3d_fwd(self.x, self.y, None, self.w.kernel, self.w.stride)
         else:
             self.mp.adaptive_maxpool3d_fwd(self.x, self.y, None, self.w.out)
@@ -206,7 +215,9 @@ class Runner:
             else:
                 self.mp.adaptive_maxpool3d_fwd_ndhwc(x, y, idx, self.w.out)
             return
-        if self.w.mode == "fixed":
+        if any(self.w.pad):
+            self.mp.maxpool3d_fwd_ex(x, y, idx, self.w.kernel, self.w.stride, self.w.pad)
+        elif self.w.mode == "fixed":
             self.mp.maxpool3d_fwd(x, y, idx, self.w.kernel, self.w.stride)
         else:
             self.mp.adaptive_maxpool3d_fwd(x, y, idx, self.w.out)
@@ -217,6 +228,10 @@ class Runner:
         gin = self.gin if gin is None else gin
         if self.layout == "ndhwc":
             self.mp.maxpool3d_bwd_ndhwc(g, idx, gin, self.k, self.s)
+            return
+        if any(self.w.pad):
+            self.mp.maxpool3d_bwd_ex(g, idx, gin, self.k, self.s, self.w.pad, algo=self.algo,
+                                     workspace=self.ws)
             return
         self.mp.maxpool3d_bwd(g, idx, gin, self.k, self.s, algo=self.algo, workspace=self.ws)
 
@@ -274,14 +289,16 @@ def time_one(fn, dev, iters, flush):
     return statistics.median(ts)
 
 
-# Sources of the two kernels the traffic record covers (the stride-2 forward
-# and the rolling backward) and the headers they include.
-TRAFFIC_SOURCES = ("bwd_roll.cu", "common.cuh", "fwd.cu", "internal.h")
+# Sources each kernel's traffic record depends on (the kernel's file and the
+# headers it includes): a record applies only while their hash is the one
+# stored with it.
+TRAFFIC_SOURCES = {"fwd": ("fwd.cu", "common.cuh", "internal.h"),
+                   "bwd": ("bwd_roll.cu", "common.cuh", "internal.h")}
 
 
-def kernel_hash():
+def kernel_hash(kind):
     h = hashlib.sha256()
-    for name in TRAFFIC_SOURCES:
+    for name in TRAFFIC_SOURCES[kind]:
         with open(os.path.join(ROOT, "bwd_maxpool3d_fwd_gb300", "csrc", name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:12]
@@ -291,19 +308,20 @@ TRAFFIC_WORKLOAD = "fixed_k3s2_f16_32x128x16x112x112"
 
 
 def recorded_traffic(kernel_kind, workload_name, full):
-    """DRAM bytes per launch from the committed ncu summary, if this run is
-    the whole workload the summary was taken on and the kernel sources are
-    the ones it was taken on; else None."""
-    if workload_name != TRAFFIC_WORKLOAD or not full:
+    """DRAM bytes per launch of the whole workload from the committed ncu
+    record (a capture of a subset of planes, scaled by the planes; see the
+    record's header), if this run is the whole workload the record is for
+    and the kernel's sources are the ones it was taken on; else None."""
+    if not full:
         return None
-    path = os.path.join(ROOT, "profiles", f"dram_traffic_{TRAFFIC_WORKLOAD}.txt")
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload_name}.txt")
     try:
         with open(path) as f:
             kv = dict(ln.split(":", 1) for ln in f if ":" in ln and not ln.startswith("#"))
     except OSError:
         return None
     kv = {k.strip(): v.strip() for k, v in kv.items()}
-    if kv.get("kernel_sources_sha256_12") != kernel_hash():
+    if kv.get(f"{kernel_kind}_sources_sha256_12") != kernel_hash(kernel_kind):
         return None
     v = kv.get(f"{kernel_kind}_dram_bytes_per_launch")
     return int(v) if v else None
@@ -314,7 +332,9 @@ def recorded_traffic(kernel_kind, workload_name, full):
 def oracle_step(w, x, g):
     """One pass of the oracle over the given planes: forward then backward."""
     import oracle
-    if w.mode == "fixed":
+    if any(w.pad):
+        _, idx = oracle.maxpool3d_fwd_ex(x, w.kernel, w.stride, w.pad, (1, 1, 1), False)
+    elif w.mode == "fixed":
         _, idx = oracle.maxpool3d_fwd(x, w.kernel, w.stride)
     else:
         _, idx = oracle.adaptive_maxpool3d_fwd(x, w.out)
@@ -354,7 +374,7 @@ def workload_config(base, layout, world):
     """The `config` object of both arms' JSON lines."""
     return {"workload": base.name, "input": list(base.in_shape),
             "output": list(base.out_shape), "kernel": list(base.kernel),
-            "stride": list(base.stride), "layout": layout,
+            "stride": list(base.stride), "padding": list(base.pad), "layout": layout,
             "l2": ("inputs larger than L2 (%d MB input); no flush between steps"
                    % (base.planes * base.D * base.H * base.W * base.elem_bytes // 10**6)),
             "parallelism": f"independent shards x{world}"}
@@ -362,7 +382,7 @@ def workload_config(base, layout, world):
 
 def reference_arm(args):
     """The oracle as the reference implementation, timed on the host cores."""
-    w = workloads.WORKLOADS[args.workload]
+    w = workloads.by_name_or_index(args.workload)
     if int(os.environ.get("RANK", "0")) != 0:
         return None
     per_plane = cpu_plane_seconds(w)
@@ -622,7 +642,7 @@ def our_arm(args):
     torch.cuda.set_device(dev)
     import bwd_maxpool3d_fwd_gb300 as mp
     mp.lib()                                     # fail loudly if the library is missing
-    base = workloads.WORKLOADS[args.workload]
+    base = workloads.by_name_or_index(args.workload)
     cl = args.layout == "ndhwc"
     if args.planes:
         import dataclasses
@@ -716,7 +736,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", type=int, default=HEADLINE)
+    ap.add_argument("--workload", default=str(HEADLINE),
+                    help="index of one of the five workloads, or a workload name (e.g. "
+                         "fixed_k3s2p1_f16_32x128x16x112x112, the padded form of workload 3)")
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",

@@ -39,6 +39,7 @@ class Workload:
     x_recipe: str = "normal"   # "perm", "uniform", "normal", "normal_dup5"
     g_recipe: str = "normal"
     seed: int = BASE_SEED
+    pad: tuple = (0, 0, 0)     # fixed windows: padding per side (output sizes as stated)
 
     @property
     def planes(self) -> int:
@@ -77,6 +78,26 @@ WORKLOADS = [
     Workload("adaptive_global_f32_64x512x8x14x14", "adaptive", torch.float32,
              64, 512, 8, 14, 14, (1, 1, 1), x_recipe="uniform", seed=BASE_SEED + 4),
 ]
+
+
+# Further workloads the benchmark can time (not among the five above): the
+# k3s2 workload's input with padding 1 on every side, 3x3x3 windows, stride
+# 2 -> 8x56x56 outputs.
+EXTRA = [
+    Workload("fixed_k3s2p1_f16_32x128x16x112x112", "fixed", torch.float16,
+             32, 128, 16, 112, 112, (8, 56, 56), (3, 3, 3), (2, 2, 2),
+             x_recipe="normal_dup5", seed=BASE_SEED + 3, pad=(1, 1, 1)),
+]
+
+
+def by_name_or_index(key) -> Workload:
+    """A workload of WORKLOADS by index, or of WORKLOADS + EXTRA by name."""
+    if isinstance(key, int) or str(key).isdigit():
+        return WORKLOADS[int(key)]
+    for w in WORKLOADS + EXTRA:
+        if w.name == key:
+            return w
+    raise KeyError(f"no workload {key!r}")
 
 
 def _chunk_seed(seed: int, chunk: int, stream: int) -> int:

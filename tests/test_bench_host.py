@@ -21,7 +21,7 @@ def test_traffic_record_scope(monkeypatch):
     assert full > 0 and bench.recorded_traffic("fwd", name, True) > 0
     assert bench.recorded_traffic("bwd", name, False) is None          # a subset of planes
     assert bench.recorded_traffic("bwd", "adaptive_f16_16x64x30x50x50_to_8x12x12", True) is None
-    monkeypatch.setattr(bench, "kernel_hash", lambda: "000000000000")
+    monkeypatch.setattr(bench, "kernel_hash", lambda kind: "000000000000")
     assert bench.recorded_traffic("bwd", name, True) is None           # other sources
 
 
@@ -29,5 +29,6 @@ def test_workload_config_keys():
     w = workloads.WORKLOADS[bench.HEADLINE]
     cfg = bench.workload_config(w, "ncdhw", 1)
     assert cfg["workload"] == w.name == bench.TRAFFIC_WORKLOAD
-    assert set(cfg) == {"workload", "input", "output", "kernel", "stride", "layout", "l2", "parallelism"}
+    assert set(cfg) == {"workload", "input", "output", "kernel", "stride", "padding", "layout", "l2",
+                        "parallelism"}
     assert cfg["input"] == [32, 128, 16, 112, 112] and cfg["output"] == [32, 128, 7, 55, 55]
