@@ -28,3 +28,36 @@ def test_summaries_name_existing_kernels():
         text = open(os.path.join(PROFILES, name)).read()
         for kernel in set(re.findall(r"\b(k_[a-z0-9_]+)<", text)):
             assert re.search(rf"\b{kernel}\(", src), f"{name}: {kernel} not in the sources"
+
+
+def _ncu_commands(text):
+    """Every ncu command line in a summary, with continuation lines joined
+    (commands in a .txt record sit behind '#')."""
+    lines = [ln.lstrip("#").strip() for ln in text.splitlines()]
+    joined, cur = [], ""
+    for ln in lines:
+        if ln.endswith("\\"):
+            cur += ln[:-1] + " "
+            continue
+        joined.append(cur + ln)
+        cur = ""
+    return [c for c in joined if c.startswith("ncu ")]
+
+
+def test_captures_are_small_and_single_kernel():
+    # a capture that collects more than the launch duration names one kernel
+    # (no alternation), one to three launches, and a small case: a subset of
+    # planes, or one of the workloads of a few hundred MB
+    small_workloads = {"0", "1", "2", "4"}
+    for name in sorted(os.listdir(PROFILES)):
+        for cmd in _ncu_commands(open(os.path.join(PROFILES, name)).read()):
+            metrics = re.search(r"--metrics (\S+)", cmd)
+            if metrics and metrics.group(1) == "gpu__time_duration.sum" and "--set" not in cmd:
+                continue
+            k = re.search(r"-k regex:(\S+)", cmd)
+            assert k and "|" not in k.group(1), f"{name}: capture without a single kernel: {cmd}"
+            c = re.search(r"-c (\d+)", cmd)
+            assert c and 1 <= int(c.group(1)) <= 3, f"{name}: capture of more than three launches: {cmd}"
+            w = re.search(r"--workload (\S+)", cmd)
+            assert "--planes" in cmd or (w and w.group(1) in small_workloads), (
+                f"{name}: capture on a full-size large workload: {cmd}")
