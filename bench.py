@@ -463,8 +463,10 @@ def smi_id(dev):
 
 def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
     """Same metric through the public API with host buffers: each step copies
-    its inputs from pinned host memory, runs forward + backward, and copies
-    every result (y, idx, grad_in) back to pinned host memory. Steps are
+    its inputs (x, grad_out) from pinned host memory, runs forward + backward,
+    and copies its results (the pooled values y and grad_in) back to pinned
+    host memory; the int64 indices stay on the device, where the backward
+    consumes them (a caller keeps them there between the two calls). Steps are
     pipelined the way a data loader would run them: two sets of device
     buffers, the copies in, the compute and the copies out on three streams
     ordered by events, so step k + 1's inputs travel while step k computes
@@ -473,14 +475,13 @@ def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
     w = r.w
     xh, gh = x_cpu.pin_memory(), g_cpu.pin_memory()
     yh = torch.empty(r.y.shape, dtype=w.dtype).pin_memory()
-    ih = torch.empty(r.idx.shape, dtype=torch.int64).pin_memory()
     ginh = torch.empty(r.gin.shape, dtype=w.dtype).pin_memory()
     bufs = [(r.x, r.g, r.y, r.idx, r.gin),
             tuple(torch.empty_like(t) for t in (r.x, r.g, r.y, r.idx, r.gin))]
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     cmp_done = [ev(), ev()]   # compute of the set's last step (it read x, g)
-    out_done = [ev(), ev()]   # copies out of the set's last step (they read y, idx, grad_in)
+    out_done = [ev(), ev()]   # copies out of the set's last step (they read y, grad_in)
     for e in cmp_done + out_done:
         e.record(torch.cuda.current_stream())
 
@@ -501,7 +502,6 @@ def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
         s_out.wait_event(cmp_done[k % 2])
         with torch.cuda.stream(s_out):
             yh.copy_(y, non_blocking=True)
-            ih.copy_(idx, non_blocking=True)
             ginh.copy_(gin, non_blocking=True)
             out_done[k % 2].record(s_out)
 
@@ -519,7 +519,7 @@ def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
     del bufs
     fb, bb = algorithmic_bytes(w)
     h2d = xh.numel() * xh.element_size() + gh.numel() * gh.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in (yh, ih, ginh))
+    d2h = sum(t.numel() * t.element_size() for t in (yh, ginh))
     return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
 
