@@ -395,6 +395,165 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
     }
 }
 
+// ------------------------------------------------------------------ exchange store
+// Adaptive windows whose inputs outnumber them many times over (most of
+// grad_in is zeros): the same decode, ring and ordered passes as k_bwd_roll,
+// but the slices a window row completes are written without reading their
+// accumulators. Every element of those slices is first stored as +0 with
+// 16-byte stores; then each window whose chosen input lies in them takes
+// that input's accumulator with a shared atomicExch(acc, 0), which reads the
+// sum and clears the accumulator in one step, and stores the rounded sum
+// when it is not +0. Several windows of one input: the first exchange gets
+// the sum and the others +0, so which is first does not matter. An input
+// whose terms are all -0 keeps +0 in its accumulator; a window with a -0
+// gradient that gets +0 re-reads the input's covering windows and stores -0
+// when every term is -0. A window whose input lies in a slice the next row
+// also covers takes it when the next row completes that slice.
+template <typename T, int NT, int WPT, int MINB>
+__global__ void __launch_bounds__(NT, MINB)
+k_bwd_xroll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
+            RollGeo rg) {
+    constexpr int VEC = 16 / sizeof(T);
+    extern __shared__ __align__(16) float ring[];
+    const int RS = rg.RS, SSTR = rg.SSTR;
+    const int nacc = RS * SSTR;
+    const int tid = threadIdx.x;
+    const int W = g.W, HW = g.H * g.W, OW = g.OW, OD = g.OD;
+    {
+        float4* r4 = reinterpret_cast<float4*>(ring);
+        for (int i = tid; i < nacc / 4; i += NT) r4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const long long units = g.P * rg.nht;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const long long p = u / rg.nht;
+        const int h0 = (int)(u - p * rg.nht) * rg.TH;
+        const int h1 = min(h0 + rg.TH, g.H);
+        const int h0W = h0 * W;
+        const int L = (h1 - h0) * W;
+        const int ohl = ax_lo<true>(rg.ah, h0), ohh = ax_hi<true>(rg.ah, h1 - 1);
+        const int nw = ohh >= ohl ? (ohh - ohl + 1) * OW : 0;
+        T* gplane = gi + p * (long long)g.vol;
+        int wo[WPT], wsh[WPT];
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) {
+            const int me = tid + k * NT;
+            const int row = rg.fOW.div(me);
+            const int oh = min(ohl + row, g.OH - 1), ow = me - row * OW;
+            const int hs = ax_start<true>(rg.ah, oh), ws = ax_start<true>(rg.aw, ow);
+            wo[k] = hs * W + ws;
+            const int kh = ax_end<true>(rg.ah, oh) - hs, kw = ax_end<true>(rg.aw, ow) - ws;
+            const int sh = oh + 1 < g.OH ? ax_start<true>(rg.ah, oh + 1) - hs : 255;
+            const int sw = ow + 1 < OW ? ax_start<true>(rg.aw, ow + 1) - ws : 255;
+            wsh[k] = kh | kw << 8 | sh << 16 | sw << 24;
+        }
+        const long long rstride = (long long)g.OH * OW;
+        const int64_t* ip = idx + p * (long long)g.ovol + (long long)ohl * OW + tid;
+        const T* gp = go + p * (long long)g.ovol + (long long)ohl * OW + tid;
+        int64_t rj[WPT];
+        T rgd[WPT];
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) {
+            const bool in = tid + k * NT < nw;
+            rj[k] = in ? __ldg(ip + k * NT) : -1;
+            rgd[k] = in ? gp[k * NT] : Elem<T>::from_f(0.0f);
+        }
+        int pj[WPT], poff[WPT];        // windows of the previous row to take in this row
+        unsigned pneg = 0u;
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) pj[k] = poff[k] = -1;
+        int cs = 0;                    // first slice not yet written
+        __syncthreads();
+        for (int od = 0; od < OD; ++od) {
+            const int ods = ax_start<true>(rg.ad, od);
+            const int kd = ax_end<true>(rg.ad, od) - ods;
+            const int sbo = ods % RS;
+            const int dsHW = ods * HW;
+            const int dn = od + 1 < OD ? ax_start<true>(rg.ad, od + 1) : g.D;   // [cs, dn) complete
+            int key[WPT], off[WPT], jl[WPT];
+            float gv[WPT];
+            unsigned cneg = 0u;
+#pragma unroll
+            for (int k = 0; k < WPT; ++k) {
+                const int64_t j = rj[k];
+                gv[k] = Elem<T>::to_f(rgd[k]);
+                jl[k] = (int)j;
+                const int rel = (int)j - dsHW - wo[k];
+                const int offd = rg.fHW.div(rel);
+                const int rem = rel - offd * HW;
+                const int offh = rg.fW.div(rem);
+                const int offw = rem - offh * W;
+                const int kh = wsh[k] & 255, kw = (wsh[k] >> 8) & 255;
+                const int sh = (wsh[k] >> 16) & 255, sw = (unsigned)wsh[k] >> 24;
+                const int loc = wo[k] - h0W + rem;
+                const bool ok = (uint64_t)j < (uint64_t)g.vol && rel >= 0 && offd < kd && offh < kh &&
+                                offw < kw && (unsigned)loc < (unsigned)L;
+                int slot = sbo + offd;
+                slot -= slot >= RS ? RS : 0;
+                off[k] = (slot * SSTR + loc) * (int)sizeof(float);
+                // 0-3: pass; 4: nothing; bit 3: the next row completes the input's slice
+                key[k] = ok ? ((offh >= sh ? 0 : 2) | (offw >= sw ? 0 : 1) | (ods + offd >= dn ? 8 : 0)) : 4;
+                if (ok && __float_as_uint(gv[k]) == 0x80000000u) cneg |= 1u << k;
+            }
+            if (od + 1 < OD) {
+                ip += rstride;
+                gp += rstride;
+#pragma unroll
+                for (int k = 0; k < WPT; ++k) {
+                    if (tid + k * NT < nw) {
+                        rj[k] = __ldg(ip + k * NT);
+                        rgd[k] = gp[k * NT];
+                    }
+                }
+            }
+            // zeros into the tile's rows of the slices this row completes
+            for (int s = cs; s < dn; ++s) {
+                T* base = gplane + s * HW + h0W;
+                const int head = (int)(((16 - ((uintptr_t)base & 15)) & 15) / sizeof(T));
+                const int hd = head < L ? head : L;
+                const int nv = (L - hd) / VEC;
+                for (int e = tid; e < hd; e += NT) base[e] = Elem<T>::from_f(0.0f);
+                uint4* v4 = reinterpret_cast<uint4*>(base + hd);
+                for (int c = tid; c < nv; c += NT) v4[c] = make_uint4(0u, 0u, 0u, 0u);
+                for (int e = hd + nv * VEC + tid; e < L; e += NT) base[e] = Elem<T>::from_f(0.0f);
+            }
+            // four ordered passes
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int k = 0; k < WPT; ++k)
+                    if ((key[k] & 7) == q) {
+                        float* a = reinterpret_cast<float*>(reinterpret_cast<char*>(ring) + off[k]);
+                        *a += gv[k];
+                    }
+                __syncthreads();
+            }
+            auto take = [&](int aoff, int jj, bool neg) {
+                unsigned* a = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ring) + aoff);
+                const unsigned v = atomicExch(a, 0u);
+                if (v != 0u)
+                    gplane[jj] = Elem<T>::from_f(__uint_as_float(v));
+                else if (neg && roll_all_negzero<T, true>(go, idx, p, jj, g, rg))
+                    gplane[jj] = Elem<T>::from_f(-0.0f);
+            };
+#pragma unroll
+            for (int k = 0; k < WPT; ++k)
+                if (pj[k] >= 0) take(poff[k], pj[k], (pneg >> k) & 1u);
+#pragma unroll
+            for (int k = 0; k < WPT; ++k)
+                if (key[k] < 4) take(off[k], jl[k], (cneg >> k) & 1u);
+#pragma unroll
+            for (int k = 0; k < WPT; ++k) {
+                const bool later = key[k] != 4 && (key[k] & 8);
+                pj[k] = later ? jl[k] : -1;
+                poff[k] = off[k];
+            }
+            pneg = cneg;
+            cs = dn;
+            __syncthreads();   // exchanges done before the next row's passes
+        }
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 namespace {
@@ -561,6 +720,20 @@ cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, i
                      : roll_launch<T, false, 4, true, true, false>(go, idx, gi, g, rg, smem, s);
     if (!roll_plan(g, sizeof(T), 1LL * sms * kRollCfg.minb, kRollCfg, &rg, &smem, &wpt))
         return cudaErrorNotSupported;
+    if (g.adaptive && g.vol >= 16LL * g.ovol) {
+        // adaptive windows with many inputs each: the exchange store (the
+        // 16x64x30x50x50 -> 8x12x12 fp16 backward 47.1 -> 41.0 us; on 3x3x3
+        // stride-2 windows, 9.5 inputs each, it measured 565 against 481 us)
+        auto kern = wpt == 1 ? k_bwd_xroll<T, kRollCfg.nt, 1, kRollCfg.minb>
+                  : wpt == 2 ? k_bwd_xroll<T, kRollCfg.nt, 2, kRollCfg.minb>
+                             : k_bwd_xroll<T, kRollCfg.nt, 4, kRollCfg.minb>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const long long units = g.P * rg.nht;
+        kern<<<(unsigned)(units < INT_MAX ? units : INT_MAX), kRollCfg.nt, smem, s>>>((const T*)go, idx,
+                                                                                     (T*)gi, g, rg);
+        return cudaGetLastError();
+    }
     if (g.adaptive) {
         if (wpt == 1) return roll_launch<T, true, 1>(go, idx, gi, g, rg, smem, s);
         if (wpt == 2) return roll_launch<T, true, 2>(go, idx, gi, g, rg, smem, s);

@@ -13,16 +13,19 @@ from bwd_maxpool3d_fwd_gb300 import workloads  # noqa: E402
 
 
 def test_traffic_record_scope(monkeypatch):
+    # each kernel's record applies only to the whole workload it was taken on
+    # and only while that kernel's sources are the ones it was taken on
     name = bench.TRAFFIC_WORKLOAD
-    full = bench.recorded_traffic("bwd", name, True)
-    if full is None:      # the record was taken on other sources: nothing applies
-        assert bench.recorded_traffic("fwd", name, True) is None
-        return
-    assert full > 0 and bench.recorded_traffic("fwd", name, True) > 0
-    assert bench.recorded_traffic("bwd", name, False) is None          # a subset of planes
-    assert bench.recorded_traffic("bwd", "adaptive_f16_16x64x30x50x50_to_8x12x12", True) is None
-    monkeypatch.setattr(bench, "kernel_hash", lambda kind: "000000000000")
-    assert bench.recorded_traffic("bwd", name, True) is None           # other sources
+    for kind in ("fwd", "bwd"):
+        full = bench.recorded_traffic(kind, name, True)
+        if full is None:      # taken on other sources of this kernel: nothing applies
+            continue
+        assert full > 0
+        assert bench.recorded_traffic(kind, name, False) is None         # a subset of planes
+        assert bench.recorded_traffic(kind, "adaptive_f16_16x64x30x50x50_to_8x12x12", True) is None
+        with monkeypatch.context() as m:
+            m.setattr(bench, "kernel_hash", lambda k: "000000000000")
+            assert bench.recorded_traffic(kind, name, True) is None      # other sources
 
 
 def test_workload_config_keys():

@@ -775,3 +775,33 @@ def test_depth_walk_unaligned_input_falls_back(dtype):
     torch.cuda.synchronize()
     assert torch.equal(idx.cpu(), i_ref)
     assert_bits_equal(y.cpu(), y_ref, "y (unaligned x)")
+
+
+XROLL_CASES = [
+    ((2, 3, 13, 17, 19), (3, 4, 4)),      # 87 inputs per window
+    ((1, 4, 30, 50, 50), (8, 12, 12)),    # the adaptive workload's windows
+    ((1, 2, 9, 200, 30), (2, 50, 7)),     # several windows per thread, rows in h-tiles
+    ((2, 2, 7, 33, 41), (2, 2, 2)),       # windows of length 4 and 5 along d
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(XROLL_CASES)))
+def test_adaptive_exchange_backward(case, dtype):
+    # adaptive windows with many inputs each: the backward writes zeros, then
+    # takes each chosen input's sum from its accumulator; compared with the
+    # oracle bit for bit, with -0 gradients mixed in (an input chosen only by
+    # -0 gradients gets -0, one chosen by -0 and +0 gets +0)
+    shape, out = XROLL_CASES[case]
+    gen = torch.Generator().manual_seed(9900 + case)
+    for kind in ("ties", "special"):
+        x = random_input(gen, shape, dtype, kind)
+        _, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+        g = torch.randn(i_ref.shape, generator=gen)
+        r = torch.rand(i_ref.shape, generator=gen)
+        g = torch.where(r < 0.2, torch.tensor(-0.0), g)
+        g = torch.where((r >= 0.2) & (r < 0.25), torch.tensor(0.0), g).to(dtype)
+        gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+        assert mp.maxpool3d_bwd_plan(shape, out, None, None, dtype) == "bwd_overlap_roll"
+        gin = gpu_bwd(g, i_ref, shape)
+        assert_bits_equal(gin, gin_ref, f"grad_in (adaptive exchange backward, {kind})")
