@@ -563,21 +563,24 @@ def test_padded_fwd_bwd(case, dtype):
 
 PADDED_S2_CASES = [
     ((1, 1, 1), (2, 3, 16, 56, 56)),      # even sizes, the bench's padded geometry
-    ((1, 1, 1), (1, 2, 9, 23, 64)),       # odd D and H: the last windows clipped below
-    ((0, 1, 1), (1, 3, 8, 30, 16)),
-    ((1, 0, 1), (1, 2, 7, 17, 24)),
-    ((1, 1, 0), (2, 1, 10, 15, 40)),
+    ((1, 1, 1), (1, 2, 9, 23, 112)),      # odd D and H: the last windows clipped below
+    ((0, 1, 1), (1, 3, 8, 30, 112)),
+    ((1, 0, 1), (1, 2, 7, 17, 112)),
+    ((1, 1, 0), (2, 1, 10, 15, 112)),
     ((0, 0, 1), (1, 2, 5, 9, 8)),         # one chunk per row: the left edge everywhere
-    ((1, 0, 0), (1, 2, 6, 11, 32)),
+    ((1, 0, 0), (1, 2, 6, 11, 112)),
     ((1, 1, 1), (1, 2, 5, 112, 112)),     # several bands of output rows
 ]
+# (rows of 112 elements give the backward's h-tiles more than 256 windows,
+# which the compiled 3x3x3 rolling form takes)
 
 
 @pytest.mark.parametrize("dtype", (torch.float16, torch.bfloat16), ids=str)
 @pytest.mark.parametrize("case", range(len(PADDED_S2_CASES)))
 def test_padded_stride2_forward(case, dtype):
     # 3x3x3 windows, stride 2, padding <= 1: the stride-2 kernel with clamped
-    # slices, rows and columns; ties, signed zeros, infinities and NaNs
+    # slices, rows and columns; ties, signed zeros, infinities and NaNs; then
+    # the backward of the same windows
     p, shape = PADDED_S2_CASES[case]
     k, s = (3, 3, 3), (2, 2, 2)
     assert mp.maxpool3d_fwd_ex_plan(shape, k, s, p, (1, 1, 1), False, dtype) == "fwd_s2"
@@ -600,6 +603,16 @@ def test_padded_stride2_forward(case, dtype):
     assert_bits_equal(yv.cpu(), y_ref, "y (padded stride 2, values only)")
     assert_bits_equal(yu.cpu(), y_ref, "y (padded stride 2, unaligned)")
     assert torch.equal(iu.cpu(), i_ref)
+    # the backward of the same padded windows (the compiled 3x3x3 form where
+    # rows and planes are 16-byte multiples), -0 gradients mixed in
+    g = torch.randn(y_ref.shape, generator=gen)
+    g = torch.where(torch.rand(y_ref.shape, generator=gen) < 0.1, torch.tensor(-0.0), g).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, shape[2:])
+    assert mp.maxpool3d_bwd_ex_plan(shape, y_ref.shape[2:], k, s, p, (1, 1, 1), False, dtype) == "bwd_overlap_roll"
+    assert_bits_equal(_gpu_bwd_ex(g, i_ref, shape, k, s, p, (1, 1, 1), False), gin_ref,
+                      "grad_in (padded stride 2)")
+    gin_a = _gpu_bwd_ex(g, i_ref, shape, k, s, p, (1, 1, 1), False, algo=mp.BWD_ATOMIC)
+    assert _atomic_tolerance_ok(gin_a, gin_ref, g, i_ref, dtype)
 
 
 def test_padded_plain_geometry_matches_plain_entry_points():
