@@ -172,7 +172,7 @@ class Runner:
     def paths(self):
         mp, w = self.mp, self.w
         if self.layout == "ndhwc":
-            return "fwd_ndhwc", "bwd_ndhwc"
+            return "fwd_ndhwc", mp.maxpool3d_bwd_ndhwc_plan(w.in_shape, w.out, self.k, self.s, w.dtype)
         if any(w.pad):
             return (mp.maxpool3d_fwd_ex_plan(w.in_shape, w.kernel, w.stride, w.pad, (1, 1, 1), False,
                                              w.dtype),
@@ -630,7 +630,8 @@ def ndhwc_configs(dev, peak):
             "fwd_us": round(tf * 1e3, 2), "bwd_us": round(tb * 1e3, 2), "fwd_bytes": fb,
             "bwd_bytes": bb, "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
             "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
-            "fwd_path": "fwd_ndhwc", "bwd_path": "bwd_ndhwc"}
+            "fwd_path": "fwd_ndhwc",
+            "bwd_path": mp.maxpool3d_bwd_ndhwc_plan((N, C, D, H, W), w.out, w.kernel, w.stride, w.dtype)}
         del x, g, y, idx, gin
         torch.cuda.empty_cache()
     return out

@@ -26,7 +26,7 @@ PATHS = {0: "noop", 1: "fwd_generic", 2: "fwd_s2", 3: "fwd_global", 4: "fwd_slab
          10: "bwd_disjoint",
          11: "bwd_overlap_tile", 12: "bwd_overlap_direct", 13: "bwd_atomic", 14: "bwd_overlap_roll",
          15: "bwd_padded", 19: "fwd_roll", 16: "bwd_recompute_k2s2", 17: "bwd_recompute_direct", 6: "fwd_ndhwc",
-         18: "bwd_ndhwc"}
+         18: "bwd_ndhwc", 20: "bwd_ndhwc_roll"}
 
 _lib = None
 
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
     L.maxpool3d_fwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 7 + [vp]
     L.adaptive_maxpool3d_fwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 4 + [vp]
     L.maxpool3d_bwd_ndhwc.argtypes = [vp, vp, vp] + [i64] * 5 + [i32] * 10 + [vp]
+    L.maxpool3d_bwd_ndhwc_plan.argtypes = [i64] * 5 + [i32] * 10 + [pi32]
     L.maxpool3d_out_size.argtypes = [i64] * 3 + [i32] * 6 + [pi32] * 3
     L.maxpool3d_ex_out_size.argtypes = [i64] * 3 + [i32] * 13 + [pi32] * 3
     L.mp3d_status_string.argtypes = [i32]
@@ -74,7 +75,8 @@ def lib() -> ctypes.CDLL:
               L.adaptive_maxpool3d_fwd_plan, L.maxpool3d_bwd_plan, L.maxpool3d_fwd_ex,
               L.maxpool3d_bwd_ex, L.maxpool3d_fwd_ex_plan, L.maxpool3d_bwd_ex_plan,
               L.maxpool3d_bwd_recompute, L.maxpool3d_bwd_recompute_plan, L.maxpool3d_fwd_ndhwc,
-              L.adaptive_maxpool3d_fwd_ndhwc, L.maxpool3d_bwd_ndhwc, L.maxpool3d_out_size,
+              L.adaptive_maxpool3d_fwd_ndhwc, L.maxpool3d_bwd_ndhwc, L.maxpool3d_bwd_ndhwc_plan,
+              L.maxpool3d_out_size,
               L.maxpool3d_ex_out_size):
         f.restype = i32
     _lib = L
@@ -385,6 +387,16 @@ def maxpool3d_bwd_plan(in_shape, out_size, kernel, stride, dtype, algo=BWD_AUTO)
     k, s = _window_args(kernel, stride)
     _check(lib().maxpool3d_bwd_plan(*in_shape, *out_size, *k, *s, DTYPE_CODE[dtype], algo,
                                     ctypes.byref(p)), "maxpool3d_bwd_plan")
+    return PATHS[p.value]
+
+
+def maxpool3d_bwd_ndhwc_plan(in_shape, out_size, kernel, stride, dtype) -> str:
+    """Kernel of maxpool3d_bwd_ndhwc for 16-byte aligned buffers; in_shape is
+    (N, C, D, H, W) whatever the layout. kernel/stride None = adaptive."""
+    p = ctypes.c_int(-1)
+    k, s = _window_args(kernel, stride)
+    _check(lib().maxpool3d_bwd_ndhwc_plan(*in_shape, *out_size, *k, *s, DTYPE_CODE[dtype],
+                                          ctypes.byref(p)), "maxpool3d_bwd_ndhwc_plan")
     return PATHS[p.value]
 
 

@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmp3d.so")
-SOURCES = ["api.cu", "fwd.cu", "fwd_roll.cu", "bwd.cu", "bwd_roll.cu", "ndhwc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_roll.cu", "bwd.cu", "bwd_roll.cu", "ndhwc.cu", "ndhwc_roll.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -54,6 +54,7 @@ const char* path_name(int path) {
     case MP3D_PATH_BWD_RECOMPUTE: return "bwd_recompute_direct";
     case MP3D_PATH_FWD_NDHWC: return "fwd_ndhwc";
     case MP3D_PATH_BWD_NDHWC: return "bwd_ndhwc";
+    case MP3D_PATH_BWD_NDHWC_ROLL: return "bwd_ndhwc_roll";
     default: return "?";
     }
 }
@@ -635,11 +636,23 @@ int maxpool3d_bwd_ndhwc(const void* grad_out, const int64_t* idx, void* grad_in,
     if (g.P == 0) return MP3D_OK;
     if (C > INT32_MAX) return MP3D_ERR_SHAPE;
     g.P /= C;
-    log_path("bwd", MP3D_PATH_BWD_NDHWC, g, dtype);
+    log_path("bwd", bwd_ndhwc_path(g, (int)C, dtype, (uintptr_t)grad_in % 16 == 0), g, dtype);
     int sms = 0;
     if (sm_count(&sms) != cudaSuccess) return MP3D_ERR_CUDA;
     return launch_bwd_ndhwc(grad_out, idx, grad_in, g, (int)C, dtype, sms, stream) == cudaSuccess
                ? MP3D_OK : MP3D_ERR_CUDA;
+}
+
+int maxpool3d_bwd_ndhwc_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int od, int oh,
+                             int ow, int kd, int kh, int kw, int sd, int sh, int sw, int dtype,
+                             int* path) {
+    Geo g;
+    int st = bwd_geo(&g, N, C, D, H, W, od, oh, ow, kd, kh, kw, sd, sh, sw, dtype, MP3D_BWD_AUTO);
+    if (st) return st;
+    if (g.P > 0 && C > INT32_MAX) return MP3D_ERR_SHAPE;
+    if (g.P > 0) g.P /= C;
+    if (path) *path = g.P == 0 ? MP3D_PATH_NOOP : bwd_ndhwc_path(g, (int)C, dtype, true);
+    return MP3D_OK;
 }
 
 int mp3d_device_error_flags(unsigned int* flags, int clear) {

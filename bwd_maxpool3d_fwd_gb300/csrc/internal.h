@@ -48,6 +48,15 @@ cudaError_t launch_fwd_ndhwc(const void* x, void* y, int64_t* idx, const Geo& g,
                              int sms, cudaStream_t s);
 cudaError_t launch_bwd_ndhwc(const void* go, const int64_t* idx, void* gi, const Geo& g, int C,
                              int dtype, int sms, cudaStream_t s);
+// The channels-last backward's kernel (MP3D_PATH_BWD_NDHWC_ROLL or
+// MP3D_PATH_BWD_NDHWC); aligned16: grad_in starts on a 16-byte boundary.
+int bwd_ndhwc_path(const Geo& g, int C, int dtype, bool aligned16);
+// The rolling channels-last backward (ndhwc_roll.cu): windows with at most
+// two over any input per axis, C a multiple of its channel group, grad_in
+// 16-byte aligned.
+bool bwd_ndhwc_roll_supported(const Geo& g, int C, int dtype);
+cudaError_t launch_bwd_ndhwc_roll(const void* go, const int64_t* idx, void* gi, const Geo& g, int C,
+                                  int dtype, cudaStream_t s);
 
 // Polls the main pipeline waits of the forward kernels make before giving
 // up (fwd.cu; kWaitLimit unless a test set another value), and its setter

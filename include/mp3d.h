@@ -96,9 +96,11 @@ typedef enum {
     MP3D_PATH_BWD_RECOMPUTE_TILES = 16, /* no stored index, 2x2x2 tiling, fused */
     MP3D_PATH_BWD_RECOMPUTE = 17,    /* no stored index, direct form          */
     MP3D_PATH_BWD_NDHWC = 18,        /* channels-last layout                  */
-    MP3D_PATH_FWD_ROLL = 19          /* 16-bit, depth slices streamed in order,
+    MP3D_PATH_FWD_ROLL = 19,         /* 16-bit, depth slices streamed in order,
                                         windows as unsigned maxima of order
                                         words                                 */
+    MP3D_PATH_BWD_NDHWC_ROLL = 20    /* channels-last, ordered scatter into a
+                                        rolling ring of shared depth slices  */
 } mp3d_path;
 
 /*
@@ -194,7 +196,7 @@ int maxpool3d_bwd_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
  * of maxpool3d_fwd / adaptive_maxpool3d_fwd / maxpool3d_bwd: the results
  * are theirs with the channel axis moved last. Arguments and checks as for
  * those entry points (idx may be NULL in the forwards); the backward takes
- * no algorithm or workspace (gather form). Channel counts that are a
+ * no algorithm or workspace. Channel counts that are a
  * multiple of 16 bytes' worth of elements, on 16-byte aligned buffers, use
  * 16-byte accesses across channels; others take element accesses.
  */
@@ -210,6 +212,16 @@ int maxpool3d_bwd_ndhwc(const void* grad_out, const int64_t* idx, void* grad_in,
                         int od, int oh, int ow,
                         int kd, int kh, int kw, int sd, int sh, int sw,
                         int dtype, cudaStream_t stream);
+/* The kernel maxpool3d_bwd_ndhwc takes for these sizes with 16-byte
+ * aligned buffers: MP3D_PATH_BWD_NDHWC_ROLL (adaptive windows, or fixed
+ * windows overlapping along some axis, with at most two over any input per
+ * axis and C * sizeof(element) a multiple of 16 bytes) or
+ * MP3D_PATH_BWD_NDHWC (gather). Arguments as for maxpool3d_bwd_ndhwc;
+ * *path is written on success. */
+int maxpool3d_bwd_ndhwc_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                             int od, int oh, int ow,
+                             int kd, int kh, int kw, int sd, int sh, int sw,
+                             int dtype, int* path);
 
 /*
  * Backward without stored indices [AMPB]: the same grad_in as

@@ -722,6 +722,53 @@ def test_channels_last(case, dtype, offset):
     assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(), "grad_in (channels last)")
 
 
+# The channels-last rolling backward: tiles of input rows and columns per
+# CTA (several per axis here, with ragged last tiles), several channel
+# groups, windows with two covers per axis (stride 1 included), adaptive
+# windows, a ring as deep as the input (global windows), integer inputs with
+# many ties (windows sharing their chosen input) and signed-zero gradients.
+NDHWC_ROLL_CASES = [
+    ((3, 3, 3), (2, 2, 2), None, (2, 9, 30, 29, 16)),
+    ((3, 3, 3), (2, 2, 2), None, (1, 8, 17, 35, 40)),
+    ((2, 2, 2), (1, 1, 1), None, (1, 6, 20, 18, 8)),
+    ((3, 2, 3), (2, 1, 2), None, (2, 7, 16, 19, 24)),
+    ((3, 3, 2), (2, 2, 2), None, (2, 8, 30, 30, 16)),       # disjoint along w
+    ((2, 1, 2), (1, 1, 1), None, (1, 3, 5, 7, 8)),          # one-element along h
+    (None, None, (4, 11, 10), (1, 10, 30, 29, 16)),
+    (None, None, (3, 7, 9), (2, 9, 20, 33, 8)),
+    (None, None, (1, 1, 1), (2, 4, 6, 5, 16)),
+    ((3, 3, 3), (2, 2, 2), None, (1, 3, 3, 3, 128)),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=str)
+@pytest.mark.parametrize("case", range(len(NDHWC_ROLL_CASES)))
+def test_channels_last_rolling_backward(case, dtype):
+    k, s, out, shape = NDHWC_ROLL_CASES[case]
+    N, D, H, W, C = shape
+    gen = torch.Generator().manual_seed(9900 + case)
+    x = torch.randint(-3, 4, (N, C, D, H, W), generator=gen).to(dtype)     # ties everywhere
+    if k is not None:
+        _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    else:
+        _, i_ref = oracle.adaptive_maxpool3d_fwd(x, out)
+    osz = tuple(i_ref.shape[2:])
+    if case % 2:
+        pick = torch.randint(0, 5, i_ref.shape, generator=gen)
+        g = torch.tensor([-0.0, 0.0, -0.0, 1.0, -1.5])[pick].to(dtype)
+    else:
+        g = torch.randn(i_ref.shape, generator=gen).to(dtype)
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, (D, H, W))
+    assert mp.maxpool3d_bwd_ndhwc_plan((N, C, D, H, W), osz, k, s, dtype) == "bwd_ndhwc_roll"
+    gd = g.permute(0, 2, 3, 4, 1).contiguous().to(DEV)
+    idx = i_ref.permute(0, 2, 3, 4, 1).contiguous().to(DEV)
+    gin = torch.full(shape, float("nan"), dtype=dtype, device=DEV)
+    mp.maxpool3d_bwd_ndhwc(gd, idx, gin, k, s)
+    torch.cuda.synchronize()
+    assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(),
+                      "grad_in (channels-last rolling backward)")
+
+
 # The slab and rolling forwards for 16-bit types rank elements by one
 # unsigned word (value order key, then earliest offset). Arbitrary bit patterns pin that
 # order against the scan's rule: NaNs of either sign and any payload (the

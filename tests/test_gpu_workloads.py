@@ -2,7 +2,8 @@
 benchmark times (needs a GPU), compared with the oracle in full: indices,
 output bits and grad_in bits of every plane. Workload 3 (822M inputs) is
 checked in chunks of planes on a thread pool. The padded workload the
-benchmark also times is compared in full."""
+benchmark also times is compared in full, and workload 3 in the
+channels-last layout on sampled planes."""
 import concurrent.futures as cf
 import os
 
@@ -156,3 +157,48 @@ def test_padded_large_workload_full():
         results = list(ex.map(chunk, bounds))
     bad = [r for r in results if not all(r[1:])]
     assert not bad, f"planes differing from the oracle (first plane of chunk, idx, y, grad_in): {bad[:4]}"
+
+
+def test_workload3_channels_last_sampled():
+    # the k3s2 fp16 workload in the channels-last layout (32 x 16 x 112 x 112
+    # x 128, the same values with the channel axis last) through the
+    # channels-last forward and backward the benchmark times; every (n, c)
+    # plane of the first and last sample and 128 seeded others are compared
+    # with the oracle in full (idx, y bits, grad_in bits)
+    w = workloads.WORKLOADS[3]
+    k, s = w.kernel, w.stride
+    assert mp.maxpool3d_bwd_ndhwc_plan(w.in_shape, w.out, k, s, torch.float16) == "bwd_ndhwc_roll"
+    x, g = workloads.make_x(w), workloads.make_grad_out(w)
+    xl = x.permute(0, 2, 3, 4, 1).contiguous().to(DEV)
+    gl = g.permute(0, 2, 3, 4, 1).contiguous().to(DEV)
+    oshape = (w.N,) + tuple(w.out) + (w.C,)
+    y = torch.empty(oshape, dtype=w.dtype, device=DEV)
+    idx = torch.empty(oshape, dtype=torch.int64, device=DEV)
+    gin = torch.empty_like(xl)
+    mp.maxpool3d_fwd_ndhwc(xl, y, idx, k, s)
+    mp.maxpool3d_bwd_ndhwc(gl, idx, gin, k, s)
+    torch.cuda.synchronize()
+    y, idx, gin = y.cpu(), idx.cpu(), gin.cpu()
+    del xl, gl
+    gen = torch.Generator().manual_seed(20261304)
+    planes = [(0, c) for c in range(w.C)] + [(w.N - 1, c) for c in range(w.C)]
+    planes += [(int(n), int(c)) for n, c in zip(torch.randint(1, w.N - 1, (128,), generator=gen),
+                                                torch.randint(0, w.C, (128,), generator=gen))]
+
+    def chunk(b):
+        sel = planes[b[0]:b[1]]
+        ns = torch.tensor([p[0] for p in sel])
+        cs = torch.tensor([p[1] for p in sel])
+        xs = x[ns, cs].unsqueeze(0)                       # (1, P, D, H, W)
+        gs = g[ns, cs].unsqueeze(0)
+        y_ref, i_ref = oracle.maxpool3d_fwd(xs, k, s)
+        gin_ref = oracle.maxpool3d_bwd(gs, i_ref, (w.D, w.H, w.W))
+        return (b[0], torch.equal(idx[ns, ..., cs], i_ref[0]),
+                torch.equal(bits(y[ns, ..., cs]), bits(y_ref[0])),
+                torch.equal(bits(gin[ns, ..., cs]), bits(gin_ref[0])))
+
+    bounds = [(q, min(q + 32, len(planes))) for q in range(0, len(planes), 32)]
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(chunk, bounds))
+    bad = [r for r in results if not all(r[1:])]
+    assert not bad, f"sampled planes differing from the oracle (first of chunk, idx, y, grad_in): {bad[:4]}"
