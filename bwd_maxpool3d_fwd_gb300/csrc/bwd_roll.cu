@@ -112,6 +112,15 @@ template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float a, fl
     return *reinterpret_cast<const unsigned*>(&h);
 }
 
+// Place of accumulator x of a slice (x counted in floats from the slot's
+// start) in the swizzled order: the two 16-byte halves of 32-byte chunk
+// c = x / 8 trade places when bit 2 of c is set. A thread whose store chunks
+// all have that bit equal to fh then reads its lower halves at float offset
+// 4 * fh of each chunk: the eight chunks of a quarter-warp meet every
+// 16-byte bank group once per access, and the halves arrive in output
+// order. The map is its own inverse.
+__device__ __forceinline__ int roll_swz(int x) { return x ^ ((x >> 3) & 4); }
+
 // One 16-byte output chunk from its accumulators at src (reset to +0).
 // For 16-bit types a chunk is 32 bytes of accumulators, read and cleared as
 // two 16-byte halves. Taken in the same order by every thread, eight
@@ -155,6 +164,9 @@ __global__ void __launch_bounds__(NT, MINB)
 k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
            RollGeo rg) {
     constexpr int VEC = 16 / sizeof(T);
+    // SW: the compiled 3x3x3 form for 16-bit types keeps its accumulators
+    // in the swizzled order of roll_swz
+    constexpr bool SW = K3 && sizeof(T) == 2;
     static_assert(NT % 32 == 0, "the store's chunk c and its thread share lane bits");
     extern __shared__ __align__(16) float ring[];
     const int RS = K3 ? 3 : rg.RS, SSTR = rg.SSTR;
@@ -234,7 +246,8 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
 #pragma unroll
                 for (int t = 0; t < 3; ++t) {
                     const int sl = sbo + t >= 3 ? sbo + t - 3 : sbo + t;
-                    a3[t] = (sl * SSTR - t * HW - h0W) * (int)sizeof(float);
+                    a3[t] = SW ? sl * SSTR * (int)sizeof(float)
+                               : (sl * SSTR - t * HW - h0W) * (int)sizeof(float);
                 }
             }
             // 1. decode this row (key 4: the window adds nothing here);
@@ -260,7 +273,10 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                               (unsigned)loc < (unsigned)L;
                     if constexpr (KP)
                         ok = ok && (unsigned)(int)j < (unsigned)g.vol && (unsigned)(wcol[k] + offw) < (unsigned)W;
-                    off[k] = (d2 ? a3[2] : d1 ? a3[1] : a3[0]) + (wo[k] + rel) * (int)sizeof(float);
+                    if constexpr (SW)
+                        off[k] = (d2 ? a3[2] : d1 ? a3[1] : a3[0]) + roll_swz(loc) * (int)sizeof(float);
+                    else
+                        off[k] = (d2 ? a3[2] : d1 ? a3[1] : a3[0]) + (wo[k] + rel) * (int)sizeof(float);
                     key[k] = ok ? ((h2 ? 0 : 2) | (offw >= 2 ? 0 : 1)) : 4;
                     if (ok && __float_as_uint(gv[k]) == 0x80000000u) {
                         const int a = off[k] >> 2;
@@ -340,8 +356,9 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                             const int b = __ffs(m) - 1;
                             m &= m - 1;
                             float* acc = ring + slot * SSTR + i * 32 + b;
+                            const int x = SW ? roll_swz(i * 32 + b) : i * 32 + b;   // its place in the slice
                             if (__float_as_uint(*acc) == 0u &&
-                                roll_all_negzero<T, AD>(go, idx, p, off0 + i * 32 + b - ph, g, rg))
+                                roll_all_negzero<T, AD>(go, idx, p, off0 + x - ph, g, rg))
                                 *acc = -0.0f;
                         }
                     }
@@ -349,7 +366,33 @@ k_bwd_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restr
                 __syncthreads();
                 if (tid == 0) *slotmask &= ~stored;
             }
-            if constexpr (AL) {
+            if constexpr (SW) {
+                // chunk c's lower half sits at float offset 4 * fh (fh is bit 2
+                // of c for every chunk of this thread), its upper half beside it
+                const int nc = L / VEC;
+                for (int s = 0; s < dn - cs; ++s) {
+                    T* dst = gplane + (cs + s) * HW + h0W;     // on a 16-byte boundary
+                    int slot = sbc + s;
+                    slot -= slot >= RS ? RS : 0;
+                    float* src = ring + slot * SSTR;
+                    const int fo = 4 * fh;
+                    if (s < nring) {
+                        for (int c = tid; c < nc; c += NT) {
+                            float4* lo = reinterpret_cast<float4*>(src + c * VEC + fo);
+                            float4* hi = reinterpret_cast<float4*>(src + c * VEC + (fo ^ 4));
+                            const float4 a = *lo, b = *hi;
+                            *lo = make_float4(0.f, 0.f, 0.f, 0.f);
+                            *hi = make_float4(0.f, 0.f, 0.f, 0.f);
+                            *reinterpret_cast<uint4*>(dst + c * VEC) =
+                                make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y),
+                                           pack2<T>(b.z, b.w));
+                        }
+                    } else {
+                        for (int c = tid; c < nc; c += NT)
+                            *reinterpret_cast<uint4*>(dst + c * VEC) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            } else if constexpr (AL) {
                 for (int s = 0; s < dn - cs; ++s) {
                     T* dst = gplane + (cs + s) * HW + h0W;     // on a 16-byte boundary
                     const bool cov = s < nring;
