@@ -108,26 +108,37 @@ template <> __device__ __forceinline__ unsigned nr_pack2<__nv_bfloat16>(float a,
     return *reinterpret_cast<const unsigned*>(&h);
 }
 
-// One 16-byte output chunk from its accumulators at src, which are reset to
-// +0. For 16-bit types the chunk's accumulators are 32 bytes, read and
-// cleared as two 16-byte halves; threads whose f (bit 2 of the lane) is set
-// take the upper half first, so the eight chunks of a quarter-warp, 32 bytes
-// apart, meet each of the eight 16-byte bank groups once per access.
+// Accumulator x of a slot (floats from the slot's start) sits at nr_swz(x):
+// for 16-bit types the two 16-byte halves of 32-byte chunk c = x / 8 trade
+// places when bit 2 of c is set (the map is its own inverse). A thread's
+// store chunks all have that bit equal to f = bit 2 of its lane, so it reads
+// its lower halves at float offset 4 * f of each chunk and gets the halves
+// in output order, while the eight chunks of a quarter-warp meet each of the
+// eight 16-byte bank groups once per access.
+template <typename T>
+__device__ __forceinline__ int nr_swz(int x) {
+    if constexpr (sizeof(T) == 2) return x ^ ((x >> 3) & 4);
+    else return x;
+}
+
+// One 16-byte output chunk from its accumulators (chunk base src, lane bit
+// f as above), which are reset to +0.
 template <typename T>
 __device__ __forceinline__ uint4 nr_take(float* src, int f) {
-    float4* s4 = reinterpret_cast<float4*>(src);
     if constexpr (sizeof(T) == 4) {
+        float4* s4 = reinterpret_cast<float4*>(src);
         const float4 a = s4[0];
         s4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z),
                           __float_as_uint(a.w));
     } else {
-        const float4 a = s4[f], b = s4[f ^ 1];
-        s4[f] = make_float4(0.f, 0.f, 0.f, 0.f);
-        s4[f ^ 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const unsigned a0 = nr_pack2<T>(a.x, a.y), a1 = nr_pack2<T>(a.z, a.w);
-        const unsigned b0 = nr_pack2<T>(b.x, b.y), b1 = nr_pack2<T>(b.z, b.w);
-        return f ? make_uint4(b0, b1, a0, a1) : make_uint4(a0, a1, b0, b1);
+        float4* lo = reinterpret_cast<float4*>(src + 4 * f);
+        float4* hi = reinterpret_cast<float4*>(src + 4 * (f ^ 1));
+        const float4 a = *lo, b = *hi;
+        *lo = make_float4(0.f, 0.f, 0.f, 0.f);
+        *hi = make_float4(0.f, 0.f, 0.f, 0.f);
+        return make_uint4(nr_pack2<T>(a.x, a.y), nr_pack2<T>(a.z, a.w), nr_pack2<T>(b.x, b.y),
+                          nr_pack2<T>(b.z, b.w));
     }
 }
 
@@ -299,7 +310,7 @@ k_bwd_ndhwc_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* _
                     slot = sbo + offd;
                     slot = (slot >= RS ? slot - RS : slot) * SSTR;
                 }
-                const int off = slot + (lr * TW + lc) * CG + ch;
+                const int off = slot + nr_swz<T>((lr * TW + lc) * CG + ch);
                 kf[k] = ok ? off * 4 + (((offh >= sh ? 0 : 2) | (offw >= sw ? 0 : 1)) << 20) : -1;
                 negm |= (ok && __float_as_uint(gv[k]) == 0x80000000u) ? 1u << k : 0u;
             }
@@ -355,8 +366,8 @@ k_bwd_ndhwc_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* _
                         while (m) {
                             const int b = __ffs(m) - 1;
                             m &= m - 1;
-                            const int x = i * 32 + b;          // float offset in the slot
-                            float* acc = ring + slot * SSTR + x;
+                            float* acc = ring + slot * SSTR + i * 32 + b;
+                            const int x = nr_swz<T>(i * 32 + b);   // its place in the slot's order
                             const int pos = x / CG;
                             const int lr = rg.fTW.div(pos), lc = pos - lr * TW;
                             const int jj = (cs + s) * HW + (h0 + lr) * W + w0 + lc;
@@ -370,17 +381,20 @@ k_bwd_ndhwc_roll(const T* __restrict__ go, const int64_t* __restrict__ idx, T* _
                 if (tid == 0) *slotmask &= ~stored;
             }
             for (int s = 0; s < dn - cs; ++s) {
-                const bool cov = s < nring;
                 int slot = sbc + s;
                 slot -= slot >= RS ? RS : 0;
                 float* src = ring + slot * SSTR + tid * VEC;
                 T* dst = gbase + (long long)(cs + s) * HW * C;
+                if (s < nring) {
 #pragma unroll
-                for (int i = 0; i < kNRollSpt; ++i) {
-                    if (soff[i] < 0) continue;
-                    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-                    if (cov) out = nr_take<T>(src + i * NT * VEC, fh);
-                    *reinterpret_cast<uint4*>(dst + soff[i]) = out;
+                    for (int i = 0; i < kNRollSpt; ++i) {
+                        if (soff[i] < 0) continue;
+                        *reinterpret_cast<uint4*>(dst + soff[i]) = nr_take<T>(src + i * NT * VEC, fh);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kNRollSpt; ++i)
+                        if (soff[i] >= 0) *reinterpret_cast<uint4*>(dst + soff[i]) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             // the next row completes from dn; its slot follows
