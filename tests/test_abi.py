@@ -144,6 +144,23 @@ def test_plans_per_workload(L):
         assert pa == "bwd_atomic"
 
 
+def test_channels_last_backward_plans(L):
+    # the rolling scatter for overlapping or adaptive windows when 16 bytes
+    # of channels divide C; the gather for windows that tile the input, odd
+    # channel counts, and windows with three covers per axis
+    f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
+    plan = mp.maxpool3d_bwd_ndhwc_plan
+    for dt in (f16, bf16, f32):
+        assert plan((32, 128, 16, 112, 112), (7, 55, 55), (3, 3, 3), (2, 2, 2), dt) == "bwd_ndhwc_roll"
+        assert plan((8, 64, 32, 64, 64), (16, 32, 32), (2, 2, 2), (2, 2, 2), dt) == "bwd_ndhwc"
+        assert plan((2, 16, 10, 30, 29), (4, 11, 10), None, None, dt) == "bwd_ndhwc_roll"
+        assert plan((2, 5, 7, 9, 10), (6, 4, 3), (2, 3, 2), (1, 2, 3), dt) == "bwd_ndhwc"   # odd C
+        assert plan((1, 8, 9, 9, 9), (3, 3, 3), (5, 5, 5), (2, 2, 2), dt) == "bwd_ndhwc"    # 3 covers
+    assert plan((1, 12, 8, 17, 35), (3, 8, 17), (3, 3, 3), (2, 2, 2), f32) == "bwd_ndhwc_roll"
+    assert plan((1, 12, 8, 17, 35), (3, 8, 17), (3, 3, 3), (2, 2, 2), f16) == "bwd_ndhwc"
+    assert plan((0, 16, 8, 17, 35), (3, 8, 17), (3, 3, 3), (2, 2, 2), f16) == "noop"
+
+
 def test_plan_rules(L):
     # fixed kernel == input on every axis: a global reduction
     assert mp.maxpool3d_fwd_plan((2, 2, 3, 4, 5), (3, 4, 5), (1, 1, 1), torch.float32) == "fwd_global"

@@ -769,6 +769,28 @@ def test_channels_last_rolling_backward(case, dtype):
                       "grad_in (channels-last rolling backward)")
 
 
+# binary32 channel counts that hold 16 but not 32 bytes of channels: groups
+# of four channels per CTA (half-sector stores)
+@pytest.mark.parametrize("case", [((3, 3, 3), (2, 2, 2), (1, 8, 17, 35, 12)),
+                                  ((2, 2, 2), (1, 1, 1), (2, 5, 9, 11, 4))], ids=["k3s2_c12", "k2s1_c4"])
+def test_channels_last_rolling_backward_groups_of_four(case):
+    k, s, shape = case
+    N, D, H, W, C = shape
+    gen = torch.Generator().manual_seed(9950 + C)
+    x = torch.randint(-3, 4, (N, C, D, H, W), generator=gen).to(torch.float32)
+    _, i_ref = oracle.maxpool3d_fwd(x, k, s)
+    pick = torch.randint(0, 5, i_ref.shape, generator=gen)
+    g = torch.tensor([-0.0, 0.0, -0.0, 1.0, -1.5])[pick]
+    gin_ref = oracle.maxpool3d_bwd(g, i_ref, (D, H, W))
+    assert mp.maxpool3d_bwd_ndhwc_plan((N, C, D, H, W), tuple(i_ref.shape[2:]), k, s,
+                                       torch.float32) == "bwd_ndhwc_roll"
+    gin = torch.full(shape, float("nan"), device=DEV)
+    mp.maxpool3d_bwd_ndhwc(g.permute(0, 2, 3, 4, 1).contiguous().to(DEV),
+                           i_ref.permute(0, 2, 3, 4, 1).contiguous().to(DEV), gin, k, s)
+    torch.cuda.synchronize()
+    assert_bits_equal(gin.cpu(), gin_ref.permute(0, 2, 3, 4, 1).contiguous(), "grad_in (groups of four)")
+
+
 # The slab and rolling forwards for 16-bit types rank elements by one
 # unsigned word (value order key, then earliest offset). Arbitrary bit patterns pin that
 # order against the scan's rule: NaNs of either sign and any payload (the
