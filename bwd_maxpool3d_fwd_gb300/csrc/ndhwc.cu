@@ -200,6 +200,118 @@ k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__
     }
 }
 
+// Forward for 16-bit types, packed, fixed windows whose consecutive depth
+// windows share one slice (KD = SD + 1; 3x3x3 with stride 2, for one): one
+// thread per (n, oh, ow, 16-byte chunk of 8 channels) walks the output
+// depths. Each slice's KH x KW box is reduced once, in (h, w) order, to a
+// best element and its (h, w) offset per lane (a later element replaces only
+// when strictly greater); the slices of a window are then merged in depth
+// order the same way, so the winner is the first maximum in (d, h, w) order.
+// The slice a window shares with the next is reduced once and carried, which
+// saves a third of the loads and one round of load latency per output. NaN
+// and infinities: a running x*0 + acc per window; such chunks are recomputed
+// with the exact scalar scan.
+template <typename T, int KD, int SD, int KH, int KW>
+__global__ void __launch_bounds__(256, 3)
+k_fwd_ndhwc_dw(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C) {
+    static_assert(KD == SD + 1, "consecutive depth windows share one slice");
+    constexpr int VEC = 8;
+    const int nch = C / VEC;
+    const long long total = (long long)g.P * g.OH * g.OW * nch;
+    const int HW = g.H * g.W;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int ch = (int)(t % nch);
+        long long r = t / nch;
+        const int ow = (int)(r % g.OW);
+        r /= g.OW;
+        const int oh = (int)(r % g.OH);
+        const long long n = r / g.OH;
+        const int hs = oh * g.sh, ws = ow * g.sw;
+        const T* xn = x + n * (long long)g.vol * C + ch * VEC;
+        // slice d's box: best element and its (h, w) offset per lane, and a
+        // running x*0 + acc
+        auto slice = [&](int d, uint32_t (&sv)[4], uint32_t (&sc)[4], uint32_t& sp) {
+            const T* plane = xn + ((long long)d * HW + hs * g.W + ws) * C;
+            uint4 u[KH * KW];
+#pragma unroll
+            for (int k = 0; k < KH * KW; ++k)
+                u[k] = __ldg(reinterpret_cast<const uint4*>(plane + ((long long)(k / KW) * g.W + k % KW) * C));
+            sv[0] = u[0].x; sv[1] = u[0].y; sv[2] = u[0].z; sv[3] = u[0].w;
+            sc[0] = sc[1] = sc[2] = sc[3] = 0u;
+            sp = 0u;
+#pragma unroll
+            for (int k = 0; k < KH * KW; ++k) {
+                if (k > 0) {
+                    const uint32_t code = (uint32_t)((k / KW) * g.W + k % KW) * 0x00010001u;
+                    merge2<T>(sv[0], sc[0], u[k].x, code);
+                    merge2<T>(sv[1], sc[1], u[k].y, code);
+                    merge2<T>(sv[2], sc[2], u[k].z, code);
+                    merge2<T>(sv[3], sc[3], u[k].w, code);
+                }
+                sp = Pair<T>::poison(sp, u[k].x);
+                sp = Pair<T>::poison(sp, u[k].y);
+                sp = Pair<T>::poison(sp, u[k].z);
+                sp = Pair<T>::poison(sp, u[k].w);
+            }
+        };
+        uint32_t cv[4], cc[4], cp;           // the carried slice: first slice of window od
+        slice(0, cv, cc, cp);
+        for (int od = 0; od < g.OD; ++od) {
+            const int d0 = od * SD;
+            uint32_t mv[4] = {cv[0], cv[1], cv[2], cv[3]};
+            uint32_t mc[4] = {cc[0], cc[1], cc[2], cc[3]};
+            uint32_t pz = cp;
+#pragma unroll
+            for (int j = 1; j < KD; ++j) {
+                uint32_t sv[4], sc[4], sp;
+                slice(d0 + j, sv, sc, sp);
+                const uint32_t dcode = (uint32_t)(j * HW) * 0x00010001u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) merge2<T>(mv[q], mc[q], sv[q], sc[q] + dcode);
+                pz = Pair<T>::poison(pz, sp);
+                if (j == KD - 1) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        cv[q] = sv[q];
+                        cc[q] = sc[q];
+                    }
+                    cp = sp;
+                }
+            }
+            const int origin = d0 * HW + hs * g.W + ws;
+            const long long o = (((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C + ch * VEC;
+            if (Pair<T>::is_poisoned(pz)) {
+                // exact scalar scan of the chunk's eight channels
+                for (int k = 0; k < VEC; ++k) {
+                    int best = origin;
+                    float m = Elem<T>::to_f(xn[(long long)origin * C + k]);
+                    for (int d = d0; d < d0 + KD; ++d)
+                        for (int h = hs; h < hs + KH; ++h)
+                            for (int w = ws; w < ws + KW; ++w) {
+                                const int sidx = d * HW + h * g.W + w;
+                                const float f = Elem<T>::to_f(xn[(long long)sidx * C + k]);
+                                if (beats(f, m)) {
+                                    m = f;
+                                    best = sidx;
+                                }
+                            }
+                    y[o + k] = xn[(long long)best * C + k];
+                    if (idx) idx[o + k] = best;
+                }
+                continue;
+            }
+            *reinterpret_cast<uint4*>(y + o) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+            if (idx) {
+                int4* id = reinterpret_cast<int4*>(idx + o);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    id[q] = make_int4(origin + (int)(mc[q] & 0xFFFFu), 0, origin + (int)(mc[q] >> 16), 0);
+            }
+        }
+    }
+}
+
 // Backward: one thread per (n, d, h, w, channel chunk); walks the covering
 // windows in ascending (od, oh, ow) order and, per channel, sums the
 // gradients of the windows whose stored index is this position (first
@@ -493,6 +605,13 @@ cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int
                 const int kh = uniform_window_len(g.H, g.OH, g.kh, g.adaptive);
                 const int kw = uniform_window_len(g.W, g.OW, g.kw, g.adaptive);
                 const int k = kh == kw && (kh == 2 || kh == 3) ? kh : 0;
+                // 3x3x3 windows of stride 2 along d: walk the output depths
+                if (!g.adaptive && g.kd == 3 && g.sd == 2 && k == 3) {
+                    const long long walkers = (long long)g.P * g.OH * g.OW * (C / VEC);
+                    k_fwd_ndhwc_dw<T, 3, 2, 3, 3><<<grid_of(walkers, sms), 256, 0, s>>>((const T*)x, (T*)y, idx,
+                                                                                     g, C);
+                    return cudaGetLastError();
+                }
                 auto kern = g.adaptive ? (k == 2 ? k_fwd_ndhwc_pk<T, true, 2, 2>
                                           : k == 3 ? k_fwd_ndhwc_pk<T, true, 3, 3> : k_fwd_ndhwc_pk<T, true, 0, 0>)
                                        : (k == 2 ? k_fwd_ndhwc_pk<T, false, 2, 2>
