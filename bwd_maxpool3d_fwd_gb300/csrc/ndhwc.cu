@@ -312,6 +312,56 @@ k_fwd_ndhwc_dw(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__
     }
 }
 
+// Backward for fixed windows that tile the input exactly (K = S on every
+// axis, each size a multiple of its window): every input lies in exactly
+// one window, so its gradient is that window's gradient where the stored
+// index names it and +0 elsewhere (a sum of one term is the term, -0
+// included). One thread per (window, 16-byte chunk of channels) loads the
+// chunk's gradients and indices once and writes the window's KD*KH*KW
+// positions of the chunk with 16-byte stores.
+template <typename T, int KD, int KH, int KW>
+__global__ void __launch_bounds__(256)
+k_bwd_ndhwc_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
+                 int C) {
+    constexpr int VEC = 16 / sizeof(T);
+    const int nch = C / VEC;
+    const long long total = (long long)g.P * g.ovol * nch;   // g.P = N here
+    const int HW = g.H * g.W;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int ch = (int)(t % nch);
+        long long r = t / nch;
+        const int ow = (int)(r % g.OW);
+        r /= g.OW;
+        const int oh = (int)(r % g.OH);
+        r /= g.OH;
+        const int od = (int)(r % g.OD);
+        const long long n = r / g.OD;
+        const long long o = (((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C + ch * VEC;
+        Vec16<T> gv;
+        gv.u = *reinterpret_cast<const uint4*>(go + o);
+        // the indices' low words; an index with a nonzero high word names no
+        // position (all ones never equals an in-plane offset)
+        unsigned lo[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC / 2; ++q) {
+            const uint4 iv = __ldg(reinterpret_cast<const uint4*>(idx + o + 2 * q));
+            lo[2 * q] = iv.y == 0u ? iv.x : 0xFFFFFFFFu;
+            lo[2 * q + 1] = iv.w == 0u ? iv.z : 0xFFFFFFFFu;
+        }
+        const int origin = (od * KD) * HW + (oh * KH) * g.W + ow * KW;
+        T* gn = gi + n * (long long)g.vol * C + ch * VEC;
+#pragma unroll
+        for (int p = 0; p < KD * KH * KW; ++p) {
+            const int off = origin + (p / (KH * KW)) * HW + ((p / KW) % KH) * g.W + p % KW;
+            Vec16<T> out;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) out.e[k] = lo[k] == (unsigned)off ? gv.e[k] : Elem<T>::from_f(0.0f);
+            *reinterpret_cast<uint4*>(gn + (long long)off * C) = out.u;
+        }
+    }
+}
+
 // Backward: one thread per (n, d, h, w, channel chunk); walks the covering
 // windows in ascending (od, oh, ow) order and, per channel, sums the
 // gradients of the windows whose stored index is this position (first
@@ -639,6 +689,13 @@ template <typename T>
 cudaError_t bwd_dispatch(const void* go, const int64_t* idx, void* gi, const Geo& g, int C, int sms,
                          cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
+    // 2x2x2 windows tiling the input: each input in exactly one window
+    if (!g.adaptive && g.kd == 2 && g.kh == 2 && g.kw == 2 && g.sd == 2 && g.sh == 2 && g.sw == 2 &&
+        g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW && chunked(C, sizeof(T), {go, idx, gi})) {
+        const long long work = (long long)g.P * g.ovol * (C / VEC);
+        k_bwd_ndhwc_tile<T, 2, 2, 2><<<grid_of(work, sms), 256, 0, s>>>((const T*)go, idx, (T*)gi, g, C);
+        return cudaGetLastError();
+    }
     if (blk_ok(g, C, sizeof(T), go, idx, gi)) {
         const long long work = (long long)g.P * ((g.D + 3) / 4) * ((g.H + 3) / 4) * ((g.W + 3) / 4) * 8 *
                                (C / BLK_CH);

@@ -216,7 +216,8 @@ int maxpool3d_bwd_ndhwc(const void* grad_out, const int64_t* idx, void* grad_in,
  * aligned buffers: MP3D_PATH_BWD_NDHWC_ROLL (adaptive windows, or fixed
  * windows overlapping along some axis, with at most two over any input per
  * axis and C * sizeof(element) a multiple of 16 bytes) or
- * MP3D_PATH_BWD_NDHWC (gather). Arguments as for maxpool3d_bwd_ndhwc;
+ * MP3D_PATH_BWD_NDHWC (the rest: direct writes for 2x2x2 windows that tile
+ * the input, gathers otherwise). Arguments as for maxpool3d_bwd_ndhwc;
  * *path is written on success. */
 int maxpool3d_bwd_ndhwc_plan(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                              int od, int oh, int ow,
