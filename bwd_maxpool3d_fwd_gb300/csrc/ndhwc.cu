@@ -10,12 +10,19 @@
 // 16-byte load across channels, and neighbouring threads read neighbouring
 // chunks (coalesced). Channel counts that are not a multiple of VEC, or
 // buffers off a 16-byte boundary, take the same kernels with VEC = 1.
+#include <climits>
 #include <cstring>
 
 #include "internal.h"
 #include "mp3d.h"
 
 namespace mp3d {
+
+// Divisors of a work index t = (((n * OD + od) * OH + oh) * OW + ow) * nch + ch
+// (multiply-shift division; the launchers keep t below 2^31).
+struct NdDecomp {
+    FastDiv fc, fw, fh, fd;
+};
 
 // Forward: one thread per (n, od, oh, ow, channel chunk); scans the window
 // positions in ascending (d, h, w) order, per channel keeping the first
@@ -108,21 +115,24 @@ k_fwd_ndhwc(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ id
 // are issued together before they are merged (in order).
 template <typename T, bool ADAPTIVE, int KH, int KW>
 __global__ void __launch_bounds__(256, 4)
-k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C) {
+k_fwd_ndhwc_pk(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int C,
+               NdDecomp dc) {
     constexpr int VEC = 8;
     const int nch = C / VEC;
-    const long long total = (long long)g.P * g.ovol * nch;
+    const int total = (int)(g.P * g.ovol * nch);
     const int HW = g.H * g.W;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int ch = (int)(t % nch);
-        long long r = t / nch;
-        const int ow = (int)(r % g.OW);
-        r /= g.OW;
-        const int oh = (int)(r % g.OH);
-        r /= g.OH;
-        const int od = (int)(r % g.OD);
-        const long long n = r / g.OD;
+    for (long long tt = blockIdx.x * (long long)blockDim.x + threadIdx.x; tt < total;
+         tt += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)tt;
+        int r = dc.fc.div(t);
+        const int ch = t - r * nch;
+        int r2 = dc.fw.div(r);
+        const int ow = r - r2 * g.OW;
+        r = dc.fh.div(r2);
+        const int oh = r2 - r * g.OH;
+        const int nn = dc.fd.div(r);
+        const int od = r - nn * g.OD;
+        const long long n = nn;
         const int ds = win_start(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
         const int de = win_end(od, g.D, g.OD, g.kd, g.sd, ADAPTIVE);
         const int hs = win_start(oh, g.H, g.OH, g.kh, g.sh, ADAPTIVE);
@@ -322,21 +332,23 @@ k_fwd_ndhwc_dw(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__
 template <typename T, int KD, int KH, int KW>
 __global__ void __launch_bounds__(256)
 k_bwd_ndhwc_tile(const T* __restrict__ go, const int64_t* __restrict__ idx, T* __restrict__ gi, Geo g,
-                 int C) {
+                 int C, NdDecomp dc) {
     constexpr int VEC = 16 / sizeof(T);
     const int nch = C / VEC;
-    const long long total = (long long)g.P * g.ovol * nch;   // g.P = N here
+    const int total = (int)(g.P * g.ovol * nch);   // g.P = N here
     const int HW = g.H * g.W;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int ch = (int)(t % nch);
-        long long r = t / nch;
-        const int ow = (int)(r % g.OW);
-        r /= g.OW;
-        const int oh = (int)(r % g.OH);
-        r /= g.OH;
-        const int od = (int)(r % g.OD);
-        const long long n = r / g.OD;
+    for (long long tt = blockIdx.x * (long long)blockDim.x + threadIdx.x; tt < total;
+         tt += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)tt;
+        int r = dc.fc.div(t);
+        const int ch = t - r * nch;
+        int r2 = dc.fw.div(r);
+        const int ow = r - r2 * g.OW;
+        r = dc.fh.div(r2);
+        const int oh = r2 - r * g.OH;
+        const int nn = dc.fd.div(r);
+        const int od = r - nn * g.OD;
+        const long long n = nn;
         const long long o = (((n * g.OD + od) * g.OH + oh) * (long long)g.OW + ow) * C + ch * VEC;
         Vec16<T> gv;
         gv.u = *reinterpret_cast<const uint4*>(go + o);
@@ -643,13 +655,23 @@ bool rel_fits(const Geo& g) {
     return (kd - 1) * g.H * g.W + (kh - 1) * g.W + (kw - 1) < 65536;
 }
 
+NdDecomp nd_decomp(const Geo& g, int nch) {
+    NdDecomp d;
+    d.fc = FastDiv((uint32_t)nch);
+    d.fw = FastDiv((uint32_t)g.OW);
+    d.fh = FastDiv((uint32_t)g.OH);
+    d.fd = FastDiv((uint32_t)g.OD);
+    return d;
+}
+
 template <typename T>
 cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int C, int sms,
                          cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     if (chunked(C, sizeof(T), {x, y, idx})) {
         if constexpr (sizeof(T) == 2) {
-            if (rel_fits(g)) {
+            if (rel_fits(g) && (long long)g.P * g.ovol * (C / VEC) < INT_MAX) {
+                const NdDecomp dc = nd_decomp(g, C / VEC);
                 const long long work = (long long)g.P * g.ovol * (C / VEC);
                 // uniform (h, w) window extents 2 or 3: the unrolled form
                 const int kh = uniform_window_len(g.H, g.OH, g.kh, g.adaptive);
@@ -666,7 +688,7 @@ cudaError_t fwd_dispatch(const void* x, void* y, int64_t* idx, const Geo& g, int
                                           : k == 3 ? k_fwd_ndhwc_pk<T, true, 3, 3> : k_fwd_ndhwc_pk<T, true, 0, 0>)
                                        : (k == 2 ? k_fwd_ndhwc_pk<T, false, 2, 2>
                                           : k == 3 ? k_fwd_ndhwc_pk<T, false, 3, 3> : k_fwd_ndhwc_pk<T, false, 0, 0>);
-                kern<<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C);
+                kern<<<grid_of(work, sms), 256, 0, s>>>((const T*)x, (T*)y, idx, g, C, dc);
                 return cudaGetLastError();
             }
         }
@@ -691,9 +713,11 @@ cudaError_t bwd_dispatch(const void* go, const int64_t* idx, void* gi, const Geo
     constexpr int VEC = 16 / sizeof(T);
     // 2x2x2 windows tiling the input: each input in exactly one window
     if (!g.adaptive && g.kd == 2 && g.kh == 2 && g.kw == 2 && g.sd == 2 && g.sh == 2 && g.sw == 2 &&
-        g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW && chunked(C, sizeof(T), {go, idx, gi})) {
+        g.D == 2 * g.OD && g.H == 2 * g.OH && g.W == 2 * g.OW && chunked(C, sizeof(T), {go, idx, gi}) &&
+        (long long)g.P * g.ovol * (C / VEC) < INT_MAX) {
         const long long work = (long long)g.P * g.ovol * (C / VEC);
-        k_bwd_ndhwc_tile<T, 2, 2, 2><<<grid_of(work, sms), 256, 0, s>>>((const T*)go, idx, (T*)gi, g, C);
+        k_bwd_ndhwc_tile<T, 2, 2, 2><<<grid_of(work, sms), 256, 0, s>>>((const T*)go, idx, (T*)gi, g, C,
+                                                                     nd_decomp(g, C / VEC));
         return cudaGetLastError();
     }
     if (blk_ok(g, C, sizeof(T), go, idx, gi)) {
