@@ -674,6 +674,8 @@ NDHWC_CASES = [
     ((2, 2, 2), (2, 2, 2), None, (2, 6, 8, 10, 24)),
     ((3, 2, 3), (2, 2, 1), None, (1, 8, 7, 9, 32)),
     (None, None, (3, 4, 5), (2, 6, 9, 10, 8)),              # adaptive, special values
+    ((3, 3, 3), (2, 1, 1), None, (1, 7, 8, 9, 16)),         # depth walk, stride 1 in (h, w)
+    ((3, 3, 3), (2, 3, 3), None, (2, 9, 10, 11, 24)),       # depth walk, disjoint in (h, w)
 ]
 
 
