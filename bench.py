@@ -246,18 +246,9 @@ def l2_flush(buf):
     buf[n:].amax()
 
 
-def launch_mean(ts):
-    """Mean of per-launch event times (ms), leaving out launches that took
-    more than twice the median (a disturbed launch). CUDA events on this GPU
-    resolve 2.048 us, so one launch's time is a multiple of that; the mean
-    over launches that start at random phases of the timer is not."""
-    med = statistics.median(ts)
-    return statistics.mean(t for t in ts if t <= 2 * med)
-
-
 def time_per_kernel(r, iters, warmup, flush):
-    """Mean fwd and bwd device times (ms, launch_mean), each launch preceded
-    by an L2 flush, CUDA events on the launching stream."""
+    """Median fwd and bwd device times (ms), each launch preceded by an L2
+    flush, CUDA events on the launching stream."""
     stream = torch.cuda.current_stream()
     fb = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=r.dev) if flush else None
     for _ in range(warmup):
@@ -275,12 +266,11 @@ def time_per_kernel(r, iters, warmup, flush):
             b.record(stream)
             b.synchronize()
             out.append(a.elapsed_time(b))
-    return launch_mean(tf), launch_mean(tb)
+    return statistics.median(tf), statistics.median(tb)
 
 
 def time_one(fn, dev, iters, flush):
-    """Mean device time (ms, launch_mean) of fn, each launch preceded by an
-    L2 flush."""
+    """Median device time (ms) of fn, each launch preceded by an L2 flush."""
     stream = torch.cuda.current_stream()
     fb = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     for _ in range(3):
@@ -296,7 +286,7 @@ def time_one(fn, dev, iters, flush):
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    return launch_mean(ts)
+    return statistics.median(ts)
 
 
 # Sources each kernel's traffic record depends on (the kernel's file and the
@@ -537,17 +527,17 @@ def e2e(r, x_cpu, g_cpu, steps=8, warmup=2):
 # ---------------------------------------------------------------- main arm
 
 def per_config(dev, peak):
-    """Each workload's forward and backward timed alone (mean of 30 launches, L2
+    """Each workload's forward and backward timed alone (median of 20, L2
     flushed before every launch), as GB/s and fraction of the HBM peak."""
     out = {}
     for n, w in enumerate(workloads.WORKLOADS):
         r = Runner(w, workloads.make_x(w), workloads.make_grad_out(w), dev)
-        tf, tb = time_per_kernel(r, iters=30, warmup=3, flush=True)
+        tf, tb = time_per_kernel(r, iters=20, warmup=3, flush=True)
         fb, bb = algorithmic_bytes(w)
         pf, pb = r.paths()
         fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
         # values-only forward: the same minus the int64 index writes
-        tv = time_one(r.fwd_values, dev, iters=30, flush=True)
+        tv = time_one(r.fwd_values, dev, iters=20, flush=True)
         vb = fb - w.planes * w.out[0] * w.out[1] * w.out[2] * 8
         vg = vb / (tv * 1e-3) / 1e9
         # backward without stored indices: timed where the fused 2x2x2 kernel
@@ -556,7 +546,7 @@ def per_config(dev, peak):
         if w.mode == "fixed" and r.mp.maxpool3d_bwd_recompute_plan(
                 w.in_shape, w.out, w.kernel, w.stride, w.dtype) == "bwd_recompute_k2s2":
             tr = time_one(lambda: r.mp.maxpool3d_bwd_recompute(r.x, r.g, r.gin, w.kernel, w.stride),
-                          dev, iters=30, flush=True)
+                          dev, iters=20, flush=True)
             rb = w.planes * (w.D * w.H * w.W * w.elem_bytes * 2 + w.out[0] * w.out[1] * w.out[2] *
                              w.elem_bytes)
             rg = rb / (tr * 1e-3) / 1e9
@@ -589,7 +579,7 @@ PADDED_LARGE = {"name": "padded_k3s2p1_f16_32x128x16x112x112", "shape": (32, 128
 
 
 def padded_config(dev, peak, c=PADDED):
-    """A padded workload's forward and backward timed alone (mean of 30 launches,
+    """A padded workload's forward and backward timed alone (median of 20,
     L2 flushed before every launch). Inputs are drawn on the device (seeded)."""
     import bwd_maxpool3d_fwd_gb300 as mp
     gen = torch.Generator(device=dev).manual_seed(c["seed"])
@@ -602,8 +592,8 @@ def padded_config(dev, peak, c=PADDED):
     gin = torch.empty(c["shape"], dtype=torch.float16, device=dev)
     fwd = lambda: mp.maxpool3d_fwd_ex(x, y, idx, c["k"], c["s"], c["p"], c["dl"])
     bwd = lambda: mp.maxpool3d_bwd_ex(g, idx, gin, c["k"], c["s"], c["p"], c["dl"])
-    tf = time_one(fwd, dev, iters=30, flush=True)
-    tb = time_one(bwd, dev, iters=30, flush=True)
+    tf = time_one(fwd, dev, iters=20, flush=True)
+    tb = time_one(bwd, dev, iters=20, flush=True)
     nin, nout = x.numel(), y.numel()
     fb, bb = nin * 2 + nout * (2 + 8), nout * (2 + 8) + nin * 2
     fg, bg = fb / (tf * 1e-3) / 1e9, bb / (tb * 1e-3) / 1e9
@@ -619,7 +609,7 @@ def padded_config(dev, peak, c=PADDED):
 def ndhwc_configs(dev, peak):
     """The k2s2 and k3s2 workloads in the channels-last layout (the same
     values with the channel axis moved last): forward and backward timed
-    alone (mean of 30 launches, L2 flushed before every launch)."""
+    alone (median of 20, L2 flushed before every launch)."""
     import bwd_maxpool3d_fwd_gb300 as mp
     out = {}
     for w in workloads.WORKLOADS:
