@@ -7,6 +7,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "internal.h"
 #include "mp3d.h"
@@ -338,6 +341,27 @@ int bwd_ex_geo(Geo* g, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, in
 }  // namespace
 
 namespace mp3d {
+
+int resident_ctas(const void* kern, int block, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    const auto key = std::make_tuple(dev, kern, block, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block, smem) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();   // the launch reports its own errors
+        n = 1;
+    }
+    cache.emplace(key, n);
+    return n;
+}
 
 // Geometry of a backward call (maxpool3d_bwd's checks of sizes, window,
 // dtype and algorithm).

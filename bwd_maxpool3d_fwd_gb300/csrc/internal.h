@@ -10,6 +10,24 @@
 
 namespace mp3d {
 
+// CTAs of `block` threads with `smem` bytes of dynamic shared memory that one
+// SM of the current device keeps resident for kernel `kern` (api.cu; the
+// occupancy query is made once per device and kernel; 1 if it fails).
+int resident_ctas(const void* kern, int block, size_t smem);
+
+// Blocks of 256 threads for a grid-stride loop over `work` threads: at most
+// one wave of the CTAs that kern keeps resident on each SM. Not a general
+// rule: the warp-per-plane global-window kernels ran faster with a partial
+// second wave (its CTAs start as others end, which keeps more planes'
+// first loads in flight), so each launch takes the grid measured best for it.
+template <typename K>
+inline int stride_grid(K kern, long long work, int sms) {
+    long long b = (work + 255) / 256;
+    const long long cap = (long long)sms * resident_ctas(reinterpret_cast<const void*>(kern), 256, 0);
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
 // Argument checks of a backward call (api.cu), before any CUDA call:
 // sizes, window, dtype and algorithm into *g; then the buffers (NULL,
 // alignment, overlap, and the workspace when algo needs one).
