@@ -979,7 +979,7 @@ static cudaError_t bwd_disjoint_t(const void* go, const int64_t* idx, void* gi, 
     const bool aligned = (uintptr_t)gi % 16 == 0;
     const bool plane_vec = aligned && ((long long)g.vol * sizeof(T)) % 16 == 0;
     if (g.ovol == 1 && g.kd == g.D && g.kh == g.H && g.kw == g.W) {
-        const int grid = grid_for(g.P * 32, 256, sms, 8);
+        const int grid = grid_for(g.P * 32, 256, sms, kGlobalCtasPerSm);
         if (plane_vec)
             k_bwd_global<T, VEC><<<grid, 256, 0, s>>>((const T*)go, idx, (T*)gi, g.P, g.vol);
         else

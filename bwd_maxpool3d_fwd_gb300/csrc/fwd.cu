@@ -494,7 +494,7 @@ static cudaError_t fwd_global_t(const void* x, void* y, int64_t* idx, const Geo&
                                 cudaStream_t s) {
     constexpr int VEC = 16 / sizeof(T);
     const bool vec_ok = ((uintptr_t)x % 16 == 0) && (((long long)g.vol * sizeof(T)) % 16 == 0);
-    const int grid = grid_for(g.P * 32, 256, sms, 8);
+    const int grid = grid_for(g.P * 32, 256, sms, kGlobalCtasPerSm);
     if (vec_ok)
         k_fwd_global<T, VEC><<<grid, 256, 0, s>>>((const T*)x, (T*)y, idx, g.P, g.vol);
     else

@@ -17,9 +17,9 @@ int resident_ctas(const void* kern, int block, size_t smem);
 
 // Blocks of 256 threads for a grid-stride loop over `work` threads: at most
 // one wave of the CTAs that kern keeps resident on each SM. Not a general
-// rule: the warp-per-plane global-window kernels ran faster with a partial
-// second wave (its CTAs start as others end, which keeps more planes'
-// first loads in flight), so each launch takes the grid measured best for it.
+// rule (the warp-per-plane global-window kernels run fastest with a CTA per
+// eight planes and no stride, kGlobalCtasPerSm below), so each launch takes
+// the grid measured best for it.
 template <typename K>
 inline int stride_grid(K kern, long long work, int sms) {
     long long b = (work + 255) / 256;
@@ -27,6 +27,15 @@ inline int stride_grid(K kern, long long work, int sms) {
     if (b > cap) b = cap;
     return (int)(b < 1 ? 1 : b);
 }
+
+// Grid cap of the warp-per-plane global-window kernels (k_fwd_global,
+// k_bwd_global), in 256-thread CTAs per SM: high enough that each warp
+// takes one plane (a CTA starts as another ends, so the planes' first loads
+// overlap other planes' work), where a stride of eight CTAs per SM made each
+// warp's planes wait on their loads one after another (on the
+// 64x512x8x14x14 fp32 global pool: forward 45.1 -> 43.0 us, backward
+// 32.8 -> 30.7 us); a grid-stride loop only for more planes than that.
+constexpr int kGlobalCtasPerSm = 4096;
 
 // Argument checks of a backward call (api.cu), before any CUDA call:
 // sizes, window, dtype and algorithm into *g; then the buffers (NULL,
