@@ -750,18 +750,21 @@ cudaError_t roll_t(const void* go, const int64_t* idx, void* gi, const Geo& g, i
     RollGeo rg;
     size_t smem = 0;
     int wpt = 0;
-    // one wave of CTAs at minb per SM
+    // h-tiles split further only while the planes give fewer than half a
+    // wave of CTAs at minb per SM: splitting to reach a whole wave left a
+    // partial second one (the padded 8x64x16x56x56 fp16 backward: 1536
+    // CTAs 34.8 us, 1024 CTAs 26.6 us, 2560 CTAs 45.1 us)
     const bool k3 = !g.adaptive && g.kd == 3 && g.kh == 3 && g.kw == 3 && g.sd == 2 && g.sh == 2 &&
                     g.sw == 2 && g.pd <= 1 && g.ph <= 1 && g.pw <= 1 && g.W % VEC == 0 &&
                     g.vol % VEC == 0;
     // padded, or ceil-mode sizes: windows reach past the input
     const bool reach = g.pd || g.ph || g.pw || g.OD != (g.D - 3) / 2 + 1 || g.OH != (g.H - 3) / 2 + 1 ||
                        g.OW != (g.W - 3) / 2 + 1;
-    if (k3 && roll_plan(g, sizeof(T), 1LL * sms * kRollCfgK3.minb, kRollCfgK3, &rg, &smem, &wpt) &&
+    if (k3 && roll_plan(g, sizeof(T), 1LL * sms * kRollCfgK3.minb / 2, kRollCfgK3, &rg, &smem, &wpt) &&
         wpt == 4)
         return reach ? roll_launch<T, false, 4, true, true, true>(go, idx, gi, g, rg, smem, s)
                      : roll_launch<T, false, 4, true, true, false>(go, idx, gi, g, rg, smem, s);
-    if (!roll_plan(g, sizeof(T), 1LL * sms * kRollCfg.minb, kRollCfg, &rg, &smem, &wpt))
+    if (!roll_plan(g, sizeof(T), 1LL * sms * kRollCfg.minb / 2, kRollCfg, &rg, &smem, &wpt))
         return cudaErrorNotSupported;
     if (g.adaptive && g.vol >= 16LL * g.ovol) {
         // adaptive windows with many inputs each: the exchange store (the
