@@ -569,7 +569,8 @@ int set_pipeline_wait_limit(int polls) {
 // such a duplicate is either the same element as a candidate met earlier,
 // or comes first and bears the code of the real element that follows it,
 // so ties still go to the first real occurrence and padding is never chosen.
-template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS, int PADC = 0>
+template <typename T, int KD, int SD, int KH, int SH, int KW, int TOH, int NS, int PADC = 0,
+          bool VO = false>
 __global__ void __launch_bounds__(128, PADC ? 4 : 5)
 k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g, int odg,
          int nq, int G, int nbands, int nc, int wait_limit) {
@@ -657,7 +658,7 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
             const int oh = oh0 + j;
             const long long o0 = ((p * g.OD + od) * g.OH + oh) * (long long)g.OW + ow0;
             uint16_t* yo = reinterpret_cast<uint16_t*>(y) + o0;
-            int64_t* io = idx ? idx + o0 : nullptr;
+            int64_t* io = !VO && idx ? idx + o0 : nullptr;   // VO: values only
             // in-plane offsets (below 2^31) of the four winners
             int off[4];
             uint32_t yw[2] = {v[j][0], v[j][1]};
@@ -978,7 +979,7 @@ bool fwd_s2_supported(const Geo& g, int dtype, bool aligned16) {
     return true;
 }
 
-template <typename T, int KD, int SD, int KH, int SH, int KW, int PADC = 0>
+template <typename T, int KD, int SD, int KH, int SH, int KW, int PADC = 0, bool VO = false>
 static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, int sms,
                             cudaStream_t s) {
     constexpr int TOH = 4, NS = 2;
@@ -1002,7 +1003,7 @@ static cudaError_t fwd_s2_t(const void* x, void* y, int64_t* idx, const Geo& g, 
     const int band_rows = (G * TOH - 1) * SH + KH;
     const size_t stage = ((size_t)band_rows * g.W * sizeof(T) + 127) / 128 * 128;
     const size_t smem = NS * stage + NS * 8;
-    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS, PADC>;
+    auto kern = k_fwd_s2<T, KD, SD, KH, SH, KW, TOH, NS, PADC, VO>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long blocks = g.P * nq * nbands;
@@ -1033,9 +1034,15 @@ static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const G
                                            FastDiv((uint32_t)g.OH));
         return cudaGetLastError();
     }
-    switch (s2_variant(g)) {
+    // values only (no index output): compiled without the winners' codes,
+    // which the packed merges otherwise carry in a second word
+    const int v = s2_variant(g);
+    if (v < 0) return cudaErrorNotSupported;
+    switch (v + (idx ? 0 : 2)) {
     case 0: return fwd_s2_t<T, 2, 2, 2, 2, 2>(x, y, idx, g, sms, s);
     case 1: return fwd_s2_t<T, 3, 2, 3, 2, 3>(x, y, idx, g, sms, s);
+    case 2: return fwd_s2_t<T, 2, 2, 2, 2, 2, 0, true>(x, y, idx, g, sms, s);
+    case 3: return fwd_s2_t<T, 3, 2, 3, 2, 3, 0, true>(x, y, idx, g, sms, s);
     default: return cudaErrorNotSupported;
     }
 }

@@ -451,6 +451,7 @@ VALUES_ONLY = [
     ("fwd_s2", (3, 3, 3), (2, 2, 2), None, (1, 2, 9, 20, 48), torch.float16),
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 8, 6, 32), torch.bfloat16),    # 2x2x2 tiling
     ("fwd_s2", (2, 2, 2), (2, 2, 2), None, (1, 2, 9, 7, 32), torch.float16),
+    ("fwd_s2", (3, 3, 3), (2, 2, 2), None, (2, 3, 11, 24, 64), torch.bfloat16),
     ("fwd_slab", None, None, (5, 4, 8), (2, 2, 9, 7, 13), torch.float32),
     ("fwd_roll", None, None, (8, 12, 12), (1, 3, 30, 50, 50), torch.float16),
     ("fwd_roll", None, None, (3, 4, 5), (2, 3, 7, 9, 13), torch.bfloat16),

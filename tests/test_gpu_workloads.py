@@ -90,6 +90,12 @@ def test_workload3_full():
         results = list(ex.map(lambda b: _oracle_chunk_matches(w, x, g, y, idx, gin, *b), bounds))
     bad = [r for r in results if not all(r[1:])]
     assert not bad, f"planes differing from the oracle (first plane of chunk, idx, y, grad_in): {bad[:4]}"
+    # values only (idx NULL, compiled without the winners' codes): the same y
+    # bits as the forward with indices, on every plane
+    yv = torch.empty(w.out_shape, dtype=w.dtype, device=DEV)
+    mp.maxpool3d_fwd(x.to(DEV), yv, None, w.kernel, w.stride)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(yv.cpu()), bits(y))
     # the tie injection produced windows whose maximum occurs more than once
     planes = [0, 1, 2047, 4095]
     xs = x.reshape(w.planes, w.D, w.H, w.W)[planes].float()
