@@ -865,7 +865,7 @@ k_fwd_s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, 
 // store of the four maxima and two 16-byte stores of their indices. When a
 // NaN or an infinity was loaded, the four windows are rescanned exactly from
 // the loaded rows with the scalar rule.
-template <typename T>
+template <typename T, bool VO = false>
 __global__ void __launch_bounds__(256)
 k_fwd_k2s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx, Geo g,
            FastDiv fSpr, FastDiv fOH) {
@@ -949,7 +949,7 @@ k_fwd_k2s2(const T* __restrict__ x, T* __restrict__ y, int64_t* __restrict__ idx
                 }
             }
             *reinterpret_cast<uint2*>(y + o0) = yv;
-            if (idx) {
+            if (!VO && idx) {   // VO: values only, the codes are never used
                 int4* id = reinterpret_cast<int4*>(idx + o0);
                 id[0] = make_int4((int)iv[0], (int)(iv[0] >> 32), (int)iv[1], (int)(iv[1] >> 32));
                 id[1] = make_int4((int)iv[2], (int)(iv[2] >> 32), (int)iv[3], (int)(iv[3] >> 32));
@@ -1030,8 +1030,9 @@ static cudaError_t fwd_s2_dispatch(const void* x, void* y, int64_t* idx, const G
         g.OW % 4 == 0 && (uintptr_t)y % 8 == 0 && (uintptr_t)idx % 16 == 0) {
         const int nseg = g.ovol / 4;
         dim3 grid((unsigned)((nseg + 255) / 256), (unsigned)(g.P < 65535 ? g.P : 65535));
-        k_fwd_k2s2<T><<<grid, 256, 0, s>>>((const T*)x, (T*)y, idx, g, FastDiv((uint32_t)(g.OW / 4)),
-                                           FastDiv((uint32_t)g.OH));
+        auto kern = idx ? k_fwd_k2s2<T, false> : k_fwd_k2s2<T, true>;
+        kern<<<grid, 256, 0, s>>>((const T*)x, (T*)y, idx, g, FastDiv((uint32_t)(g.OW / 4)),
+                                  FastDiv((uint32_t)g.OH));
         return cudaGetLastError();
     }
     // values only (no index output): compiled without the winners' codes,
